@@ -1,0 +1,197 @@
+/*
+ * mfsdp.h -- C ABI of the owner-local optimizer step of MatrixFSDP on one GPU.
+ *
+ * Source: "MatrixFSDP: Communication-Free Matrix Optimizers Under ZeRO-3
+ * Parameter Sharding" (Gao, Xu, Zhang; arXiv 2607.05895).  Abstract: for each
+ * 2D weight one data-parallel rank owns the whole matrix and the other ranks
+ * hold empty shards; non-matrix tensors are packed into tail owners and stay
+ * on AdamW; the reduced gradient lands whole on its owner, so Muon's momentum
+ * and Newton-Schulz run locally; the runtime carries the plan in MatrixShard
+ * metadata produced by a balance-aware owner planner.  FAQ (docshare page):
+ * MatrixShard metadata carries the owner plan through optimizer routing and
+ * resharding; owner segments replace equal-size shard assumptions.
+ *
+ * Conventions for every entry point:
+ *   - Return value: MFSDP_OK (0) or a negative mfsdp_status.  The library never
+ *     aborts, never prints and never allocates device memory; it keeps no state
+ *     between calls.
+ *   - Device pointers are plain CUDA device addresses owned by the caller and
+ *     must stay valid until the work queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All device work is asynchronous on it; all argument checks happen on the
+ *     host before anything is queued, so an error return means nothing ran.
+ *   - A matrix is stored row-major, `rows` x `cols`, in a flat buffer at an
+ *     element `offset`.  s = min(rows, cols), l = max(rows, cols).
+ */
+#ifndef MFSDP_H
+#define MFSDP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MFSDP_OK = 0,
+  MFSDP_ERR_INVALID_ARG = -1,        /* null pointer, negative count, bad enum, bad hyper-parameter */
+  MFSDP_ERR_MISALIGNED = -2,         /* base pointer not 16-byte aligned, workspace not 256-byte aligned */
+  MFSDP_ERR_OVERLAP = -3,            /* two segments, or two distinct buffers, share elements */
+  MFSDP_ERR_OUT_OF_BOUNDS = -4,      /* a segment extends past its buffer */
+  MFSDP_ERR_UNSUPPORTED_DTYPE = -5,  /* dtype code other than MFSDP_DTYPE_F32 / _BF16 where allowed */
+  MFSDP_ERR_UNSUPPORTED_SHAPE = -6,  /* dimension < 1, s > MFSDP_MAX_SHORT_SIDE, or l > MFSDP_MAX_LONG_SIDE */
+  MFSDP_ERR_WORKSPACE_TOO_SMALL = -7,
+  MFSDP_ERR_CUDA = -8,               /* a CUDA runtime call failed (no device, launch failure, ...) */
+  MFSDP_ERR_DEVICE_TIMEOUT = -9      /* a kernel's bounded wait expired (reported by mfsdp_muon_device_status) */
+} mfsdp_status;
+
+typedef enum { MFSDP_DTYPE_F32 = 0, MFSDP_DTYPE_BF16 = 1 } mfsdp_dtype;
+typedef enum { MFSDP_KIND_MATRIX = 0, MFSDP_KIND_TAIL = 1 } mfsdp_kind;
+
+#define MFSDP_MAX_SHORT_SIDE 32768
+#define MFSDP_MAX_LONG_SIDE (1 << 24)
+
+/* One parameter of the model, in declaration order (its index is its param id).
+ * kind MATRIX: a 2D weight updated by Muon.  kind TAIL: any tensor updated by
+ * AdamW; numel = rows * cols (a 1D tensor of n elements is rows = n, cols = 1). */
+typedef struct {
+  int64_t rows;
+  int64_t cols;
+  int32_t kind;
+  int32_t reserved;
+} mfsdp_param;
+
+/* MatrixShard: one whole matrix inside its owner's flat matrix buffer.
+ * The owner's gradient, fp32 momentum and update buffers all use this offset.
+ * transposed = rows > cols: Newton-Schulz then runs on the transpose, so the
+ * Gram matrix is always s x s.  cost = ns_steps * (4 s^2 l + 2 s^3), the dense
+ * Newton-Schulz FLOP count the planner balances. */
+typedef struct {
+  int32_t param_id;
+  int32_t owner;
+  int64_t offset;
+  int64_t rows;
+  int64_t cols;
+  int32_t transposed;
+  int32_t reserved;
+  uint64_t cost;
+} mfsdp_matrix_shard;
+
+/* One tail tensor inside its owner's flat fp32 tail buffer. */
+typedef struct {
+  int32_t param_id;
+  int32_t owner;
+  int64_t offset;
+  int64_t numel;
+} mfsdp_tail_shard;
+
+/* Balance-aware owner planner (Abstract: "a balance-aware owner planner";
+ * every 2D weight wholly on one rank, tail tensors on tail owners).  Host only.
+ *
+ * The pages give no algorithm; this one is:
+ *   matrices sorted by (cost desc, param id asc), each to the rank with the
+ *   smallest (matrix load, rank id) -- longest-processing-time first;
+ *   tail tensors sorted by (numel desc, param id asc), each to the rank with the
+ *   smallest (tail load, matrix load, rank id);
+ *   per rank, segments in ascending param id, each offset rounded up to
+ *   align_elems, matrix and tail buffers separate.
+ *
+ * params[n_params]     in: the model's parameters.
+ * world                in: number of data-parallel ranks (>= 1).
+ * ns_steps             in: Newton-Schulz steps (>= 0; scales every cost).
+ * align_elems          in: segment alignment in elements (>= 1; 128 keeps
+ *                      every segment 256-byte aligned in bf16).
+ * out_m                out: capacity >= number of MATRIX params; filled in
+ *                      (owner, offset) order.  *n_m receives the count.
+ * out_t                out: capacity >= number of TAIL params; same order.
+ * rank_matrix_elems    out[world]: each rank's matrix-buffer extent, the end of
+ *                      its last segment rounded up to align_elems (0 if empty).
+ * rank_tail_elems      out[world]: the same for the tail buffer.
+ * Any out pointer except out_m/out_t/n_m/n_t may be NULL.  Errors:
+ * INVALID_ARG, UNSUPPORTED_SHAPE (dimension < 1 or a cost above 2^64). */
+int mfsdp_plan_owners(const mfsdp_param* params, int32_t n_params, int32_t world,
+                      int32_t ns_steps, int64_t align_elems,
+                      mfsdp_matrix_shard* out_m, int32_t* n_m,
+                      mfsdp_tail_shard* out_t, int32_t* n_t,
+                      int64_t* rank_matrix_elems, int64_t* rank_tail_elems);
+
+/* Bytes of device workspace mfsdp_muon_owner_step needs for these shards
+ * (0 on invalid input).  Holds, per matrix, X (two bf16 ping-pong copies of
+ * the s x l iterate) and the s x s bf16 matrices A = X X^T and B = bA + cA^2,
+ * each padded to multiples of 128, plus norm partials and a status word. */
+size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards);
+
+/* Owner-local Muon step over one rank's owned matrices (Abstract: the reduced
+ * gradient lands whole on its owner; "Newton-Schulz runs locally with no
+ * optimizer-step matrix collective"; the update matches full-matrix Muon).
+ *
+ * For every shard (offset, rows, cols):
+ *   M <- beta*M + G                         (fp32, in place in `momentum`)
+ *   U  = M  (nesterov = 0)  or  G + beta*M  (nesterov = 1)
+ *   X  = U / (||U||_F + eps), transposed to s x l when rows > cols
+ *   ns_steps times:  A = X X^T,  B = b*A + c*A*A,  X <- a*X + B*X
+ *   update[offset ..] = X, transposed back to rows x cols.
+ * The Newton-Schulz products run on tensor cores with bf16 operands and fp32
+ * accumulation; A, B and X are held in bf16 between products.  A matrix whose
+ * momentum is exactly zero gets an all-zero update.
+ *
+ * shards[n_shards]  host array; segments must not overlap.  owner is ignored.
+ * grad              device, `numel` elements of grad_dtype (F32 or BF16).
+ * momentum          device, `numel` fp32; read and written.
+ * update            device, `numel` elements of update_dtype (F32 or BF16);
+ *                   only the shards' elements are written.  update may equal
+ *                   grad when both dtypes match (in-place); otherwise the three
+ *                   buffers must not overlap.
+ * numel             length of each buffer in elements.
+ * ns_steps          0..64; 0 returns the normalised momentum.
+ * workspace         device, >= mfsdp_muon_workspace_bytes(), 256-byte aligned;
+ *                   scratch only, contents undefined after the call.
+ * Errors: INVALID_ARG, MISALIGNED, OVERLAP, OUT_OF_BOUNDS, UNSUPPORTED_DTYPE,
+ * UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR. */
+int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                          const void* grad, int32_t grad_dtype,
+                          float* momentum,
+                          void* update, int32_t update_dtype,
+                          int64_t numel,
+                          float beta, int32_t nesterov, int32_t ns_steps,
+                          float a, float b, float c, float eps,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reads the device status word a previous mfsdp_muon_owner_step left in
+ * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
+ * if one of its kernels gave up on a bounded wait (its outputs are then
+ * undefined).  *detail (may be NULL) receives the raw word: bits 0-7 the
+ * waiting role, bits 8-31 the pipeline stage. */
+int mfsdp_muon_device_status(const void* workspace, void* stream, int32_t* detail);
+
+/* Layout of the workspace, for inspection: for shard i, out[8*i + 0..7] =
+ * { byte offset of X0, of X1, of A, of B, s_pad, l_pad, s, l }.  X0/X1 are
+ * s_pad x l_pad, A/B s_pad x s_pad, bf16, stored as 1024-byte atoms of
+ * 8 rows x 64 columns; atom (row/8, col/64) sits at
+ * ((col/64) * (rows_pad/8) + row/8) * 1024, and inside it element (r, c) at
+ * (r%8)*128 + ((((c%64)/8) ^ (r%8)) * 16) + (c%8)*2.  Returns the status. */
+int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int64_t* out);
+
+/* AdamW over a packed fp32 tail buffer (Abstract: non-matrix tensors "stay on
+ * AdamW"), decoupled weight decay, step counted from 1:
+ *   p <- p*(1 - lr*wd); m <- b1*m + (1-b1)*g; v <- b2*v + (1-b2)*g^2;
+ *   p <- p - lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
+ * p, m, v read and written in place; g read.  All device, n fp32 elements,
+ * 16-byte aligned, not overlapping (n == 0 is a no-op).  Errors: INVALID_ARG
+ * (null pointer, n < 0, step < 1, beta outside [0, 1)), MISALIGNED, OVERLAP,
+ * CUDA_ERROR. */
+int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t n,
+                          float lr, float beta1, float beta2, float eps, float wd,
+                          int64_t step, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mfsdp_status_string(int status);
+
+/* Library version as "major.minor.patch". */
+const char* mfsdp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MFSDP_H */

@@ -1,0 +1,222 @@
+"""Thin Python binding of libmfsdp.so (the C ABI declared in include/mfsdp.h).
+
+Argument marshalling only: every step of the owner-local optimizer step runs in
+the library's CUDA kernels.  Device buffers are torch tensors (PyTorch supplies
+device memory and streams); the library never allocates.  Importing this
+module raises if the library has not been built -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import List, Optional, Sequence, Tuple
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmfsdp.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libmfsdp.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_MISALIGNED = -2
+ERR_OVERLAP = -3
+ERR_OUT_OF_BOUNDS = -4
+ERR_UNSUPPORTED_DTYPE = -5
+ERR_UNSUPPORTED_SHAPE = -6
+ERR_WORKSPACE_TOO_SMALL = -7
+ERR_CUDA = -8
+ERR_DEVICE_TIMEOUT = -9
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+KIND_MATRIX = 0
+KIND_TAIL = 1
+
+EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step",
+            "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
+            "mfsdp_status_string", "mfsdp_version")
+
+
+class CParam(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("kind", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class MatrixShard(ctypes.Structure):
+    _fields_ = [("param_id", ctypes.c_int32), ("owner", ctypes.c_int32), ("offset", ctypes.c_int64),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("transposed", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("cost", ctypes.c_uint64)]
+
+    def as_dict(self) -> dict:
+        return dict(param_id=self.param_id, owner=self.owner, offset=self.offset, rows=self.rows,
+                    cols=self.cols, transposed=self.transposed, cost=self.cost)
+
+
+class TailShard(ctypes.Structure):
+    _fields_ = [("param_id", ctypes.c_int32), ("owner", ctypes.c_int32), ("offset", ctypes.c_int64),
+                ("numel", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return dict(param_id=self.param_id, owner=self.owner, offset=self.offset, numel=self.numel)
+
+
+_i32, _i64, _u64, _f, _vp, _sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float,
+                                  ctypes.c_void_p, ctypes.c_size_t)
+_lib.mfsdp_plan_owners.argtypes = [ctypes.POINTER(CParam), _i32, _i32, _i32, _i64, ctypes.POINTER(MatrixShard),
+                                   ctypes.POINTER(_i32), ctypes.POINTER(TailShard), ctypes.POINTER(_i32),
+                                   ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+_lib.mfsdp_plan_owners.restype = ctypes.c_int
+_lib.mfsdp_muon_workspace_bytes.argtypes = [ctypes.POINTER(MatrixShard), _i32]
+_lib.mfsdp_muon_workspace_bytes.restype = _sz
+_lib.mfsdp_muon_workspace_layout.argtypes = [ctypes.POINTER(MatrixShard), _i32, ctypes.POINTER(_i64)]
+_lib.mfsdp_muon_workspace_layout.restype = ctypes.c_int
+_lib.mfsdp_muon_owner_step.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _i64, _f, _i32,
+                                       _i32, _f, _f, _f, _f, _vp, _sz, _vp]
+_lib.mfsdp_muon_owner_step.restype = ctypes.c_int
+_lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
+_lib.mfsdp_muon_device_status.restype = ctypes.c_int
+_lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f, _f, _f, _f, _f, _i64, _vp]
+_lib.mfsdp_adamw_tail_step.restype = ctypes.c_int
+_lib.mfsdp_status_string.argtypes = [ctypes.c_int]
+_lib.mfsdp_status_string.restype = ctypes.c_char_p
+_lib.mfsdp_version.argtypes = []
+_lib.mfsdp_version.restype = ctypes.c_char_p
+
+
+class MfsdpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def status_string(status: int) -> str:
+    return _lib.mfsdp_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.mfsdp_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise MfsdpError(status, what)
+
+
+@dataclasses.dataclass
+class Plan:
+    matrix_shards: List[MatrixShard]
+    tail_shards: List[TailShard]
+    rank_matrix_elems: List[int]
+    rank_tail_elems: List[int]
+
+    def rank_matrices(self, r: int) -> List[MatrixShard]:
+        return [s for s in self.matrix_shards if s.owner == r]
+
+    def rank_tails(self, r: int) -> List[TailShard]:
+        return [s for s in self.tail_shards if s.owner == r]
+
+
+def plan_owners(params: Sequence[Tuple[int, int, int]], world: int, ns_steps: int = 5,
+                align_elems: int = 128) -> Plan:
+    """Balance-aware owner plan: params are (rows, cols, kind) in declaration order."""
+    n = len(params)
+    arr = (CParam * max(n, 1))()
+    for i, (r, c, k) in enumerate(params):
+        arr[i].rows, arr[i].cols, arr[i].kind = int(r), int(c), int(k)
+    nm = sum(1 for p in params if p[2] == KIND_MATRIX)
+    nt = n - nm
+    out_m = (MatrixShard * max(nm, 1))()
+    out_t = (TailShard * max(nt, 1))()
+    cm, ct = _i32(0), _i32(0)
+    world_i = int(world)
+    rme = (_i64 * max(world_i, 1))()
+    rte = (_i64 * max(world_i, 1))()
+    _check(_lib.mfsdp_plan_owners(arr, n, world_i, int(ns_steps), int(align_elems), out_m, ctypes.byref(cm), out_t,
+                                  ctypes.byref(ct), rme, rte), "plan_owners")
+    return Plan([out_m[i] for i in range(cm.value)], [out_t[i] for i in range(ct.value)],
+                list(rme[:world_i]), list(rte[:world_i]))
+
+
+def _shard_array(shards: Sequence[MatrixShard]):
+    arr = (MatrixShard * max(len(shards), 1))()
+    for i, s in enumerate(shards):
+        arr[i] = s
+    return arr
+
+
+def make_shard(offset: int, rows: int, cols: int, param_id: int = 0, owner: int = 0) -> MatrixShard:
+    s = MatrixShard()
+    s.param_id, s.owner, s.offset, s.rows, s.cols = param_id, owner, offset, rows, cols
+    s.transposed = int(rows > cols)
+    return s
+
+
+def muon_workspace_bytes(shards: Sequence[MatrixShard]) -> int:
+    return int(_lib.mfsdp_muon_workspace_bytes(_shard_array(shards), len(shards)))
+
+
+def muon_workspace_layout(shards: Sequence[MatrixShard]) -> List[Tuple[int, ...]]:
+    out = (_i64 * max(8 * len(shards), 1))()
+    _check(_lib.mfsdp_muon_workspace_layout(_shard_array(shards), len(shards), out), "muon_workspace_layout")
+    return [tuple(out[8 * i: 8 * i + 8]) for i in range(len(shards))]
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    return 99   # rejected by the library as UNSUPPORTED_DTYPE
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(stream) if isinstance(stream, int) else int(stream.cuda_stream)
+
+
+def muon_owner_step(shards: Sequence[MatrixShard], grad, momentum, update, workspace, *, beta: float = 0.95,
+                    nesterov: bool = False, ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315),
+                    eps: float = 1e-7, numel: Optional[int] = None, stream=None) -> None:
+    """One owner-local Muon step over the shards of one rank (see include/mfsdp.h).
+
+    grad: flat fp32/bf16 CUDA tensor; momentum: flat fp32; update: flat fp32/bf16;
+    workspace: CUDA uint8 tensor of at least muon_workspace_bytes(shards) bytes."""
+    arr = _shard_array(shards)
+    n = int(numel if numel is not None else grad.numel())
+    a, b, c = coeffs
+    _check(_lib.mfsdp_muon_owner_step(arr, len(shards), _ptr(grad), _dtype_code(grad), _ptr(momentum), _ptr(update),
+                                      _dtype_code(update), n, float(beta), int(bool(nesterov)), int(ns_steps),
+                                      float(a), float(b), float(c), float(eps), _ptr(workspace),
+                                      int(workspace.numel() if workspace is not None else 0), _stream(stream)),
+           "muon_owner_step")
+
+
+def muon_device_status(workspace, stream=None) -> Tuple[int, int]:
+    detail = _i32(0)
+    st = _lib.mfsdp_muon_device_status(_ptr(workspace), _stream(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def adamw_tail_step(p, g, m, v, *, lr: float, beta1: float, beta2: float, eps: float, wd: float, step: int,
+                    stream=None) -> None:
+    """Fused AdamW over one rank's packed fp32 tail (see include/mfsdp.h)."""
+    n = int(p.numel())
+    _check(_lib.mfsdp_adamw_tail_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n, float(lr), float(beta1), float(beta2),
+                                      float(eps), float(wd), int(step), _stream(stream)), "adamw_tail_step")
+
+
+def raw_lib() -> ctypes.CDLL:
+    """The loaded library, for callers that marshal raw pointers themselves."""
+    return _lib

@@ -1,0 +1,370 @@
+// Host side of the C ABI: argument checks, workspace layout, and the launch
+// sequence of the owner-local optimizer step.
+//
+// MatrixFSDP: Communication-Free Matrix Optimizers Under ZeRO-3 Parameter
+// Sharding -- Abstract: the owner rank holds each owned matrix whole in its
+// owner shard (MatrixShard metadata: offset, rows, cols), applies Muon
+// momentum and Newton-Schulz locally, and applies AdamW to the packed tail.
+//
+// Launch sequence of mfsdp_muon_owner_step on one stream:
+//   momentum/segment-view kernel (grouped over all shards)
+//   norm finalise
+//   ns_steps x { Gram, polynomial, update }   (each one grouped launch)
+// Grouped launches carry their per-matrix table as a kernel parameter, at most
+// kMaxBatch matrices per launch.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "mfsdp.h"
+#include "mfsdp_internal.h"
+
+namespace mfsdp {
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct MatLayout {
+  int s, l, s_pad, l_pad;
+  int transposed;
+  size_t x0, x1, a, b;   // byte offsets in the workspace
+  int tiles_k1;          // momentum-kernel tiles (kTile x kTile over s_pad x l_pad)
+  int partial0;
+};
+
+struct Layout {
+  std::vector<MatLayout> mats;
+  size_t norm_off = 0;
+  size_t partial_off = 0;
+  int partials = 0;
+  size_t bytes = 0;
+};
+
+int shape_ok(const mfsdp_matrix_shard& sh) {
+  if (sh.rows < 1 || sh.cols < 1) return MFSDP_ERR_UNSUPPORTED_SHAPE;
+  const int64_t s = std::min(sh.rows, sh.cols), l = std::max(sh.rows, sh.cols);
+  if (s > MFSDP_MAX_SHORT_SIDE || l > MFSDP_MAX_LONG_SIDE) return MFSDP_ERR_UNSUPPORTED_SHAPE;
+  return MFSDP_OK;
+}
+
+int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
+  if (n < 0 || (n > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
+  L->mats.resize(n);
+  int partials = 0;
+  for (int i = 0; i < n; ++i) {
+    const int st = shape_ok(shards[i]);
+    if (st != MFSDP_OK) return st;
+    MatLayout& m = L->mats[i];
+    m.s = (int)std::min(shards[i].rows, shards[i].cols);
+    m.l = (int)std::max(shards[i].rows, shards[i].cols);
+    m.s_pad = (int)round_up((size_t)m.s, kPad);
+    m.l_pad = (int)round_up((size_t)m.l, kPad);
+    m.transposed = shards[i].rows > shards[i].cols ? 1 : 0;
+    m.tiles_k1 = (m.s_pad / kTile) * (m.l_pad / kTile);
+    m.partial0 = partials;
+    partials += m.tiles_k1;
+  }
+  size_t off = kHeaderBytes;
+  L->norm_off = off;
+  off = round_up(off + sizeof(float2) * (size_t)n, 256);
+  L->partial_off = off;
+  L->partials = partials;
+  off = round_up(off + sizeof(float) * (size_t)partials, 1024);
+  for (int i = 0; i < n; ++i) {
+    MatLayout& m = L->mats[i];
+    const size_t xb = (size_t)m.s_pad * m.l_pad * 2, ab = (size_t)m.s_pad * m.s_pad * 2;
+    m.x0 = off; off += xb;
+    m.x1 = off; off += xb;
+    m.a = off; off += ab;
+    m.b = off; off += ab;
+  }
+  L->bytes = off;
+  return MFSDP_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool ranges_overlap(const void* p, size_t pb, const void* q, size_t qb) {
+  if (pb == 0 || qb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(q);
+  return a0 < b0 + qb && b0 < a0 + pb;
+}
+
+size_t dtype_size(int32_t dt) { return dt == MFSDP_DTYPE_BF16 ? 2 : 4; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_CUDA; }
+
+}  // namespace
+}  // namespace mfsdp
+
+using namespace mfsdp;
+
+extern "C" const char* mfsdp_status_string(int status) {
+  switch (status) {
+    case MFSDP_OK: return "ok";
+    case MFSDP_ERR_INVALID_ARG: return "invalid argument";
+    case MFSDP_ERR_MISALIGNED: return "misaligned pointer";
+    case MFSDP_ERR_OVERLAP: return "overlapping segments or buffers";
+    case MFSDP_ERR_OUT_OF_BOUNDS: return "segment out of bounds";
+    case MFSDP_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case MFSDP_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MFSDP_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MFSDP_ERR_CUDA: return "CUDA runtime error";
+    case MFSDP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* mfsdp_version(void) { return "0.1.0"; }
+
+extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
+  Layout L;
+  if (make_layout(shards, n_shards, &L) != MFSDP_OK) return 0;
+  return L.bytes;
+}
+
+extern "C" int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int64_t* out) {
+  Layout L;
+  const int st = make_layout(shards, n_shards, &L);
+  if (st != MFSDP_OK) return st;
+  if (n_shards > 0 && !out) return MFSDP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_shards; ++i) {
+    const MatLayout& m = L.mats[i];
+    int64_t* o = out + 8 * i;
+    o[0] = (int64_t)m.x0; o[1] = (int64_t)m.x1; o[2] = (int64_t)m.a; o[3] = (int64_t)m.b;
+    o[4] = m.s_pad; o[5] = m.l_pad; o[6] = m.s; o[7] = m.l;
+  }
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad,
+                                     int32_t grad_dtype, float* momentum, void* update, int32_t update_dtype,
+                                     int64_t numel, float beta, int32_t nesterov, int32_t ns_steps, float a,
+                                     float b, float c, float eps, void* workspace, size_t workspace_bytes,
+                                     void* stream_ptr) {
+  // ------------------------------------------------------------ validation
+  if (n_shards < 0 || (n_shards > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
+  if (grad_dtype != MFSDP_DTYPE_F32 && grad_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
+  if (update_dtype != MFSDP_DTYPE_F32 && update_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
+  if (numel < 0 || ns_steps < 0 || ns_steps > 64 || (nesterov != 0 && nesterov != 1)) return MFSDP_ERR_INVALID_ARG;
+  if (!std::isfinite(beta) || !std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) ||
+      eps < 0.f)
+    return MFSDP_ERR_INVALID_ARG;
+  if (n_shards == 0) return MFSDP_OK;
+  if (!grad || !momentum || !update || !workspace) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(grad, 16) || !aligned(momentum, 16) || !aligned(update, 16) || !aligned(workspace, 256))
+    return MFSDP_ERR_MISALIGNED;
+
+  Layout L;
+  int st = make_layout(shards, n_shards, &L);
+  if (st != MFSDP_OK) return st;
+  for (int i = 0; i < n_shards; ++i) {
+    const mfsdp_matrix_shard& sh = shards[i];
+    if (sh.offset < 0 || sh.offset > numel || sh.rows * sh.cols > numel - sh.offset) return MFSDP_ERR_OUT_OF_BOUNDS;
+  }
+  {
+    std::vector<int> ord(n_shards);
+    for (int i = 0; i < n_shards; ++i) ord[i] = i;
+    std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
+    for (int k = 1; k < n_shards; ++k) {
+      const mfsdp_matrix_shard& p0 = shards[ord[k - 1]];
+      if (p0.offset + p0.rows * p0.cols > shards[ord[k]].offset) return MFSDP_ERR_OVERLAP;
+    }
+  }
+  const size_t gbytes = (size_t)numel * dtype_size(grad_dtype), mbytes = (size_t)numel * 4,
+               ubytes = (size_t)numel * dtype_size(update_dtype);
+  const bool in_place = (update == grad && update_dtype == grad_dtype);
+  if (ranges_overlap(momentum, mbytes, grad, gbytes) || ranges_overlap(momentum, mbytes, update, ubytes) ||
+      (!in_place && ranges_overlap(grad, gbytes, update, ubytes)))
+    return MFSDP_ERR_OVERLAP;
+  if (workspace_bytes < L.bytes) return MFSDP_ERR_WORKSPACE_TOO_SMALL;
+  if (ranges_overlap(workspace, L.bytes, grad, gbytes) || ranges_overlap(workspace, L.bytes, momentum, mbytes) ||
+      ranges_overlap(workspace, L.bytes, update, ubytes))
+    return MFSDP_ERR_OVERLAP;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
+  float* partials = reinterpret_cast<float*>(ws + L.partial_off);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  const size_t gsz = dtype_size(grad_dtype), usz = dtype_size(update_dtype);
+
+  st = cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  if (st != MFSDP_OK) return st;
+
+  // ---------------------------------------------- momentum + segment view
+  for (int base = 0; base < n_shards; base += kMaxBatch) {
+    const int cnt = std::min(kMaxBatch, n_shards - base);
+    MomBatch mb;
+    std::memset(&mb, 0, sizeof(mb));
+    mb.n = cnt;
+    mb.grad_bf16 = grad_dtype == MFSDP_DTYPE_BF16;
+    mb.nesterov = nesterov;
+    mb.beta = beta;
+    mb.partials = partials;
+    int tiles = 0;
+    for (int k = 0; k < cnt; ++k) {
+      const int i = base + k;
+      const mfsdp_matrix_shard& sh = shards[i];
+      const MatLayout& m = L.mats[i];
+      MomMat& d = mb.mat[k];
+      d.g = static_cast<const uint8_t*>(grad) + (size_t)sh.offset * gsz;
+      d.m = momentum + sh.offset;
+      d.y = ws + m.x0;
+      d.rows = sh.rows;
+      d.cols = sh.cols;
+      d.s_pad = m.s_pad;
+      d.l_pad = m.l_pad;
+      d.transposed = m.transposed;
+      d.vec_ok = (sh.offset % 8 == 0) && (sh.cols % 8 == 0);
+      d.tiles_j = m.l_pad / kTile;
+      d.partial0 = m.partial0;
+      mb.tile_start[k] = tiles;
+      tiles += m.tiles_k1;
+    }
+    mb.tile_start[cnt] = tiles;
+    st = cuda_status(launch_momentum(mb, tiles, stream));
+    if (st != MFSDP_OK) return st;
+  }
+  for (int base = 0; base < n_shards; base += kMaxBatch) {
+    const int cnt = std::min(kMaxBatch, n_shards - base);
+    NormBatch nb;
+    std::memset(&nb, 0, sizeof(nb));
+    nb.n = cnt;
+    nb.first = base;
+    nb.eps = eps;
+    nb.partials = partials;
+    nb.norm = norm;
+    for (int k = 0; k < cnt; ++k) nb.start[k] = L.mats[base + k].partial0;
+    nb.start[cnt] = L.mats[base + cnt - 1].partial0 + L.mats[base + cnt - 1].tiles_k1;
+    st = cuda_status(launch_norm_finalize(nb, stream));
+    if (st != MFSDP_OK) return st;
+  }
+
+  // ---------------------------------------------------------- ns_steps == 0
+  if (ns_steps == 0) {
+    for (int base = 0; base < n_shards; base += kMaxBatch) {
+      const int cnt = std::min(kMaxBatch, n_shards - base);
+      EmitBatch eb;
+      std::memset(&eb, 0, sizeof(eb));
+      eb.n = cnt;
+      eb.out_bf16 = update_dtype == MFSDP_DTYPE_BF16;
+      eb.norm = norm;
+      int tiles = 0;
+      for (int k = 0; k < cnt; ++k) {
+        const int i = base + k;
+        const MatLayout& m = L.mats[i];
+        EmitMat& d = eb.mat[k];
+        d.y = ws + m.x0;
+        d.out = static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz;
+        d.rows = shards[i].rows;
+        d.cols = shards[i].cols;
+        d.s_pad = m.s_pad;
+        d.tiles_j = m.l_pad / kTile;
+        d.transposed = m.transposed;
+        d.norm_idx = i;
+        eb.tile_start[k] = tiles;
+        tiles += m.tiles_k1;
+      }
+      eb.tile_start[cnt] = tiles;
+      st = cuda_status(launch_emit(eb, tiles, stream));
+      if (st != MFSDP_OK) return st;
+    }
+    return MFSDP_OK;
+  }
+
+  // ------------------------------------------------------- Newton-Schulz
+  for (int it = 0; it < ns_steps; ++it) {
+    const bool last = (it == ns_steps - 1);
+    for (int mode = kGram; mode <= kUpdate; ++mode) {
+      const int eff_mode = (mode == kUpdate && last) ? kUpdateFinal : mode;
+      for (int base = 0; base < n_shards; base += kMaxBatch) {
+        const int cnt = std::min(kMaxBatch, n_shards - base);
+        GemmBatch gb;
+        std::memset(&gb, 0, sizeof(gb));
+        gb.n = cnt;
+        gb.mode = eff_mode;
+        gb.first_iter = it == 0;
+        gb.out_bf16 = update_dtype == MFSDP_DTYPE_BF16;
+        gb.a = a;
+        gb.b = b;
+        gb.c = c;
+        gb.norm = norm;
+        gb.status = status;
+        int tiles = 0;
+        for (int k = 0; k < cnt; ++k) {
+          const int i = base + k;
+          const MatLayout& m = L.mats[i];
+          uint8_t* xc = ws + ((it & 1) ? m.x1 : m.x0);   // current iterate
+          uint8_t* xn = ws + ((it & 1) ? m.x0 : m.x1);   // next iterate
+          GemmMat& d = gb.mat[k];
+          d.s_pad = m.s_pad;
+          d.l_pad = m.l_pad;
+          d.s = m.s;
+          d.l = m.l;
+          d.norm_idx = i;
+          d.transposed = m.transposed;
+          d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
+          d.tiles_m = m.s_pad / kBlockM;
+          const int ncols = (mode == kUpdate) ? m.l_pad : m.s_pad;
+          d.tiles_n = (ncols + kBlockN - 1) / kBlockN;
+          d.n_last = ncols - (d.tiles_n - 1) * kBlockN;
+          if (mode == kGram) {
+            d.a_op = xc; d.b_op = xc; d.c_in = nullptr; d.out = ws + m.a;
+            d.k_blocks = m.l_pad / kBlockK;
+          } else if (mode == kPoly) {
+            d.a_op = ws + m.a; d.b_op = ws + m.a; d.c_in = ws + m.a; d.out = ws + m.b;
+            d.k_blocks = m.s_pad / kBlockK;
+          } else {
+            d.a_op = ws + m.b; d.b_op = xc; d.c_in = xc;
+            d.out = last ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz)
+                         : static_cast<void*>(xn);
+            d.k_blocks = m.s_pad / kBlockK;
+          }
+          gb.tile_start[k] = tiles;
+          tiles += d.tiles_m * d.tiles_n;
+        }
+        gb.tile_start[cnt] = tiles;
+        st = cuda_status(launch_ns_gemm(gb, tiles, stream));
+        if (st != MFSDP_OK) return st;
+      }
+    }
+  }
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_device_status(const void* workspace, void* stream_ptr, int32_t* detail) {
+  if (!workspace) return MFSDP_ERR_INVALID_ARG;
+  int32_t word = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MFSDP_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MFSDP_ERR_CUDA;
+  if (detail) *detail = word;
+  return word ? MFSDP_ERR_DEVICE_TIMEOUT : MFSDP_OK;
+}
+
+extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t n, float lr, float beta1,
+                                     float beta2, float eps, float wd, int64_t step, void* stream_ptr) {
+  if (n < 0 || step < 1) return MFSDP_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return MFSDP_ERR_INVALID_ARG;
+  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd)) return MFSDP_ERR_INVALID_ARG;
+  if (n == 0) return MFSDP_OK;
+  if (!p || !g || !m || !v) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(p, 16) || !aligned(g, 16) || !aligned(m, 16) || !aligned(v, 16)) return MFSDP_ERR_MISALIGNED;
+  const size_t nb = (size_t)n * 4;
+  const void* bufs[4] = {p, g, m, v};
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (ranges_overlap(bufs[i], nb, bufs[j], nb)) return MFSDP_ERR_OVERLAP;
+  const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
+  const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
+  const float decay = (float)(1.0 - (double)lr * (double)wd);
+  const float step_size = (float)((double)lr / bc1);
+  const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  return cuda_status(launch_adamw(p, g, m, v, n, decay, beta1, beta2, step_size, inv_sqrt_bc2, eps,
+                                  static_cast<cudaStream_t>(stream_ptr)));
+}

@@ -1,0 +1,135 @@
+// Launch descriptors shared by the host orchestration (host.cu) and the
+// kernels.  Every grouped launch carries its per-matrix table by value as a
+// __grid_constant__ kernel parameter, so a step needs no device-side metadata
+// upload and can be captured in a CUDA graph as plain kernel nodes.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mfsdp {
+
+constexpr int kMaxBatch = 128;     // matrices per grouped launch
+constexpr int kTile = 64;          // momentum-kernel tile edge (elements)
+constexpr int kPad = 128;          // workspace matrices are padded to multiples of this
+constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows (UMMA M)
+constexpr int kBlockN = 256;       // Newton-Schulz GEMM tile columns (UMMA N)
+constexpr int kBlockK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kStages = 4;         // smem pipeline depth
+constexpr int kStageBytesA = kBlockM * kBlockK * 2;   // 16 KB
+constexpr int kStageBytesB = kBlockN * kBlockK * 2;   // 32 KB
+constexpr int kStageBytes = kStageBytesA + kStageBytesB;
+constexpr int kGemmThreads = 128;
+constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
+
+// Bytes between consecutive 64-column blocks of a blocked matrix with rows_pad rows.
+__host__ __device__ inline size_t colblock_stride(int rows_pad) { return (size_t)rows_pad * 128; }
+
+// Byte offset of the 16-byte chunk holding columns [col, col+8) of row `row`
+// (col a multiple of 8) in the blocked, pre-swizzled layout: 1024-byte atoms of
+// 8 rows x 64 bf16 columns, atoms column-block major, chunk index XOR row%8 --
+// the exact image of the UMMA 128-byte-swizzle canonical layout.
+__host__ __device__ inline size_t blocked_chunk(int rows_pad, int row, int col) {
+  return (size_t)(col >> 6) * colblock_stride(rows_pad) + (size_t)(row >> 3) * 1024 +
+         (size_t)(row & 7) * 128 + (size_t)((((col & 63) >> 3) ^ (row & 7)) << 4);
+}
+
+// ---------------------------------------------------------------- momentum (K1)
+struct MomMat {
+  const void* g;       // gradient at the shard's offset (fp32 or bf16)
+  float* m;            // momentum at the shard's offset
+  uint8_t* y;          // X0 in the workspace (blocked bf16, s_pad x l_pad)
+  int64_t rows, cols;  // stored shape
+  int32_t s_pad, l_pad;
+  int32_t transposed;
+  int32_t vec_ok;      // offset and cols multiples of 8: 16-byte vector access
+  int32_t tiles_j;     // l_pad / kTile
+  int32_t partial0;    // first norm-partial slot of this matrix
+};
+struct MomBatch {
+  int32_t n;
+  int32_t grad_bf16;
+  int32_t nesterov;
+  float beta;
+  float* partials;
+  int32_t tile_start[kMaxBatch + 1];
+  MomMat mat[kMaxBatch];
+};
+
+// ------------------------------------------------------- norm finalise (K2)
+struct NormBatch {
+  int32_t n;
+  int32_t first;       // global index of mat 0 of this batch
+  float eps;
+  int32_t pad;
+  const float* partials;
+  float2* norm;        // {sum of squares, 1/(sqrt(sum)+eps)} per matrix
+  int32_t start[kMaxBatch + 1];   // partial slots of matrix i: [start[i], start[i+1])
+};
+
+// ------------------------------------------------- Newton-Schulz GEMMs (K3-K5)
+enum GemmMode : int32_t {
+  kGram = 0,         // A = scale * X X^T               (X: K-major operand twice)
+  kPoly = 1,         // B = b*A + c * A A               (A symmetric: K-major twice)
+  kUpdate = 2,       // X' = scale * (a*X + B X)        (B K-major, X MN-major)
+  kUpdateFinal = 3,  // same, written to the caller's update buffer
+};
+
+struct GemmMat {
+  const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
+  const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
+  const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly, X for kUpdate*)
+  void* out;             // blocked bf16 output, or the caller's buffer at the shard offset
+  int32_t s_pad, l_pad;
+  int32_t s, l;          // true short / long side
+  int32_t tiles_m, tiles_n;
+  int32_t k_blocks;      // K / kBlockK
+  int32_t n_last;        // width of the last column tile (128 or 256)
+  int32_t norm_idx;      // index into the norm table
+  int32_t transposed;    // kUpdateFinal: stored matrix is l x s
+  int32_t vec_ok;        // kUpdateFinal: row-major stores may use 16-byte vectors
+  int32_t pad;
+};
+struct GemmBatch {
+  int32_t n;
+  int32_t mode;
+  int32_t first_iter;    // fold the 1/(||U||+eps) prescale into this launch
+  int32_t out_bf16;      // kUpdateFinal: output dtype
+  float a, b, c;
+  int32_t pad;
+  const float2* norm;
+  int32_t* status;       // device status word (timeouts)
+  int32_t tile_start[kMaxBatch + 1];
+  GemmMat mat[kMaxBatch];
+};
+
+// ------------------------------------------------------------ emit (T = 0)
+struct EmitMat {
+  const uint8_t* y;
+  void* out;
+  int64_t rows, cols;
+  int32_t s_pad, tiles_j;
+  int32_t transposed, norm_idx;
+};
+struct EmitBatch {
+  int32_t n;
+  int32_t out_bf16;
+  const float2* norm;
+  int32_t tile_start[kMaxBatch + 1];
+  EmitMat mat[kMaxBatch];
+};
+
+// Status word bits written by kernels that give up on a bounded wait.
+constexpr int32_t kStatusTimeout = 1;
+
+cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
+cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
+cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
+cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s);
+cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, float decay,
+                         float beta1, float beta2, float step_size, float inv_sqrt_bc2, float eps,
+                         cudaStream_t s);
+
+}  // namespace mfsdp

@@ -1,0 +1,160 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and exports
+every entry point include/mfsdp.h declares, the C++ planner reproduces the
+oracle planner bit for bit, and every argument error is reported with its
+status code before any device work is queued.
+
+All pointers below are fake; every case is rejected by the host checks, so no
+CUDA call is made (these tests are safe on a machine with a GPU too)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle.planner import plan_owners_ref
+from matrix_optimizers_under_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mfsdp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mfsdp_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(mfsdp):
+    decl = declared_functions()
+    assert len(decl) >= 8
+    lib = mfsdp.raw_lib()
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert sorted(mfsdp.EXPORTED) == decl
+    assert mfsdp.version().count(".") == 2
+
+
+def test_status_strings(mfsdp):
+    seen = set()
+    for code in range(0, -10, -1):
+        s = mfsdp.status_string(code)
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 10
+    assert mfsdp.status_string(-1234) == "unknown status"
+
+
+def _compare(plan, ref):
+    assert [s.as_dict() for s in plan.matrix_shards] == ref["matrix_shards"]
+    assert [s.as_dict() for s in plan.tail_shards] == ref["tail_shards"]
+    assert plan.rank_matrix_elems == ref["rank_matrix_elems"]
+    assert plan.rank_tail_elems == ref["rank_tail_elems"]
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_planner_bit_exact_on_workloads(mfsdp, name):
+    w = W.get(name)
+    params = w.param_table()
+    for world in sorted({1, 2, w.world, 64}):
+        _compare(mfsdp.plan_owners(params, world, w.ns_steps, w.align_elems),
+                 plan_owners_ref(params, world, w.ns_steps, w.align_elems))
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_planner_bit_exact_fuzz(mfsdp, seed):
+    params = W.ragged_params(seed, 1 + seed * 7)
+    for world in (1, 3, 8):
+        for align in (1, 64, 128):
+            for steps in (0, 1, 5):
+                _compare(mfsdp.plan_owners(params, world, steps, align), plan_owners_ref(params, world, steps, align))
+
+
+def test_planner_errors(mfsdp):
+    with pytest.raises(mfsdp.MfsdpError) as e:
+        mfsdp.plan_owners([(4, 4, 0)], 0)
+    assert e.value.status == mfsdp.ERR_INVALID_ARG
+    with pytest.raises(mfsdp.MfsdpError) as e:
+        mfsdp.plan_owners([(0, 4, 0)], 2)
+    assert e.value.status == mfsdp.ERR_UNSUPPORTED_SHAPE
+    with pytest.raises(mfsdp.MfsdpError) as e:
+        mfsdp.plan_owners([(4, 4, 7)], 2)
+    assert e.value.status == mfsdp.ERR_INVALID_ARG
+    with pytest.raises(mfsdp.MfsdpError) as e:   # cost above 2^64
+        mfsdp.plan_owners([(1 << 24, 1 << 24, 0)], 2, ns_steps=64)
+    assert e.value.status == mfsdp.ERR_UNSUPPORTED_SHAPE
+    plan = mfsdp.plan_owners([], 3)
+    assert plan.matrix_shards == [] and plan.rank_matrix_elems == [0, 0, 0]
+
+
+def test_workspace_layout(mfsdp):
+    shards = [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131072, 300, 130), mfsdp.make_shard(200000, 1, 9)]
+    lay = mfsdp.muon_workspace_layout(shards)
+    total = mfsdp.muon_workspace_bytes(shards)
+    assert [l[4:] for l in lay] == [(256, 512, 256, 512), (256, 384, 130, 300), (128, 128, 1, 9)]
+    end = 0
+    for x0, x1, a, b, sp, lp, _, _ in lay:
+        assert x0 % 1024 == 0 and x0 >= end
+        assert x1 == x0 + sp * lp * 2 and a == x1 + sp * lp * 2 and b == a + sp * sp * 2
+        end = b + sp * sp * 2
+    assert total == end
+    assert mfsdp.muon_workspace_bytes([mfsdp.make_shard(0, 0, 5)]) == 0
+    assert mfsdp.muon_workspace_bytes([mfsdp.make_shard(0, 40000, 40000)]) == 0
+
+
+# ------------------------------------------------------------ error paths
+BF, F32 = 1, 0
+G, M, U, WS = 0x10000000, 0x20000000, 0x30000000, 0x40000000   # fake, aligned, disjoint
+
+
+def step(mfsdp, shards, grad=G, gdt=BF, mom=M, upd=U, udt=BF, numel=1 << 20, ns=5, ws=WS, wsb=None,
+         beta=0.95, nesterov=0, eps=1e-7):
+    arr = (mfsdp.MatrixShard * max(len(shards), 1))(*shards)
+    if wsb is None:
+        wsb = mfsdp.muon_workspace_bytes(shards) if shards else 0
+    return mfsdp.raw_lib().mfsdp_muon_owner_step(arr, len(shards), grad, gdt, mom, upd, udt, numel, beta, nesterov,
+                                                 ns, 3.4445, -4.775, 2.0315, eps, ws, wsb, None)
+
+
+def test_step_error_paths(mfsdp):
+    ok = [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131072, 512, 256)]
+    assert step(mfsdp, [], grad=None, mom=None, upd=None, ws=None) == mfsdp.OK   # empty owner set: no-op
+    assert step(mfsdp, ok, gdt=7) == mfsdp.ERR_UNSUPPORTED_DTYPE
+    assert step(mfsdp, ok, udt=2) == mfsdp.ERR_UNSUPPORTED_DTYPE
+    assert step(mfsdp, ok, ns=-1) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, ns=65) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, nesterov=2) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, eps=-1.0) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, beta=float("nan")) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, grad=None) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, numel=-5) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, grad=G + 2) == mfsdp.ERR_MISALIGNED
+    assert step(mfsdp, ok, mom=M + 4) == mfsdp.ERR_MISALIGNED
+    assert step(mfsdp, ok, ws=WS + 16) == mfsdp.ERR_MISALIGNED
+    assert step(mfsdp, [mfsdp.make_shard(0, 0, 4)]) == mfsdp.ERR_UNSUPPORTED_SHAPE
+    assert step(mfsdp, [mfsdp.make_shard(0, 40000, 40000)], numel=1 << 31) == mfsdp.ERR_UNSUPPORTED_SHAPE
+    assert step(mfsdp, [mfsdp.make_shard(-128, 16, 16)]) == mfsdp.ERR_OUT_OF_BOUNDS
+    assert step(mfsdp, [mfsdp.make_shard(1 << 20, 16, 16)]) == mfsdp.ERR_OUT_OF_BOUNDS
+    assert step(mfsdp, ok, numel=131072 + 512 * 255) == mfsdp.ERR_OUT_OF_BOUNDS
+    assert step(mfsdp, [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131071, 4, 4)]) == mfsdp.ERR_OVERLAP
+    # distinct buffers that overlap
+    assert step(mfsdp, ok, mom=G + 1024) == mfsdp.ERR_OVERLAP
+    assert step(mfsdp, ok, upd=G + 1024) == mfsdp.ERR_OVERLAP
+    assert step(mfsdp, ok, upd=G, udt=F32) == mfsdp.ERR_OVERLAP        # same address, different dtype
+    assert step(mfsdp, ok, ws=G) == mfsdp.ERR_OVERLAP
+    assert step(mfsdp, ok, wsb=mfsdp.muon_workspace_bytes(ok) - 1) == mfsdp.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_adamw_error_paths(mfsdp):
+    lib = mfsdp.raw_lib()
+    P, Gp, Mm, V = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+
+    def call(p=P, g=Gp, m=Mm, v=V, n=4096, b1=0.9, b2=0.95, step=1, lr=1e-3):
+        return lib.mfsdp_adamw_tail_step(p, g, m, v, n, lr, b1, b2, 1e-8, 0.1, step, None)
+    assert call(n=0, p=None, g=None, m=None, v=None) == mfsdp.OK
+    assert call(n=-1) == mfsdp.ERR_INVALID_ARG
+    assert call(step=0) == mfsdp.ERR_INVALID_ARG
+    assert call(b1=1.0) == mfsdp.ERR_INVALID_ARG
+    assert call(b2=-0.1) == mfsdp.ERR_INVALID_ARG
+    assert call(lr=float("inf")) == mfsdp.ERR_INVALID_ARG
+    assert call(g=None) == mfsdp.ERR_INVALID_ARG
+    assert call(v=V + 8) == mfsdp.ERR_MISALIGNED
+    assert call(m=P + 1024) == mfsdp.ERR_OVERLAP

@@ -1,0 +1,283 @@
+"""GPU parity of the owner-local optimizer step against the fp64 oracle.
+
+Every case calls the CUDA library through its C ABI (via the thin binding) on
+seeded inputs and compares element by element with the oracle:
+  * momentum buffer: fp32 within one rounding of beta*M + G;
+  * Newton-Schulz update: relative Frobenius error <= 2e-2 per matrix, exact
+    zero for all-zero matrices;
+  * AdamW: max relative error <= 1e-5 (floor 1e-2 * max |reference|);
+  * padding between segments (filled with NaN canaries) is never read or written.
+Equivalence (MatrixFSDP -- Abstract: the update matches full-matrix Muon):
+an owner set's update equals, bit for bit, the update of each matrix run alone
+from its own buffer.
+"""
+import numpy as np
+import pytest
+
+from oracle import adamw_ref, muon_matrix_ref, bf16_bits_to_f64, newton_schulz_ref
+from matrix_optimizers_under_gb300 import workloads as W
+from tests import helpers as H
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+A, B, C = W.NS_COEFFS
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def to_dev_grad(buf: np.ndarray):
+    if buf.dtype == np.uint16:
+        return torch.from_numpy(buf.view(np.int16)).to(_dev()).view(torch.bfloat16)
+    return torch.from_numpy(buf).to(_dev())
+
+
+def from_dev(t) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return H.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return t.cpu().numpy()
+
+
+def run_step(mfsdp, shards, grad_np, mom_np, *, update_dtype, ns_steps=5, beta=0.95, nesterov=False,
+             coeffs=W.NS_COEFFS, eps=W.NS_EPS, ws_extra=0):
+    dev = _dev()
+    grad = to_dev_grad(grad_np)
+    mom = torch.from_numpy(mom_np.copy()).to(dev)
+    numel = grad_np.size
+    upd = torch.full((numel,), float("nan"), dtype=update_dtype, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards) + ws_extra, dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step(shards, grad, mom, upd, ws, beta=beta, nesterov=nesterov, ns_steps=ns_steps,
+                          coeffs=coeffs, eps=eps)
+    st, detail = mfsdp.muon_device_status(ws)
+    assert st == mfsdp.OK, (st, detail)
+    torch.cuda.synchronize()
+    return from_dev(upd), mom.cpu().numpy(), ws
+
+
+def grad_f64(buf, s):
+    seg = buf[s.offset:s.offset + s.rows * s.cols]
+    return (bf16_bits_to_f64(seg) if seg.dtype == np.uint16 else seg.astype(np.float64)).reshape(s.rows, s.cols)
+
+
+def check_matrix(s, upd, mom, grad_np, mom0, *, ns_steps, beta=0.95, nesterov=False, zero=False):
+    G = grad_f64(grad_np, s)
+    M0 = mom0[s.offset:s.offset + s.rows * s.cols].astype(np.float64).reshape(s.rows, s.cols)
+    M_ref, O_ref = muon_matrix_ref(G, M0, beta, nesterov, ns_steps, A, B, C, W.NS_EPS)
+    O = upd[s.offset:s.offset + s.rows * s.cols].reshape(s.rows, s.cols)
+    M = mom[s.offset:s.offset + s.rows * s.cols].reshape(s.rows, s.cols)
+    bound = H.MOM_REL * (np.abs(beta * M0) + np.abs(G)) + 1e-30
+    assert np.all(np.abs(M - M_ref) <= bound), f"momentum mismatch param {s.param_id}"
+    if zero:
+        assert np.all(O == 0.0), f"zero matrix {s.param_id} not exactly zero"
+        return 0.0
+    err = H.rel_fro(O, O_ref)
+    assert np.all(np.isfinite(O)), f"non-finite update param {s.param_id}"
+    assert err <= H.NS_REL_FRO, f"param {s.param_id} {s.rows}x{s.cols}: rel Frobenius error {err:.3e}"
+    return err
+
+
+def check_padding(upd, mom, shards, numel):
+    used = np.zeros(numel, bool)
+    for s in shards:
+        used[s.offset:s.offset + s.rows * s.cols] = True
+    assert np.all(np.isnan(upd[~used])), "update written outside the segments"
+    assert np.all(mom[~used] == 0.0), "momentum written outside the segments"
+
+
+def owner_set(mfsdp, w, rank=None):
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan) if rank is None else rank
+    return plan, r, plan.rank_matrices(r), plan.rank_matrix_elems[r]
+
+
+# ------------------------------------------------------------------ AdamW
+@pytest.mark.parametrize("n", [1, 3, 13, 4096, 4097, 9984, 1 << 20])
+def test_adamw_parity(mfsdp, n):
+    dev = _dev()
+    w = W.get("tiny")
+    rng = np.random.default_rng(n)
+    p = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    tp, tm, tv = (torch.from_numpy(x.copy()).to(dev) for x in (p, m, v))
+    rp, rm, rv = p.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    for t in (1, 2, 3):
+        g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        tg = torch.from_numpy(g).to(dev)
+        mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
+                              wd=w.weight_decay, step=t)
+        # the oracle continues from the GPU's fp32 state, as the next step would
+        rp, rm, rv = adamw_ref(rp, g, rm, rv, w.lr, w.betas[0], w.betas[1], w.adam_eps, w.weight_decay, t)
+        gp, gm, gv = (x.cpu().numpy() for x in (tp, tm, tv))
+        assert H.adam_err(gp, rp) <= H.ADAM_REL
+        assert H.adam_err(gm, rm) <= H.ADAM_REL
+        assert H.adam_err(gv, rv) <= H.ADAM_REL
+        rp, rm, rv = gp.astype(np.float64), gm.astype(np.float64), gv.astype(np.float64)
+
+
+def test_adamw_tiny_workload_first_step_closed_form(mfsdp):
+    dev = _dev()
+    w = W.get("tiny")
+    tid = [i for i, p in enumerate(w.params) if p.kind == W.KIND_TAIL][0]
+    p0 = W.tail_param_f32(w, tid)
+    g = W.grad_f32(w, tid)
+    tp, tg = torch.from_numpy(p0.copy()).to(dev), torch.from_numpy(g).to(dev)
+    tm, tv = torch.zeros_like(tp), torch.zeros_like(tp)
+    mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=1)
+    g64 = g.astype(np.float64)
+    closed = p0.astype(np.float64) * (1 - 1e-3 * 0.1) - 1e-3 * g64 / (np.abs(g64) + 1e-8)
+    assert H.adam_err(tp.cpu().numpy(), closed) <= H.ADAM_REL
+    assert H.adam_err(tm.cpu().numpy(), 0.1 * g64) <= H.ADAM_REL
+    assert H.adam_err(tv.cpu().numpy(), 0.05 * g64 * g64) <= H.ADAM_REL
+
+
+# ------------------------------------------------------- momentum + NS
+@pytest.mark.parametrize("ns_steps", [0, 1, 2, 5])
+@pytest.mark.parametrize("upd_dtype", ["f32", "bf16"])
+def test_tiny_workload(mfsdp, ns_steps, upd_dtype):
+    w = W.get("tiny")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    dt = torch.float32 if upd_dtype == "f32" else torch.bfloat16
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=dt, ns_steps=ns_steps)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=ns_steps)
+
+
+@pytest.mark.parametrize("ns_steps", [1, 2])
+def test_each_product_from_workspace(mfsdp, ns_steps):
+    """Isolates every kernel: the workspace keeps X0 = bf16(U), the last
+    iteration's A and B, and (for two steps) X1, so each product is checked
+    against fp64 arithmetic on the bf16 inputs it actually read.  ns_steps=1
+    covers the first-iteration prescale paths, ns_steps=2 the plain ones."""
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    upd, mom, ws = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32, ns_steps=ns_steps)
+    wsb = ws.cpu().numpy()
+    for s, (x0, x1, a_off, b_off, sp, lp, sd, ld) in zip(shards, mfsdp.muon_workspace_layout(shards)):
+        G = grad_f64(grad, s)
+        X = G.T if s.rows > s.cols else G
+        Yw = H.unblock(wsb, x0, sp, lp).astype(np.float64)
+        assert np.array_equal(Yw[:sd, :ld], X), "X0 is not bf16(U) (G is bf16 and M = G)"
+        assert np.all(Yw[sd:, :] == 0) and np.all(Yw[:, ld:] == 0), "X0 padding not zero"
+        Aw = H.unblock(wsb, a_off, sp, sp).astype(np.float64)[:sd, :sd]
+        Bw = H.unblock(wsb, b_off, sp, sp).astype(np.float64)[:sd, :sd]
+        O = upd[s.offset:s.offset + s.rows * s.cols].reshape(s.rows, s.cols).astype(np.float64)
+        O = O.T if s.rows > s.cols else O
+        if ns_steps == 1:
+            inv = 1.0 / (np.sqrt(np.sum(X * X)) + W.NS_EPS)
+            Xin, scale_a, scale_x = X, inv * inv, inv
+        else:
+            Xin = H.unblock(wsb, x1, sp, lp).astype(np.float64)[:sd, :ld]
+            scale_a = scale_x = 1.0
+        assert H.rel_fro(Aw, scale_a * (Xin @ Xin.T)) < 1e-2, "Gram product"
+        assert H.rel_fro(Bw, B * Aw + C * (Aw @ Aw)) < 1e-2, "polynomial product"
+        assert H.rel_fro(O, scale_x * (A * Xin + Bw @ Xin)) < 1e-2, "update product"
+
+
+@pytest.mark.parametrize("upd_dtype", ["f32", "bf16"])
+def test_gpt2_block_workload(mfsdp, upd_dtype):
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    dt = torch.float32 if upd_dtype == "f32" else torch.bfloat16
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=dt)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=5)
+    check_padding(upd, mom, shards, numel)
+
+
+RAGGED = [(1, 1), (1, 9), (9, 1), (7, 300), (300, 7), (130, 257), (257, 130), (129, 129), (200, 640), (513, 96)]
+
+
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_ragged_shapes_odd_offsets(mfsdp, gdt):
+    """Shapes that are not multiples of any tile, at offsets that are not
+    multiples of 8 (scalar paths), plus a zero matrix."""
+    rng = np.random.default_rng(123)
+    shards, off = [], 0
+    for i, (r, c) in enumerate(RAGGED):
+        off += int(rng.integers(1, 40))
+        shards.append(mfsdp.make_shard(off, r, c, param_id=i))
+        off += r * c
+    numel = off + 5
+    vals = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
+    zero = shards[3]
+    vals[zero.offset:zero.offset + zero.rows * zero.cols] = 0
+    grad = vals if gdt == "f32" else W.f32_to_bf16_bits(vals)
+    mom0 = (rng.standard_normal(numel) * 1e-3).astype(np.float32)   # a second step: M != 0
+    mom0[zero.offset:zero.offset + zero.rows * zero.cols] = 0
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=5, zero=(s is zero))
+
+
+def test_nesterov_and_second_step(mfsdp):
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    rng = np.random.default_rng(5)
+    mom0 = np.zeros(numel, np.float32)
+    for s in shards:
+        mom0[s.offset:s.offset + s.rows * s.cols] = rng.standard_normal(s.rows * s.cols) * 1e-3
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32, nesterov=True)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=5, nesterov=True)
+
+
+def test_equivalence_owner_set_vs_standalone(mfsdp):
+    """The owner-set update equals each matrix's standalone update, bitwise."""
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.bfloat16)
+    for s in shards:
+        n = s.rows * s.cols
+        alone = [mfsdp.make_shard(0, s.rows, s.cols, param_id=s.param_id)]
+        u1, m1, _ = run_step(mfsdp, alone, grad[s.offset:s.offset + n].copy(), np.zeros(n, np.float32),
+                             update_dtype=torch.bfloat16)
+        assert np.array_equal(u1.view(np.uint32), upd[s.offset:s.offset + n].view(np.uint32))
+        assert np.array_equal(m1, mom[s.offset:s.offset + n])
+
+
+def test_determinism(mfsdp):
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    u1, m1, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32)
+    u2, m2, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32)
+    assert np.array_equal(u1.view(np.uint32), u2.view(np.uint32))
+    assert np.array_equal(m1, m2)
+
+
+def test_in_place_update_over_grad(mfsdp):
+    dev = _dev()
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    ref_upd, _, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.bfloat16)
+    g = to_dev_grad(grad)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step(shards, g, mom, g, ws)
+    out = from_dev(g)
+    for s in shards:
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        assert np.array_equal(out[seg].view(np.uint32), ref_upd[seg].view(np.uint32))
+
+
+def test_empty_owner_set(mfsdp):
+    dev = _dev()
+    g = torch.zeros(16, dtype=torch.bfloat16, device=dev)
+    mfsdp.muon_owner_step([], g, torch.zeros(16, device=dev), g, None)
