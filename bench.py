@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark of the owner-local optimizer step (MatrixFSDP: Communication-Free
+Matrix Optimizers Under ZeRO-3 Parameter Sharding -- Abstract).
+
+One step = one pass of the whole hot path over one owner set: the momentum /
+segment-view / norm phase, five Newton-Schulz iterations (Gram, polynomial,
+update products on tcgen05 tensor cores) and AdamW over the rank's packed tail,
+all through the C ABI (libmfsdp.so) on one stream.  Default workload: the
+Llama-3-8B-shaped owner set (one rank of eight: 28 matrices, 872.4M bf16
+gradient elements with Student-t(3) entries, 32,768-element RMSNorm tail).
+
+Prints one JSON line.  `value` is the device-timed owner-step latency in ms
+(inputs resident in HBM; every input is larger than L2, so no flush is needed),
+`e2e` the same latency through the same API with the gradient copied in from
+pinned host memory and the update copied back every step.  `--impl reference`
+times the fp64 CPU oracle on a bounded sample of the same workload instead.
+
+Under torchrun (N > 1) each GPU runs the owner set of a different simulated
+rank (weak scaling: no collective on the data path; a barrier and a max over
+ranks bracket the timed region).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from matrix_optimizers_under_gb300 import workloads as W  # noqa: E402
+
+METRIC = "owner-step ms; Newton–Schulz TFLOP/s (% BF16 peak); AdamW-tail GB/s (% HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ns_flops(rows: int, cols: int, steps: int) -> int:
+    s, l = min(rows, cols), max(rows, cols)
+    return steps * (4 * s * s * l + 2 * s ** 3)
+
+
+def heaviest_rank(plan) -> int:
+    world = len(plan.rank_matrix_elems)
+    cost, tail = [0] * world, [0] * world
+    for s in plan.matrix_shards:
+        cost[s.owner] += s.cost
+    for s in plan.tail_shards:
+        tail[s.owner] += s.numel
+    return min(range(world), key=lambda r: (-cost[r], tail[r], r))
+
+
+def _gen_matrix(args):
+    name, pid = args
+    return pid, W.grad_storage(W.get(name), pid)
+
+
+def generate_grads(w, shards, numel):
+    """Flat gradient buffer of one rank (bf16 bits or fp32), generated per matrix
+    in a spawn-started process pool (started before any CUDA call)."""
+    dtype = np.uint16 if w.grad_dtype == "bf16" else np.float32
+    buf = np.zeros(numel, dtype)
+    jobs = [(w.name, s.param_id) for s in shards]
+    by_id = {s.param_id: s for s in shards}
+    nproc = max(1, min(len(jobs), (os.cpu_count() or 2), 16))
+    if nproc > 1 and sum(s.rows * s.cols for s in shards) > 8_000_000:
+        with mp.get_context("spawn").Pool(nproc) as pool:
+            for pid, g in pool.imap_unordered(_gen_matrix, jobs):
+                s = by_id[pid]
+                buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
+    else:
+        for j in jobs:
+            pid, g = _gen_matrix(j)
+            s = by_id[pid]
+            buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
+    return buf
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, shards, tail_n, sample_ids, threads_note=""):
+    """Times the fp64 oracle on the sample matrices (momentum + Newton-Schulz)
+    and on the AdamW tail; returns (seconds, sample NS FLOPs, sample elements)."""
+    from oracle import adamw_ref, muon_matrix_ref
+    a, b, c = w.ns_coeffs
+    t0 = time.perf_counter()
+    flops = 0
+    elems = 0
+    for s in shards:
+        if s.param_id not in sample_ids:
+            continue
+        g = W.grad_storage(w, s.param_id)
+        G = ((g.astype(np.uint32) << 16).view(np.float32) if g.dtype == np.uint16 else g).astype(np.float64)
+        muon_matrix_ref(G, np.zeros_like(G), w.beta, w.nesterov, w.ns_steps, a, b, c, w.ns_eps)
+        flops += ns_flops(s.rows, s.cols, w.ns_steps)
+        elems += s.rows * s.cols
+    if tail_n:
+        rng = np.random.default_rng(0)
+        p = rng.standard_normal(tail_n)
+        adamw_ref(p, p, np.zeros(tail_n), np.zeros(tail_n), w.lr, w.betas[0], w.betas[1], w.adam_eps,
+                  w.weight_decay, w.step)
+    return time.perf_counter() - t0, flops, elems
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return int(max(i.get("num_threads", 1) for i in info))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def pick_sample(shards):
+    """A bounded sample of the owner set: its smallest matrix plus one square one
+    (about 10-30 s of fp64 CPU work for the transformer owner sets)."""
+    by_size = sorted(shards, key=lambda s: (s.rows * s.cols, s.param_id))
+    ids = [by_size[0].param_id]
+    sq = [s for s in shards if s.rows == s.cols]
+    if sq and sq[0].param_id not in ids:
+        ids.append(sq[0].param_id)
+    return ids
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return 0
+    w = W.get(args.workload)
+    from oracle.planner import plan_owners_ref, heaviest_rank_ref
+    plan = plan_owners_ref(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = heaviest_rank_ref(plan)
+
+    class S:  # adapter with attribute access
+        def __init__(self, d):
+            self.__dict__.update(d)
+    shards = [S(d) for d in plan["matrix_shards"] if d["owner"] == r]
+    tail_n = plan["rank_tail_numel"][r]
+    total_flops = sum(ns_flops(s.rows, s.cols, w.ns_steps) for s in shards)
+    sample = [min(shards, key=lambda s: (s.rows * s.cols, s.param_id)).param_id]
+    ms = []
+    for i in range(args.warmup + args.steps):
+        sec, fl, el = oracle_sample(w, shards, tail_n, sample)
+        if i >= args.warmup:
+            ms.append(sec * 1e3 * total_flops / fl)
+    value = statistics.mean(ms)
+    cores = cpu_threads()
+    desc = (f"fp64 NumPy oracle on param {sample[0]} "
+            f"({[(s.rows, s.cols) for s in shards if s.param_id == sample[0]][0]}) + the {tail_n}-element tail "
+            f"per step, scaled by dense Newton-Schulz FLOPs to the {len(shards)}-matrix owner set")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "matrices": len(shards),
+                       "elements": sum(s.rows * s.cols for s in shards), "ns_steps": w.ns_steps},
+            "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.get(args.workload)
+
+    from matrix_optimizers_under_gb300 import _build
+    _build.ensure_built()
+    from matrix_optimizers_under_gb300 import binding as mfsdp
+
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    heavy = heaviest_rank(plan)
+    sim_rank = heavy if world == 1 else (heavy + rank) % w.world
+    shards = plan.rank_matrices(sim_rank)
+    tails = plan.rank_tails(sim_rank)
+    numel = plan.rank_matrix_elems[sim_rank]
+    tail_numel = plan.rank_tail_elems[sim_rank]
+
+    t_gen = time.time()
+    grad_np = generate_grads(w, shards, numel)       # before any CUDA call (spawn pool)
+    t_gen = time.time() - t_gen
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+
+    bf16 = w.grad_dtype == "bf16"
+    grad_host = torch.from_numpy(grad_np.view(np.int16) if bf16 else grad_np).pin_memory()
+    grad_host = grad_host.view(torch.bfloat16) if bf16 else grad_host
+    grad = grad_host.to(dev)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    rng = np.random.default_rng(w.seed)
+    tp = torch.from_numpy((rng.standard_normal(max(tail_numel, 1)) * w.tail_scale).astype(np.float32)).to(dev)
+    tg_host = torch.from_numpy((rng.standard_normal(max(tail_numel, 1)) * w.tail_scale)
+                               .astype(np.float32)).pin_memory()
+    tg = tg_host.to(dev)
+    tm, tv = torch.zeros_like(tp), torch.zeros_like(tp)
+    upd_host = torch.empty(numel, dtype=torch.bfloat16).pin_memory()
+    tp_host = torch.empty_like(tg_host).pin_memory()
+    a, b, c = w.ns_coeffs
+    kw = dict(beta=w.beta, nesterov=w.nesterov, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
+    batches = math.ceil(len(shards) / 128) if shards else 0
+    launches_per_step = (2 * batches + (3 * w.ns_steps if w.ns_steps else 1) * batches + (1 if tail_numel else 0))
+
+    step_counter = [0]
+
+    def one_step(ev=None):
+        step_counter[0] += 1
+        if ev:
+            ev[0].record(stream)
+        mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
+        if ev:
+            ev[1].record(stream)
+        mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_NEWTON_SCHULZ, **kw)
+        if ev:
+            ev[2].record(stream)
+        if tail_numel:
+            mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
+                                  wd=w.weight_decay, step=step_counter[0])
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    st, detail = mfsdp.muon_device_status(ws)
+    if st != mfsdp.OK:
+        raise RuntimeError(f"device status after warm-up: {mfsdp.status_string(st)} ({detail})")
+
+    # ---------------------------------------------------------- timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.4)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        one_step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    mom_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    ns_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    adam_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    step_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    st, detail = mfsdp.muon_device_status(ws)
+    if st != mfsdp.OK:
+        raise RuntimeError(f"device status after timed region: {mfsdp.status_string(st)} ({detail})")
+
+    # ---------------------------------------------------------- end to end
+    e2e_steps = max(1, min(args.steps, 5))
+    h2d = grad_host.numel() * grad_host.element_size() + (tg_host.numel() * 4 if tail_numel else 0)
+    d2h = upd_host.numel() * 2 + (tp_host.numel() * 4 if tail_numel else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        grad.copy_(grad_host, non_blocking=True)
+        if tail_numel:
+            tg.copy_(tg_host, non_blocking=True)
+        one_step()
+        upd_host.copy_(upd, non_blocking=True)
+        if tail_numel:
+            tp_host.copy_(tp, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---------------------------------------------------------- supplementary: a large AdamW tail
+    sup = {}
+    if rank == 0 and not args.no_supplementary:
+        n_big = 50_000_000
+        bp = torch.randn(n_big, device=dev) * 1e-3
+        bg = torch.randn(n_big, device=dev) * 1e-3
+        bm, bv = torch.zeros_like(bp), torch.zeros_like(bp)
+        for i in range(3):
+            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=i + 1)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for i in range(reps):
+            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=4 + i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        a_ms = s0.elapsed_time(s1) / reps
+        sup["adamw_50M"] = {"ms": round(a_ms, 4), "gbs": round(28 * n_big / a_ms / 1e6, 1)}
+        del bp, bg, bm, bv
+
+    # ---------------------------------------------------------- figures
+    peaks, peak_src = load_peaks()
+    flops = sum(ns_flops(s.rows, s.cols, w.ns_steps) for s in shards)
+    elems = sum(s.rows * s.cols for s in shards)
+    gsz = 2 if bf16 else 4
+    mom_bytes = elems * (gsz + 4 + 4 + 2)
+    ns_tflops = flops / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
+    mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
+    adam_gbs = 28 * tail_numel / (adam_ms * 1e-3) / 1e9 if adam_ms > 0 and tail_numel else 0.0
+    peak_tf = peaks["bf16_tflops_sustained"]
+    hbm = peaks["hbm_gbs"]
+    ns_launches = 3 * w.ns_steps * batches
+    if "adamw_50M" in sup:
+        sup["adamw_50M"]["frac_hbm"] = round(sup["adamw_50M"]["gbs"] / hbm, 4)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = pick_sample(shards)
+        sec, fl, el = oracle_sample(w, shards, 0, sample)
+        est_ms = sec * 1e3 * flops / fl
+        desc = (f"fp64 NumPy oracle (momentum + Newton-Schulz) on params {sample} "
+                f"{[(s.rows, s.cols) for s in shards if s.param_id in sample]} of the benched owner set, "
+                f"{sec:.1f} s, scaled by dense Newton-Schulz FLOPs to all {len(shards)} matrices")
+        cpu = {"value": round(est_ms, 1), "unit": "ms", "cores": cpu_threads(), "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": round(step_ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "simulated_rank": sim_rank, "planner_world": w.world,
+                   "matrices": len(shards), "elements": elems, "ns_steps": w.ns_steps,
+                   "grad_dtype": w.grad_dtype, "update_dtype": "bf16", "tail_elems": tail_numel,
+                   "grad_dist": w.grad_dist,
+                   "l2": f"no flush: inputs {(grad_np.nbytes + 4 * numel + ws.numel()) / 1e9:.1f} GB > 129 MB L2",
+                   "parallelism": f"owner sets x{world}"},
+        "phases": {"momentum_ms": round(mom_ms, 4), "momentum_gbs": round(mom_gbs, 1),
+                   "momentum_frac_hbm": round(mom_gbs / hbm, 4),
+                   "newton_schulz_ms": round(ns_ms, 4), "newton_schulz_tflops": round(ns_tflops, 1),
+                   "newton_schulz_frac_bf16": round(ns_tflops / peak_tf, 4),
+                   "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1)},
+        "roofline": {"kernel": "ns_gemm_kernel", "bound": "tensor", "achieved": round(ns_tflops, 1),
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops / peak_tf, 4), "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained",
+                     "flops_per_launch": round(flops / max(ns_launches, 1)), "launches_per_step": ns_launches},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+        "supplementary": sup,
+        "input_generation_s": round(t_gen, 1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama3_8b_rank", choices=W.ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-supplementary", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

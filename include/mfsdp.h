@@ -133,8 +133,12 @@ size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_sh
  *   ns_steps times:  A = X X^T,  B = b*A + c*A*A,  X <- a*X + B*X
  *   update[offset ..] = X, transposed back to rows x cols.
  * The Newton-Schulz products run on tensor cores with bf16 operands and fp32
- * accumulation; A, B and X are held in bf16 between products.  A matrix whose
- * momentum is exactly zero gets an all-zero update.
+ * accumulation; A, B and X are held in bf16 between products, and the
+ * hyper-parameters are applied as fp32 values rounded from the doubles given.
+ * A matrix whose momentum is exactly zero gets an all-zero update.  The fp32
+ * Gram product needs ||U||_F < 1e18 and the entries of U above ~1e-18 in
+ * magnitude (outside that range the result may be Inf/NaN or lose the small
+ * entries).
  *
  * shards[n_shards]  host array; segments must not overlap.  owner is ignored.
  * grad              device, `numel` elements of grad_dtype (F32 or BF16).
@@ -154,9 +158,31 @@ int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards,
                           float* momentum,
                           void* update, int32_t update_dtype,
                           int64_t numel,
-                          float beta, int32_t nesterov, int32_t ns_steps,
-                          float a, float b, float c, float eps,
+                          double beta, int32_t nesterov, int32_t ns_steps,
+                          double a, double b, double c, double eps,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same step split in two, for callers that interleave other work or time
+ * the phases separately: `phases` is a bit set of
+ *   MFSDP_PHASE_MOMENTUM        momentum, segment view and norm (writes
+ *                               momentum and the workspace; clears its status word)
+ *   MFSDP_PHASE_NEWTON_SCHULZ   the Newton-Schulz products and the update
+ *                               (reads what the momentum phase left in the workspace)
+ * Calling MOMENTUM then NEWTON_SCHULZ with identical arguments on one stream
+ * gives bit-identical results to mfsdp_muon_owner_step (phases = both).
+ * Same arguments and errors as mfsdp_muon_owner_step, plus INVALID_ARG for an
+ * empty or unknown phase set. */
+#define MFSDP_PHASE_MOMENTUM 1
+#define MFSDP_PHASE_NEWTON_SCHULZ 2
+int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                                 const void* grad, int32_t grad_dtype,
+                                 float* momentum,
+                                 void* update, int32_t update_dtype,
+                                 int64_t numel,
+                                 double beta, int32_t nesterov, int32_t ns_steps,
+                                 double a, double b, double c, double eps,
+                                 void* workspace, size_t workspace_bytes, void* stream,
+                                 int32_t phases);
 
 /* Reads the device status word a previous mfsdp_muon_owner_step left in
  * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
@@ -178,11 +204,13 @@ int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int32_t n_shar
  *   p <- p*(1 - lr*wd); m <- b1*m + (1-b1)*g; v <- b2*v + (1-b2)*g^2;
  *   p <- p - lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
  * p, m, v read and written in place; g read.  All device, n fp32 elements,
- * 16-byte aligned, not overlapping (n == 0 is a no-op).  Errors: INVALID_ARG
+ * 16-byte aligned, not overlapping (n == 0 is a no-op).  The kernel computes
+ * in fp32 with 1-b1, 1-b2, 1-lr*wd, lr/(1-b1^step) and 1/sqrt(1-b2^step)
+ * formed in double on the host.  Errors: INVALID_ARG
  * (null pointer, n < 0, step < 1, beta outside [0, 1)), MISALIGNED, OVERLAP,
  * CUDA_ERROR. */
 int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t n,
-                          float lr, float beta1, float beta2, float eps, float wd,
+                          double lr, double beta1, double beta2, double eps, double wd,
                           int64_t step, void* stream);
 
 /* Static description of a status code (never NULL). */

@@ -33,7 +33,10 @@ DTYPE_BF16 = 1
 KIND_MATRIX = 0
 KIND_TAIL = 1
 
-EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step",
+PHASE_MOMENTUM = 1
+PHASE_NEWTON_SCHULZ = 2
+
+EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version")
 
@@ -61,7 +64,7 @@ class TailShard(ctypes.Structure):
         return dict(param_id=self.param_id, owner=self.owner, offset=self.offset, numel=self.numel)
 
 
-_i32, _i64, _u64, _f, _vp, _sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float,
+_i32, _i64, _u64, _d, _vp, _sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_double,
                                   ctypes.c_void_p, ctypes.c_size_t)
 _lib.mfsdp_plan_owners.argtypes = [ctypes.POINTER(CParam), _i32, _i32, _i32, _i64, ctypes.POINTER(MatrixShard),
                                    ctypes.POINTER(_i32), ctypes.POINTER(TailShard), ctypes.POINTER(_i32),
@@ -71,12 +74,15 @@ _lib.mfsdp_muon_workspace_bytes.argtypes = [ctypes.POINTER(MatrixShard), _i32]
 _lib.mfsdp_muon_workspace_bytes.restype = _sz
 _lib.mfsdp_muon_workspace_layout.argtypes = [ctypes.POINTER(MatrixShard), _i32, ctypes.POINTER(_i64)]
 _lib.mfsdp_muon_workspace_layout.restype = ctypes.c_int
-_lib.mfsdp_muon_owner_step.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _i64, _f, _i32,
-                                       _i32, _f, _f, _f, _f, _vp, _sz, _vp]
+_STEP_ARGS = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _i64, _d, _i32, _i32, _d, _d, _d, _d,
+              _vp, _sz, _vp]
+_lib.mfsdp_muon_owner_step.argtypes = _STEP_ARGS
 _lib.mfsdp_muon_owner_step.restype = ctypes.c_int
+_lib.mfsdp_muon_owner_step_phases.argtypes = _STEP_ARGS + [_i32]
+_lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
 _lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.mfsdp_muon_device_status.restype = ctypes.c_int
-_lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _f, _f, _f, _f, _f, _i64, _vp]
+_lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _d, _d, _d, _d, _d, _i64, _vp]
 _lib.mfsdp_adamw_tail_step.restype = ctypes.c_int
 _lib.mfsdp_status_string.argtypes = [ctypes.c_int]
 _lib.mfsdp_status_string.restype = ctypes.c_char_p
@@ -188,19 +194,24 @@ def _stream(stream) -> Optional[int]:
 
 def muon_owner_step(shards: Sequence[MatrixShard], grad, momentum, update, workspace, *, beta: float = 0.95,
                     nesterov: bool = False, ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315),
-                    eps: float = 1e-7, numel: Optional[int] = None, stream=None) -> None:
+                    eps: float = 1e-7, numel: Optional[int] = None, stream=None,
+                    phases: int = PHASE_MOMENTUM | PHASE_NEWTON_SCHULZ) -> None:
     """One owner-local Muon step over the shards of one rank (see include/mfsdp.h).
 
     grad: flat fp32/bf16 CUDA tensor; momentum: flat fp32; update: flat fp32/bf16;
-    workspace: CUDA uint8 tensor of at least muon_workspace_bytes(shards) bytes."""
+    workspace: CUDA uint8 tensor of at least muon_workspace_bytes(shards) bytes.
+    phases: both (default, mfsdp_muon_owner_step) or one of PHASE_MOMENTUM /
+    PHASE_NEWTON_SCHULZ (mfsdp_muon_owner_step_phases)."""
     arr = _shard_array(shards)
     n = int(numel if numel is not None else grad.numel())
     a, b, c = coeffs
-    _check(_lib.mfsdp_muon_owner_step(arr, len(shards), _ptr(grad), _dtype_code(grad), _ptr(momentum), _ptr(update),
-                                      _dtype_code(update), n, float(beta), int(bool(nesterov)), int(ns_steps),
-                                      float(a), float(b), float(c), float(eps), _ptr(workspace),
-                                      int(workspace.numel() if workspace is not None else 0), _stream(stream)),
-           "muon_owner_step")
+    args = (arr, len(shards), _ptr(grad), _dtype_code(grad), _ptr(momentum), _ptr(update), _dtype_code(update), n,
+            float(beta), int(bool(nesterov)), int(ns_steps), float(a), float(b), float(c), float(eps),
+            _ptr(workspace), int(workspace.numel() if workspace is not None else 0), _stream(stream))
+    if phases == PHASE_MOMENTUM | PHASE_NEWTON_SCHULZ:
+        _check(_lib.mfsdp_muon_owner_step(*args), "muon_owner_step")
+    else:
+        _check(_lib.mfsdp_muon_owner_step_phases(*args, int(phases)), "muon_owner_step_phases")
 
 
 def muon_device_status(workspace, stream=None) -> Tuple[int, int]:

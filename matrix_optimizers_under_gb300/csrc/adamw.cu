@@ -3,7 +3,7 @@
 // MatrixFSDP: Communication-Free Matrix Optimizers Under ZeRO-3 Parameter
 // Sharding -- Abstract: non-matrix tensors are packed into tail owners and stay
 // on AdamW.  Decoupled weight decay (PyTorch order), bias corrections folded
-// into two scalars computed on the host in double precision.
+// into scalars computed on the host in double precision.
 //
 // One pass over HBM: read p, g, m, v and write p, m, v (28 bytes per element),
 // 128-bit streaming loads/stores, a grid-stride loop over a grid that is a
@@ -14,10 +14,6 @@
 
 namespace mfsdp {
 namespace {
-
-struct AdamScalars {
-  float decay, beta1, beta2, omb1, omb2, step_size, inv_sqrt_bc2, eps;
-};
 
 __device__ __forceinline__ void adam1(float& p, float g, float& m, float& v, const AdamScalars& k) {
   p *= k.decay;
@@ -73,8 +69,8 @@ __global__ void __launch_bounds__(256) adamw_kernel(float* __restrict__ p, const
 
 }  // namespace
 
-cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, float decay, float beta1,
-                         float beta2, float step_size, float inv_sqrt_bc2, float eps, cudaStream_t s) {
+cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, const AdamScalars& k,
+                         cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -85,7 +81,6 @@ cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n
   const int64_t want = (n4 + 2 * 256 - 1) / (2 * 256);       // two float4 groups per thread
   int64_t blocks = std::min<int64_t>(want, (int64_t)sms * 8);  // 8 resident CTAs of 256 per SM
   if (blocks < 1) blocks = 1;
-  AdamScalars k{decay, beta1, beta2, 1.0f - beta1, 1.0f - beta2, step_size, inv_sqrt_bc2, eps};
   adamw_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, g, m, v, n, k);
   return cudaGetLastError();
 }

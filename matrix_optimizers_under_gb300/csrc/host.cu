@@ -97,6 +97,13 @@ size_t dtype_size(int32_t dt) { return dt == MFSDP_DTYPE_BF16 ? 2 : 4; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_CUDA; }
 
+int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
+                          int32_t grad_dtype, float* momentum, float beta, int32_t nesterov, float eps, uint8_t* ws,
+                          cudaStream_t stream);
+int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, void* update,
+                    int32_t update_dtype, int32_t ns_steps, float a, float b, float c, uint8_t* ws,
+                    cudaStream_t stream);
+
 }  // namespace
 }  // namespace mfsdp
 
@@ -140,19 +147,23 @@ extern "C" int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int
   return MFSDP_OK;
 }
 
-extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad,
-                                     int32_t grad_dtype, float* momentum, void* update, int32_t update_dtype,
-                                     int64_t numel, float beta, int32_t nesterov, int32_t ns_steps, float a,
-                                     float b, float c, float eps, void* workspace, size_t workspace_bytes,
-                                     void* stream_ptr) {
+extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                                            const void* grad, int32_t grad_dtype, float* momentum, void* update,
+                                            int32_t update_dtype, int64_t numel, double beta_d, int32_t nesterov,
+                                            int32_t ns_steps, double a_d, double b_d, double c_d, double eps_d,
+                                            void* workspace, size_t workspace_bytes, void* stream_ptr,
+                                            int32_t phases) {
   // ------------------------------------------------------------ validation
+  if (phases <= 0 || (phases & ~(MFSDP_PHASE_MOMENTUM | MFSDP_PHASE_NEWTON_SCHULZ)) != 0)
+    return MFSDP_ERR_INVALID_ARG;
   if (n_shards < 0 || (n_shards > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
+  if (!std::isfinite(beta_d) || !std::isfinite(a_d) || !std::isfinite(b_d) || !std::isfinite(c_d) ||
+      !std::isfinite(eps_d) || eps_d < 0.0)
+    return MFSDP_ERR_INVALID_ARG;
+  const float beta = (float)beta_d, a = (float)a_d, b = (float)b_d, c = (float)c_d, eps = (float)eps_d;
   if (grad_dtype != MFSDP_DTYPE_F32 && grad_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
   if (update_dtype != MFSDP_DTYPE_F32 && update_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
   if (numel < 0 || ns_steps < 0 || ns_steps > 64 || (nesterov != 0 && nesterov != 1)) return MFSDP_ERR_INVALID_ARG;
-  if (!std::isfinite(beta) || !std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) ||
-      eps < 0.f)
-    return MFSDP_ERR_INVALID_ARG;
   if (n_shards == 0) return MFSDP_OK;
   if (!grad || !momentum || !update || !workspace) return MFSDP_ERR_INVALID_ARG;
   if (!aligned(grad, 16) || !aligned(momentum, 16) || !aligned(update, 16) || !aligned(workspace, 256))
@@ -187,15 +198,39 @@ extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  if (phases & MFSDP_PHASE_MOMENTUM) {
+    st = launch_momentum_phase(shards, n_shards, L, grad, grad_dtype, momentum, beta, nesterov, eps, ws, stream);
+    if (st != MFSDP_OK) return st;
+  }
+  if (phases & MFSDP_PHASE_NEWTON_SCHULZ) {
+    st = launch_ns_phase(shards, n_shards, L, update, update_dtype, ns_steps, a, b, c, ws, stream);
+    if (st != MFSDP_OK) return st;
+  }
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad,
+                                     int32_t grad_dtype, float* momentum, void* update, int32_t update_dtype,
+                                     int64_t numel, double beta, int32_t nesterov, int32_t ns_steps, double a,
+                                     double b, double c, double eps, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return mfsdp_muon_owner_step_phases(shards, n_shards, grad, grad_dtype, momentum, update, update_dtype, numel,
+                                      beta, nesterov, ns_steps, a, b, c, eps, workspace, workspace_bytes, stream,
+                                      MFSDP_PHASE_MOMENTUM | MFSDP_PHASE_NEWTON_SCHULZ);
+}
+
+namespace mfsdp {
+namespace {
+
+int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
+                          int32_t grad_dtype, float* momentum, float beta, int32_t nesterov, float eps, uint8_t* ws,
+                          cudaStream_t stream) {
   float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
   float* partials = reinterpret_cast<float*>(ws + L.partial_off);
-  int32_t* status = reinterpret_cast<int32_t*>(ws);
-  const size_t gsz = dtype_size(grad_dtype), usz = dtype_size(update_dtype);
-
-  st = cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  const size_t gsz = dtype_size(grad_dtype);
+  int st = cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
   if (st != MFSDP_OK) return st;
-
-  // ---------------------------------------------- momentum + segment view
   for (int base = 0; base < n_shards; base += kMaxBatch) {
     const int cnt = std::min(kMaxBatch, n_shards - base);
     MomBatch mb;
@@ -243,8 +278,16 @@ extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n
     st = cuda_status(launch_norm_finalize(nb, stream));
     if (st != MFSDP_OK) return st;
   }
+  return MFSDP_OK;
+}
 
-  // ---------------------------------------------------------- ns_steps == 0
+int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, void* update,
+                    int32_t update_dtype, int32_t ns_steps, float a, float b, float c, uint8_t* ws,
+                    cudaStream_t stream) {
+  float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  const size_t usz = dtype_size(update_dtype);
+  int st = MFSDP_OK;
   if (ns_steps == 0) {
     for (int base = 0; base < n_shards; base += kMaxBatch) {
       const int cnt = std::min(kMaxBatch, n_shards - base);
@@ -336,6 +379,9 @@ extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n
   return MFSDP_OK;
 }
 
+}  // namespace
+}  // namespace mfsdp
+
 extern "C" int mfsdp_muon_device_status(const void* workspace, void* stream_ptr, int32_t* detail) {
   if (!workspace) return MFSDP_ERR_INVALID_ARG;
   int32_t word = 0;
@@ -347,10 +393,11 @@ extern "C" int mfsdp_muon_device_status(const void* workspace, void* stream_ptr,
   return word ? MFSDP_ERR_DEVICE_TIMEOUT : MFSDP_OK;
 }
 
-extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t n, float lr, float beta1,
-                                     float beta2, float eps, float wd, int64_t step, void* stream_ptr) {
+extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t n, double lr,
+                                     double beta1, double beta2, double eps, double wd, int64_t step,
+                                     void* stream_ptr) {
   if (n < 0 || step < 1) return MFSDP_ERR_INVALID_ARG;
-  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f)) return MFSDP_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0)) return MFSDP_ERR_INVALID_ARG;
   if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd)) return MFSDP_ERR_INVALID_ARG;
   if (n == 0) return MFSDP_OK;
   if (!p || !g || !m || !v) return MFSDP_ERR_INVALID_ARG;
@@ -360,11 +407,16 @@ extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* 
   for (int i = 0; i < 4; ++i)
     for (int j = i + 1; j < 4; ++j)
       if (ranges_overlap(bufs[i], nb, bufs[j], nb)) return MFSDP_ERR_OVERLAP;
-  const double bc1 = 1.0 - std::pow((double)beta1, (double)step);
-  const double bc2 = 1.0 - std::pow((double)beta2, (double)step);
-  const float decay = (float)(1.0 - (double)lr * (double)wd);
-  const float step_size = (float)((double)lr / bc1);
-  const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
-  return cuda_status(launch_adamw(p, g, m, v, n, decay, beta1, beta2, step_size, inv_sqrt_bc2, eps,
-                                  static_cast<cudaStream_t>(stream_ptr)));
+  const double bc1 = 1.0 - std::pow(beta1, (double)step);
+  const double bc2 = 1.0 - std::pow(beta2, (double)step);
+  AdamScalars k;
+  k.decay = (float)(1.0 - lr * wd);
+  k.beta1 = (float)beta1;
+  k.beta2 = (float)beta2;
+  k.omb1 = (float)(1.0 - beta1);
+  k.omb2 = (float)(1.0 - beta2);
+  k.step_size = (float)(lr / bc1);
+  k.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  k.eps = (float)eps;
+  return cuda_status(launch_adamw(p, g, m, v, n, k, static_cast<cudaStream_t>(stream_ptr)));
 }

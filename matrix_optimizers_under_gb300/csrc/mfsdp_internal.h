@@ -128,8 +128,16 @@ cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
 cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s);
-cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, float decay,
-                         float beta1, float beta2, float step_size, float inv_sqrt_bc2, float eps,
+// fp32 scalars of one AdamW step, formed in double on the host.
+struct AdamScalars {
+  float decay;         // 1 - lr*wd
+  float beta1, beta2;
+  float omb1, omb2;    // 1 - beta1, 1 - beta2
+  float step_size;     // lr / (1 - beta1^step)
+  float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^step)
+  float eps;
+};
+cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, const AdamScalars& k,
                          cudaStream_t s);
 
 }  // namespace mfsdp

@@ -172,6 +172,26 @@ def _rng(w: Workload, param_id: int, salt: int = 0) -> np.random.Generator:
     return np.random.default_rng([w.seed, param_id, salt])
 
 
+def _student_t_polar(rng: np.random.Generator, n: int, nu: float) -> np.ndarray:
+    """n Student-t(nu) variates in fp32 by Bailey's polar method (Bailey 1994,
+    Math. Comp. 62): (U, V) uniform on the square (-1, 1)^2 kept when
+    W = U^2 + V^2 < 1, then T = U * sqrt(nu * (W^(-2/nu) - 1) / W)."""
+    out = np.empty(n, np.float32)
+    got = 0
+    while got < n:
+        m = int((n - got) * 1.3) + 1024
+        u = rng.random(m, dtype=np.float32) * np.float32(2.0) - np.float32(1.0)
+        v = rng.random(m, dtype=np.float32) * np.float32(2.0) - np.float32(1.0)
+        wsq = u * u + v * v
+        keep = (wsq < 1.0) & (wsq > 0.0)
+        u, wsq = u[keep], wsq[keep]
+        t = u * np.sqrt(np.float32(nu) * (np.power(wsq, np.float32(-2.0 / nu)) - np.float32(1.0)) / wsq)
+        k = min(t.size, n - got)
+        out[got:got + k] = t[:k]
+        got += k
+    return out
+
+
 def grad_f32(w: Workload, param_id: int) -> np.ndarray:
     """fp32 gradient of one parameter, shape (rows, cols) (tail tensors: (numel,))."""
     p = w.params[param_id]
@@ -184,10 +204,7 @@ def grad_f32(w: Workload, param_id: int) -> np.ndarray:
     if w.grad_dist == "normal":
         x = rng.standard_normal(shape, dtype=np.float32)
     elif w.grad_dist == "student_t3":
-        # Student-t with nu=3 as Z / sqrt(chi2_3 / 3), chi2_3 = 2 * Gamma(3/2, 1).
-        z = rng.standard_normal(shape, dtype=np.float32)
-        g = rng.standard_gamma(np.float32(1.5), size=shape, dtype=np.float32)
-        x = z / np.sqrt(g * np.float32(2.0 / 3.0))
+        x = _student_t_polar(rng, p.numel, 3.0).reshape(shape)
     else:
         raise ValueError(w.grad_dist)
     return x * np.float32(w.grad_scale)

@@ -8,7 +8,10 @@ import numpy as np
 from matrix_optimizers_under_gb300 import workloads as W
 
 # Tolerances (derived in the design notes from the arithmetic):
-NS_REL_FRO = 2e-2      # Newton-Schulz: bf16 operands, fp32 accumulate, 5 iterations
+NS_REL_FRO = 2e-2      # Newton-Schulz: bf16 operands, fp32 accumulate, 5 iterations (s >= 64)
+NS_REL_FRO_SMALL = 1e-1  # s < 64: bf16 rounding of A puts an absolute error on the small
+                         # singular values that the quintic's steep slope near 0
+                         # amplifies, with no averaging over many singular values
 ADAM_REL = 1e-5        # AdamW: fp32 arithmetic against fp64
 ADAM_FLOOR = 1e-2      # relative-error floor: fraction of max |reference|
 MOM_REL = 4e-7         # momentum: one fp32 rounding of beta*M + G (2^-23 ~ 1.2e-7, x3 slack)
@@ -19,6 +22,10 @@ def rel_fro(x, ref) -> float:
     ref = np.asarray(ref, np.float64)
     nr = np.linalg.norm(ref)
     return float(np.linalg.norm(x - ref) / nr) if nr > 0 else float(np.linalg.norm(x))
+
+
+def ns_tol(rows: int, cols: int) -> float:
+    return NS_REL_FRO if min(rows, cols) >= 64 else NS_REL_FRO_SMALL
 
 
 def adam_err(x, ref) -> float:

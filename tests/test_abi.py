@@ -106,12 +106,15 @@ G, M, U, WS = 0x10000000, 0x20000000, 0x30000000, 0x40000000   # fake, aligned, 
 
 
 def step(mfsdp, shards, grad=G, gdt=BF, mom=M, upd=U, udt=BF, numel=1 << 20, ns=5, ws=WS, wsb=None,
-         beta=0.95, nesterov=0, eps=1e-7):
+         beta=0.95, nesterov=0, eps=1e-7, phases=None):
     arr = (mfsdp.MatrixShard * max(len(shards), 1))(*shards)
     if wsb is None:
         wsb = mfsdp.muon_workspace_bytes(shards) if shards else 0
-    return mfsdp.raw_lib().mfsdp_muon_owner_step(arr, len(shards), grad, gdt, mom, upd, udt, numel, beta, nesterov,
-                                                 ns, 3.4445, -4.775, 2.0315, eps, ws, wsb, None)
+    args = (arr, len(shards), grad, gdt, mom, upd, udt, numel, beta, nesterov, ns, 3.4445, -4.775, 2.0315, eps, ws,
+            wsb, None)
+    if phases is None:
+        return mfsdp.raw_lib().mfsdp_muon_owner_step(*args)
+    return mfsdp.raw_lib().mfsdp_muon_owner_step_phases(*args, phases)
 
 
 def test_step_error_paths(mfsdp):
@@ -141,6 +144,12 @@ def test_step_error_paths(mfsdp):
     assert step(mfsdp, ok, upd=G, udt=F32) == mfsdp.ERR_OVERLAP        # same address, different dtype
     assert step(mfsdp, ok, ws=G) == mfsdp.ERR_OVERLAP
     assert step(mfsdp, ok, wsb=mfsdp.muon_workspace_bytes(ok) - 1) == mfsdp.ERR_WORKSPACE_TOO_SMALL
+    # the phase-split entry point checks the same arguments, plus the phase set
+    assert step(mfsdp, ok, phases=0) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, phases=4) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, ok, phases=mfsdp.PHASE_MOMENTUM, grad=G + 2) == mfsdp.ERR_MISALIGNED
+    assert step(mfsdp, ok, phases=mfsdp.PHASE_NEWTON_SCHULZ, ns=-1) == mfsdp.ERR_INVALID_ARG
+    assert step(mfsdp, [], phases=mfsdp.PHASE_NEWTON_SCHULZ, grad=None, mom=None, upd=None, ws=None) == mfsdp.OK
 
 
 def test_adamw_error_paths(mfsdp):

@@ -76,7 +76,7 @@ def check_matrix(s, upd, mom, grad_np, mom0, *, ns_steps, beta=0.95, nesterov=Fa
         return 0.0
     err = H.rel_fro(O, O_ref)
     assert np.all(np.isfinite(O)), f"non-finite update param {s.param_id}"
-    assert err <= H.NS_REL_FRO, f"param {s.param_id} {s.rows}x{s.cols}: rel Frobenius error {err:.3e}"
+    assert err <= H.ns_tol(s.rows, s.cols), f"param {s.param_id} {s.rows}x{s.cols}: rel Frobenius error {err:.3e}"
     return err
 
 
@@ -247,6 +247,25 @@ def test_equivalence_owner_set_vs_standalone(mfsdp):
                              update_dtype=torch.bfloat16)
         assert np.array_equal(u1.view(np.uint32), upd[s.offset:s.offset + n].view(np.uint32))
         assert np.array_equal(m1, mom[s.offset:s.offset + n])
+
+
+def test_phase_split_matches_full_step(mfsdp):
+    """Momentum phase then Newton-Schulz phase == one full step, bitwise."""
+    dev = _dev()
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    u1, m1, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.bfloat16)
+    g = to_dev_grad(grad)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.full((numel,), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step(shards, g, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM)
+    mfsdp.muon_owner_step(shards, g, mom, upd, ws, phases=mfsdp.PHASE_NEWTON_SCHULZ)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(upd).view(np.uint32), u1.view(np.uint32))
+    assert np.array_equal(mom.cpu().numpy(), m1)
 
 
 def test_determinism(mfsdp):
