@@ -184,6 +184,38 @@ int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_sha
                                  void* workspace, size_t workspace_bytes, void* stream,
                                  int32_t phases);
 
+/* mfsdp_muon_owner_step for callers that cannot allocate device memory (no
+ * counterpart in the paper: an addition of this library).  Some callers have
+ * no allocator to provide the workspace from -- a plug-in inside a framework
+ * that owns all device memory through its own pool, a callback that must not
+ * allocate, a C program linking only this library.  This entry point takes no
+ * workspace: its scratch is a file-scope device array of
+ * MFSDP_STATIC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  It calls no cudaMalloc/cudaFree and nothing that
+ * allocates.
+ *   - Same arguments, semantics and errors as mfsdp_muon_owner_step without
+ *     workspace/workspace_bytes; an owner set whose
+ *     mfsdp_muon_workspace_bytes() exceeds MFSDP_STATIC_SCRATCH_BYTES is
+ *     rejected with MFSDP_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (the step clears what must start at zero itself).  Calls whose
+ *     work overlaps on the GPU (different streams, or different host threads
+ *     without ordering) race on it: serialise them.
+ *   - The device status word of these calls is not readable through
+ *     mfsdp_muon_device_status (the caller holds no workspace pointer). */
+#define MFSDP_STATIC_SCRATCH_BYTES (64u << 20)
+int mfsdp_muon_owner_step_static_scratch(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                                         const void* grad, int32_t grad_dtype,
+                                         float* momentum,
+                                         void* update, int32_t update_dtype,
+                                         int64_t numel,
+                                         double beta, int32_t nesterov, int32_t ns_steps,
+                                         double a, double b, double c, double eps,
+                                         void* stream);
+
 /* Reads the device status word a previous mfsdp_muon_owner_step left in
  * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
  * if one of its kernels gave up on a bounded wait (its outputs are then

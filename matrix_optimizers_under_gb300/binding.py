@@ -38,7 +38,9 @@ PHASE_NEWTON_SCHULZ = 2
 
 EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
-            "mfsdp_status_string", "mfsdp_version")
+            "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch")
+
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 class CParam(ctypes.Structure):
@@ -80,6 +82,8 @@ _lib.mfsdp_muon_owner_step.argtypes = _STEP_ARGS
 _lib.mfsdp_muon_owner_step.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_phases.argtypes = _STEP_ARGS + [_i32]
 _lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
+_lib.mfsdp_muon_owner_step_static_scratch.argtypes = _STEP_ARGS[:15] + [_vp]
+_lib.mfsdp_muon_owner_step_static_scratch.restype = ctypes.c_int
 _lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.mfsdp_muon_device_status.restype = ctypes.c_int
 _lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _d, _d, _d, _d, _d, _i64, _vp]
@@ -212,6 +216,22 @@ def muon_owner_step(shards: Sequence[MatrixShard], grad, momentum, update, works
         _check(_lib.mfsdp_muon_owner_step(*args), "muon_owner_step")
     else:
         _check(_lib.mfsdp_muon_owner_step_phases(*args, int(phases)), "muon_owner_step_phases")
+
+
+def muon_owner_step_static_scratch(shards: Sequence[MatrixShard], grad, momentum, update, *, beta: float = 0.95,
+                                   nesterov: bool = False, ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315),
+                                   eps: float = 1e-7, numel: Optional[int] = None, stream=None) -> None:
+    """The owner step for callers that cannot allocate device memory: no
+    workspace argument; the library's fixed STATIC_SCRATCH_BYTES device array
+    serves as scratch (see include/mfsdp.h).  Calls that overlap on the GPU race."""
+    arr = _shard_array(shards)
+    n = int(numel if numel is not None else grad.numel())
+    a, b, c = coeffs
+    _check(_lib.mfsdp_muon_owner_step_static_scratch(arr, len(shards), _ptr(grad), _dtype_code(grad), _ptr(momentum),
+                                                     _ptr(update), _dtype_code(update), n, float(beta),
+                                                     int(bool(nesterov)), int(ns_steps), float(a), float(b), float(c),
+                                                     float(eps), _stream(stream)),
+           "muon_owner_step_static_scratch")
 
 
 def muon_device_status(workspace, stream=None) -> Tuple[int, int]:
