@@ -71,8 +71,8 @@ int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
   L->norm_off = off;
   off = round_up(off + sizeof(float2) * (size_t)n, 256);
   L->partial_off = off;
-  L->partials = partials;
-  off = round_up(off + sizeof(float) * (size_t)partials, 1024);
+  L->partials = partials * kPartialsPerTile;
+  off = round_up(off + sizeof(float) * (size_t)L->partials, 1024);
   for (int i = 0; i < n; ++i) {
     MatLayout& m = L->mats[i];
     const size_t xb = (size_t)m.s_pad * m.l_pad * 2, ab = (size_t)m.s_pad * m.s_pad * 2;
@@ -273,8 +273,8 @@ int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const 
     nb.eps = eps;
     nb.partials = partials;
     nb.norm = norm;
-    for (int k = 0; k < cnt; ++k) nb.start[k] = L.mats[base + k].partial0;
-    nb.start[cnt] = L.mats[base + cnt - 1].partial0 + L.mats[base + cnt - 1].tiles_k1;
+    for (int k = 0; k < cnt; ++k) nb.start[k] = L.mats[base + k].partial0 * kPartialsPerTile;
+    nb.start[cnt] = (L.mats[base + cnt - 1].partial0 + L.mats[base + cnt - 1].tiles_k1) * kPartialsPerTile;
     st = cuda_status(launch_norm_finalize(nb, stream));
     if (st != MFSDP_OK) return st;
   }

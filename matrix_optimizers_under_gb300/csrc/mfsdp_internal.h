@@ -13,6 +13,7 @@ namespace mfsdp {
 
 constexpr int kMaxBatch = 128;     // matrices per grouped launch
 constexpr int kTile = 64;          // momentum-kernel tile edge (elements)
+constexpr int kPartialsPerTile = 8;  // momentum kernel: one norm partial per warp
 constexpr int kPad = 128;          // workspace matrices are padded to multiples of this
 constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows (UMMA M)
 constexpr int kBlockN = 256;       // Newton-Schulz GEMM tile columns (UMMA N)
@@ -21,7 +22,8 @@ constexpr int kStages = 4;         // smem pipeline depth
 constexpr int kStageBytesA = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBytesB = kBlockN * kBlockK * 2;   // 32 KB
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-constexpr int kGemmThreads = 128;
+constexpr int kEpilogueWarps = 4;  // warps 2-5 of the GEMM CTA
+constexpr int kGemmThreads = 64 + 32 * kEpilogueWarps;   // producer warp, MMA warp, epilogue warps
 constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 
 // Bytes between consecutive 64-column blocks of a blocked matrix with rows_pad rows.
@@ -46,7 +48,7 @@ struct MomMat {
   int32_t transposed;
   int32_t vec_ok;      // offset and cols multiples of 8: 16-byte vector access
   int32_t tiles_j;     // l_pad / kTile
-  int32_t partial0;    // first norm-partial slot of this matrix
+  int32_t partial0;    // first tile index of this matrix (its partial slots start at 8x this)
 };
 struct MomBatch {
   int32_t n;

@@ -10,16 +10,17 @@
 // X0 = U / (||U||_F + eps) that Newton-Schulz needs.
 //
 // Each CTA takes one 64 x 64 tile of the Newton-Schulz iterate X0 (s x l, the
-// stored matrix transposed when rows > cols).  It reads the matching stored
-// block of G and M once (16-byte vectors when the segment allows), writes M
-// back, stages U in shared memory, and writes X0 = bf16(U) as eight 1 KB
-// pre-swizzled atoms of the workspace's blocked layout -- transposing through
-// shared memory for tall matrices, so every later GEMM sees the short side
-// first.  The padding up to multiples of 128 is written as zeros.  The per-CTA
-// sum of U^2 (fp32, warp shuffles then a fixed-order block sum) goes to its own
-// slot; the finalise kernel adds a matrix's slots in a fixed order, so the
-// norm is bitwise reproducible.  HBM traffic: 2 (bf16 G) + 4 + 4 (M) + 2 (X0)
-// = 12 bytes per element.
+// stored matrix transposed when rows > cols).  Every thread issues all its
+// loads of the matching stored G and M (16-byte vectors when the segment
+// allows) before using any, writes M back, and writes X0 = bf16(U) into the
+// workspace's blocked, pre-swizzled layout: straight from registers when X0
+// has the stored orientation (each warp fills one 1 KB atom), through a
+// per-warp shared buffer when it is the transpose.  No block-wide barrier.
+// The padding up to multiples of 128 is written as zeros.  Each warp's sum of
+// U^2 (fp32, fixed shuffle order) goes to its own slot; the finalise kernel
+// adds a matrix's slots in a fixed order, so the norm is bitwise
+// reproducible.  HBM traffic: 2 (bf16 G) + 4 + 4 (M) + 2 (X0) = 12 bytes per
+// element.
 #include <cuda_bf16.h>
 
 #include "mfsdp_internal.h"
@@ -43,10 +44,52 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 16 consecutive elements of one stored row: gradient as fp32, momentum.
+struct Row16 {
+  float g[16];
+  float m[16];
+};
+
+__device__ __forceinline__ void load_row16_vec(const MomMat& d, int grad_bf16, int64_t e0, Row16& r) {
+  // All six (bf16) or eight (fp32) 16-byte loads are issued before any use.
+  const float4* mp = reinterpret_cast<const float4*>(d.m + e0);
+  float4 mq[4];
+  if (grad_bf16) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(d.g) + e0);
+    const uint4 q0 = __ldcs(src), q1 = __ldcs(src + 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mq[k] = __ldcs(mp + k);
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      r.g[2 * k] = bf16_bits_to_float(w[k] & 0xFFFFu);
+      r.g[2 * k + 1] = bf16_bits_to_float(w[k] >> 16);
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(d.g) + e0);
+    float4 gq[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) gq[k] = __ldcs(src + k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mq[k] = __ldcs(mp + k);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      r.g[4 * k] = gq[k].x; r.g[4 * k + 1] = gq[k].y; r.g[4 * k + 2] = gq[k].z; r.g[4 * k + 3] = gq[k].w;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    r.m[4 * k] = mq[k].x; r.m[4 * k + 1] = mq[k].y; r.m[4 * k + 2] = mq[k].z; r.m[4 * k + 3] = mq[k].w;
+  }
+}
+
+// One CTA = one 64 x 64 tile of X0; warp w owns stored rows [r0 + 8w, r0 + 8w + 8),
+// lane l row r0 + 8w + l/4 and stored columns [c0 + 16(l%4), +16).  No block-wide
+// barrier: tall matrices are transposed through a per-warp shared buffer, and
+// every warp writes its own norm partial.
 __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ MomBatch p) {
-  __shared__ float tile[kTile][kTile + 1];
-  __shared__ float warp_sum[8];
-  const int t = threadIdx.x;
+  __shared__ __align__(16) uint16_t xpose[8][8][kTile + 8];   // per warp: 8 rows x 64 (+8 pad) bf16
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int mi = find_mat(p.tile_start, p.n, blockIdx.x);
   const MomMat& d = p.mat[mi];
   const int local = blockIdx.x - p.tile_start[mi];
@@ -55,7 +98,7 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
   const int64_t r0 = d.transposed ? j0 : i0;         // matching stored block
   const int64_t c0 = d.transposed ? i0 : j0;
 
-  const int lr = t >> 2, lc = (t & 3) * 16;
+  const int lr = warp * 8 + (lane >> 2), lc = (lane & 3) * 16;
   const int64_t gr = r0 + lr, gc = c0 + lc;
   const float beta = p.beta;
   float u[16];
@@ -63,38 +106,17 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
   if (gr < d.rows && gc < d.cols) {
     const int64_t e0 = gr * d.cols + gc;
     if (d.vec_ok && gc + 16 <= d.cols) {
-      float g[16];
-      if (p.grad_bf16) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(d.g) + e0);
-        const uint4 q0 = __ldcs(src), q1 = __ldcs(src + 1);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      Row16 r;
+      load_row16_vec(d, p.grad_bf16, e0, r);
+      float mn[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          g[2 * k] = bf16_bits_to_float(w[k] & 0xFFFFu);
-          g[2 * k + 1] = bf16_bits_to_float(w[k] >> 16);
-        }
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(d.g) + e0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 q = __ldcs(src + k);
-          g[4 * k] = q.x; g[4 * k + 1] = q.y; g[4 * k + 2] = q.z; g[4 * k + 3] = q.w;
-        }
+      for (int e = 0; e < 16; ++e) {
+        mn[e] = fmaf(beta, r.m[e], r.g[e]);
+        u[e] = p.nesterov ? fmaf(beta, mn[e], r.g[e]) : mn[e];
       }
       float4* mp = reinterpret_cast<float4*>(d.m + e0);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float4 q = __ldcs(mp + k);
-        float mv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float gv = g[4 * k + e];
-          const float mn = fmaf(beta, mv[e], gv);
-          mv[e] = mn;
-          u[4 * k + e] = p.nesterov ? fmaf(beta, mn, gv) : mn;
-        }
-        __stcs(mp + k, make_float4(mv[0], mv[1], mv[2], mv[3]));
-      }
+      for (int k = 0; k < 4; ++k) __stcs(mp + k, make_float4(mn[4 * k], mn[4 * k + 1], mn[4 * k + 2], mn[4 * k + 3]));
     } else {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -103,9 +125,9 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
           const int64_t idx = e0 + e;
           const float gv = p.grad_bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(d.g)[idx])
                                        : static_cast<const float*>(d.g)[idx];
-          const float mn = fmaf(beta, d.m[idx], gv);
-          d.m[idx] = mn;
-          u[e] = p.nesterov ? fmaf(beta, mn, gv) : mn;
+          const float mnv = fmaf(beta, d.m[idx], gv);
+          d.m[idx] = mnv;
+          u[e] = p.nesterov ? fmaf(beta, mnv, gv) : mnv;
         }
       }
     }
@@ -114,43 +136,44 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
     for (int e = 0; e < 16; ++e) u[e] = 0.f;
   }
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    ss = fmaf(u[e], u[e], ss);
-    tile[lr][lc + e] = u[e];
-  }
-  __syncthreads();
-
-  // X0 tile rows [i0, i0+64), columns [j0, j0+64): 64 rows x 8 chunks of 8.
-  const size_t stride = colblock_stride(d.s_pad);
+  for (int e = 0; e < 16; ++e) ss = fmaf(u[e], u[e], ss);
+  uint32_t pk[8];
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int q = t + 256 * it;
-    const int yi = q >> 3, ch = q & 7;
-    float v[8];
+  for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(u[2 * k], u[2 * k + 1]);
+
+  if (!d.transposed) {
+    // X0 row = stored row: two 16-byte chunks straight from registers; the warp
+    // writes one whole 1 KB atom (8 rows x 64 columns).
+    const int row = i0 + lr;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = d.transposed ? tile[ch * 8 + e][yi] : tile[yi][ch * 8 + e];
-    uint4 w;
-    w.x = pack_bf16x2(v[0], v[1]);
-    w.y = pack_bf16x2(v[2], v[3]);
-    w.z = pack_bf16x2(v[4], v[5]);
-    w.w = pack_bf16x2(v[6], v[7]);
-    const int row = i0 + yi;
-    uint8_t* dst = d.y + (size_t)(j0 >> 6) * stride + (size_t)(row >> 3) * 1024 + (size_t)(row & 7) * 128 +
-                   (size_t)((ch ^ (row & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst) = w;
+    for (int h = 0; h < 2; ++h) {
+      const int col = j0 + lc + 8 * h;
+      uint8_t* dst = d.y + blocked_chunk(d.s_pad, row, col);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+    }
+  } else {
+    // X0 row i = stored column i: the warp's 8 stored rows are columns
+    // [j0 + 8w, +8) of X0 rows i0 .. i0+63; transpose them in the warp's buffer.
+    uint4* srow = reinterpret_cast<uint4*>(&xpose[warp][lane >> 2][lc]);
+    srow[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    srow[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ii = lane + 32 * h;                  // X0 row within the tile
+      uint32_t w4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w4[k] = (uint32_t)xpose[warp][2 * k][ii] | ((uint32_t)xpose[warp][2 * k + 1][ii] << 16);
+      uint8_t* dst = d.y + blocked_chunk(d.s_pad, i0 + ii, j0 + 8 * warp);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
   }
 
-  // Fixed-order reduction of the tile's sum of squares.
+  // Fixed-order warp reduction; one partial per warp.
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((t & 31) == 0) warp_sum[t >> 5] = ss;
-  __syncthreads();
-  if (t == 0) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) s += warp_sum[w];
-    p.partials[d.partial0 + local] = s;
-  }
+  if (lane == 0) p.partials[(size_t)(d.partial0 + local) * 8 + warp] = ss;
 }
 
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constant__ NormBatch p) {

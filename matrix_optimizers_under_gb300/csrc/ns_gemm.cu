@@ -20,14 +20,25 @@
 // stored X serves as the K-major operand of the Gram product and the MN-major
 // operand of the update.
 //
-// One CTA computes one 128 x 256 (or 128 x 128) output tile: warp 0 / lane 0
-// streams K in 64-element stages through a 4-deep mbarrier ring, warp 1 /
-// lane 0 issues 128 x N x 16 UMMAs into a TMEM accumulator, then all four warps
-// read the accumulator (tcgen05.ld, one TMEM lane quadrant each), apply the
-// fused polynomial epilogue in fp32 and store bf16 (or the final update in the
-// caller's dtype and layout, transposed back for tall matrices).  Every wait is
-// bounded: on expiry the CTA records kStatusTimeout, drains what it issued,
-// frees TMEM and returns.
+// Persistent, warp-specialised CTAs (one per SM) walk the launch's tile list
+// round-robin.  Warp 0 (one lane) streams K in 64-element stages through a
+// 4-deep mbarrier ring of 48 KB stages; warp 1 (one lane) issues 128 x N x 16
+// UMMAs into one of two 256-column TMEM accumulators; warps 2-5 drain the other
+// accumulator (tcgen05.ld, one TMEM lane quadrant each), apply the fused
+// polynomial epilogue in fp32 and store bf16 -- or, on the last iteration, the
+// update in the caller's dtype and layout, transposed back for tall matrices.
+// So one tile's epilogue runs under the next tile's main loop.  Every wait is
+// bounded: on expiry the CTA records kStatusTimeout, stops, drains what it
+// issued, frees TMEM and returns.
+//
+// Bounds of every bulk copy (all matrices are padded to multiples of 128, K is
+// a multiple of 64): the A operand of stage kb starts at kb*s_pad*128 +
+// (m0/8)*1024 and spans 16 KB, ending at most at (K/64-1)*s_pad*128 +
+// (s_pad-128)*128 + 16384 = K*s_pad*2, the end of the operand; the K-major B
+// operand likewise ends at most at (K/64-1)*s_pad*128 + n0*128 + N*128 <=
+// K*s_pad*2 since n0 + N <= s_pad; the MN-major X runs (column block
+// n0/64 + j, K rows 64kb..64kb+63) end at most at (l_pad/64-1)*s_pad*128 +
+// (s_pad/64-1)*8192 + 8192 = l_pad*s_pad*2, the end of X.
 #include <cuda_bf16.h>
 
 #include "mfsdp_internal.h"
@@ -37,7 +48,8 @@ namespace mfsdp {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCols = 256;     // one fp32 accumulator of 128 lanes x 256 columns
+constexpr uint32_t kTmemCols = 512;    // two accumulators: epilogue of tile i overlaps the MMAs of tile i+1
 
 __device__ __forceinline__ int find_mat(const int32_t* start, int n, int t) {
   int lo = 0, hi = n - 1;
@@ -125,51 +137,74 @@ __device__ __forceinline__ void store_final(const GemmMat& d, int out_bf16, int 
   }
 }
 
+struct Tile {
+  int mi;        // matrix index in the batch
+  int m0, n0;    // output tile origin
+  int N;         // tile width (256, or 128 for the last column tile)
+  bool zero;     // the matrix's momentum is exactly zero: no products
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmBatch& p, int t) {
+  Tile r;
+  r.mi = find_mat(p.tile_start, p.n, t);
+  const GemmMat& d = p.mat[r.mi];
+  const int local = t - p.tile_start[r.mi];
+  const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // m fastest: neighbours share B-operand columns
+  r.m0 = mt * kBlockM;
+  r.n0 = nt * kBlockN;
+  r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
+  r.zero = p.norm[d.norm_idx].x == 0.0f;
+  return r;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int32_t* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmBatch p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
-  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2];    // accumulator ready for the epilogue
+  __shared__ __align__(8) uint64_t tempty_bar[2];   // accumulator drained, MMA may reuse it
+  __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mi = find_mat(p.tile_start, p.n, blockIdx.x);
-  const GemmMat& d = p.mat[mi];
-  const int local = blockIdx.x - p.tile_start[mi];
-  const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // m fastest: neighbours share B-operand columns
-  const int m0 = mt * kBlockM, n0 = nt * kBlockN;
-  const int N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
-  const int mode = p.mode;
-
-  // A matrix whose momentum is exactly zero has X = 0 throughout: skip the
-  // products, and write the zero update once at the end.
-  const float2 nrm = p.norm[d.norm_idx];
-  if (nrm.x == 0.0f) {
-    if (mode == kUpdateFinal) {
-      const int m = m0 + threadIdx.x;
-      float z[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) z[j] = 0.f;
-      for (int c = 0; c < N; c += 32) store_final(d, p.out_bf16, m, n0 + c, z);
-    }
-    return;
-  }
-
+  const int total = p.tile_start[p.n];
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  auto stage_a = [&](int s) { return smem_base + (uint32_t)s * kStageBytes; };
-  auto stage_b = [&](int s) { return smem_base + (uint32_t)s * kStageBytes + kStageBytesA; };
+  const int mode = p.mode;
+  const bool b_mn = (mode == kUpdate || mode == kUpdateFinal);
 
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (threadIdx.x == 32) {
+  if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&done_bar), 1);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&tfull_bar[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&tempty_bar[a]), kEpilogueWarps);
+    }
+    ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
     abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -177,138 +212,158 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem_d = tmem_slot;
-
-  const int kb_total = d.k_blocks;
-  const size_t a_kstride = colblock_stride(d.s_pad);   // every operand has s_pad rows per column block
-  const bool b_mn = (mode == kUpdate || mode == kUpdateFinal);
+  const uint32_t tmem_base = tmem_slot;
+  volatile int* abort_v = &abort_flag;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       const uint64_t pol = ptx::policy_evict_last();
-      const uint32_t a_bytes = kStageBytesA;
-      const uint32_t b_bytes = (uint32_t)N * kBlockK * 2;
-      int issued = 0;
-      for (int kb = 0; kb < kb_total; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[s]), ((kb / kStages) - 1) & 1, kWaitLimitNs)) {
-            atomicOr(p.status, kStatusTimeout);
-            atomicExch(&abort_flag, 1);
-            break;
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < total && !*abort_v; t += gridDim.x) {
+        const Tile tl = decode_tile(p, t);
+        if (tl.zero) continue;
+        const GemmMat& d = p.mat[tl.mi];
+        const size_t kstride = colblock_stride(d.s_pad);   // every operand has s_pad rows per column block
+        const uint32_t b_bytes = (uint32_t)tl.N * kBlockK * 2;
+        for (int kb = 0; kb < d.k_blocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t use = it / kStages;
+          if (!wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, abort_v, p.status)) break;
+          const uint32_t fb = ptx::smem_u32(&full_bar[s]);
+          const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
+          ptx::mbar_arrive_expect_tx(fb, kStageBytesA + b_bytes);
+          ptx::bulk_g2s(sa, d.a_op + (size_t)kb * kstride + (size_t)(tl.m0 >> 3) * 1024, kStageBytesA, fb, pol);
+          if (!b_mn) {
+            ptx::bulk_g2s(sb, d.b_op + (size_t)kb * kstride + (size_t)(tl.n0 >> 3) * 1024, b_bytes, fb, pol);
+          } else {
+            // X as the MN-major operand: K rows [64 kb, 64 kb + 64) of column
+            // blocks n0/64 ..; each block's 8 atoms are one 8 KB run.
+            for (int j = 0; j < tl.N / 64; ++j) {
+              const uint8_t* src = d.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
+              ptx::bulk_g2s(sb + (uint32_t)j * 8192u, src, 8192u, fb, pol);
+            }
           }
         }
-        if (*(volatile int*)&abort_flag) break;
-        const uint32_t fb = ptx::smem_u32(&full_bar[s]);
-        ptx::mbar_arrive_expect_tx(fb, a_bytes + b_bytes);
-        ptx::bulk_g2s(stage_a(s), d.a_op + (size_t)kb * a_kstride + (size_t)(m0 >> 3) * 1024, a_bytes, fb, pol);
-        if (!b_mn) {
-          ptx::bulk_g2s(stage_b(s), d.b_op + (size_t)kb * a_kstride + (size_t)(n0 >> 3) * 1024, b_bytes, fb, pol);
-        } else {
-          // X as the MN-major operand: K rows [64 kb, 64 kb + 64) of column
-          // blocks n0/64 ..; each block's 8 atoms are one 8 KB run.
-          for (int j = 0; j < N / 64; ++j) {
-            const uint8_t* src = d.b_op + (size_t)((n0 >> 6) + j) * a_kstride + (size_t)kb * 8 * 1024;
-            ptx::bulk_g2s(stage_b(s) + (uint32_t)j * 8192u, src, 8192u, fb, pol);
-          }
-        }
-        issued = kb + 1;
       }
-      // Drain: wait (bounded) until the copies of the last uses of each stage landed.
-      for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
-        ptx::mbar_wait(ptx::smem_u32(&full_bar[kb % kStages]), (kb / kStages) & 1, kWaitLimitNs);
-      }
+      // Drain: the copies of the last use of each stage have landed (bounded).
+      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+      for (uint32_t k = first; k < it; ++k)
+        ptx::mbar_wait(ptx::smem_u32(&full_bar[k % kStages]), (k / kStages) & 1, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------- MMA issuer
-      const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, (uint32_t)N, b_mn ? 1u : 0u);
-      for (int kb = 0; kb < kb_total; ++kb) {
-        const int s = kb % kStages;
-        if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (kb / kStages) & 1, kWaitLimitNs)) {
-          atomicOr(p.status, kStatusTimeout);
-          atomicExch(&abort_flag, 1);
-          break;
-        }
-        if (*(volatile int*)&abort_flag) break;
+      uint32_t it = 0, acc_it = 0;
+      for (int t = blockIdx.x; t < total && !*abort_v; t += gridDim.x) {
+        const Tile tl = decode_tile(p, t);
+        if (tl.zero) continue;
+        const GemmMat& d = p.mat[tl.mi];
+        const uint32_t a = acc_it & 1, ause = acc_it >> 1;
+        if (!wait_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, abort_v, p.status)) break;
         ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + a * kAccCols;
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, (uint32_t)tl.N, b_mn ? 1u : 0u);
+        bool ok = true;
+        for (int kb = 0; kb < d.k_blocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t use = it / kStages;
+          if (!wait_or_abort(ptx::smem_u32(&full_bar[s]), use & 1, abort_v, p.status)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
 #pragma unroll
-        for (int k = 0; k < kBlockK / 16; ++k) {
-          // K-major operand: advance 16 elements (32 bytes) inside the swizzle row.
-          const uint64_t adesc = ptx::smem_desc_sw128(stage_a(s) + (uint32_t)k * 32u, 16u, 1024u);
-          uint64_t bdesc;
-          if (!b_mn) {
-            bdesc = ptx::smem_desc_sw128(stage_b(s) + (uint32_t)k * 32u, 16u, 1024u);
-          } else {
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            // K-major operand: advance 16 elements (32 bytes) inside the swizzle row.
+            const uint64_t adesc = ptx::smem_desc_sw128(sa + (uint32_t)k * 32u, 16u, 1024u);
             // MN-major operand: 16 K rows = two 8-row atoms (2 KB); 64-column
             // blocks 8 KB apart (leading byte offset), 8-row K groups 1 KB
             // apart (stride byte offset).
-            bdesc = ptx::smem_desc_sw128(stage_b(s) + (uint32_t)k * 2048u, 8192u, 1024u);
+            const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 8192u, 1024u)
+                                        : ptx::smem_desc_sw128(sb + (uint32_t)k * 32u, 16u, 1024u);
+            ptx::umma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          ptx::umma_bf16(tmem_d, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          ptx::umma_commit(ptx::smem_u32(&empty_bar[s]));   // frees the stage once these MMAs finish
         }
-        ptx::umma_commit(ptx::smem_u32(&empty_bar[s]));   // frees the stage once these MMAs finish
+        if (!ok) break;
+        ptx::umma_commit(ptx::smem_u32(&tfull_bar[a]));     // accumulator complete
+        ++acc_it;
       }
-      ptx::umma_commit(ptx::smem_u32(&done_bar));        // accumulator complete (or drained on abort)
+      // Every MMA this thread issued has completed before TMEM is released.
+      ptx::umma_commit(ptx::smem_u32(&drain_bar));
+      ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, kWaitLimitNs);
     }
     __syncwarp();
-  }
-
-  // ------------------------------------------------------------------ epilogue
-  const bool done_ok = ptx::mbar_wait(ptx::smem_u32(&done_bar), 0, kWaitLimitNs);
-  if (!done_ok) {
-    if (lane == 0) atomicOr(p.status, kStatusTimeout);
-    atomicExch(&abort_flag, 1);
-  }
-  ptx::tc_fence_after();
-  __syncwarp();
-  const bool write = done_ok && !*(volatile int*)&abort_flag;
-  if (done_ok) {
-    const int m = m0 + warp * 32 + lane;                         // this thread's output row
-    const uint32_t t_row = tmem_d + ((uint32_t)(warp * 32) << 16);
-    const float scale_gram = p.first_iter ? nrm.y * nrm.y : 1.0f;
-    const float scale_upd = p.first_iter ? nrm.y : 1.0f;
-    const size_t stride = colblock_stride(d.s_pad);
-    const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
-    for (int c = 0; c < N; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
-      ptx::tmem_ld_wait();
-      if (!write) continue;
-      const int n = n0 + c;
-      size_t off[4];
-      const size_t base = (size_t)(n >> 6) * stride + row_off;
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+    uint32_t acc_it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode_tile(p, t);
+      const GemmMat& d = p.mat[tl.mi];
+      const int m = tl.m0 + quad * 32 + lane;          // this thread's output row
+      if (tl.zero) {
+        if (mode == kUpdateFinal) {
+          float z[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) off[q] = base + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
-      float v[32];
-      if (mode == kGram) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
-        store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
-      } else if (mode == kPoly) {
-        float x[32];
-        load_bf16x32(d.c_in, off, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
-        store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
-      } else {
-        float x[32];
-        load_bf16x32(d.c_in, off, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
-        if (mode == kUpdate) store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
-        else store_final(d, p.out_bf16, m, n, v);
+          for (int j = 0; j < 32; ++j) z[j] = 0.f;
+          for (int c = 0; c < tl.N; c += 32) store_final(d, p.out_bf16, m, tl.n0 + c, z);
+        }
+        continue;
       }
+      const uint32_t a = acc_it & 1, ause = acc_it >> 1;
+      if (!wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, abort_v, p.status)) break;
+      ptx::tc_fence_after();
+      const float2 nrm = p.norm[d.norm_idx];
+      const float scale_gram = p.first_iter ? nrm.y * nrm.y : 1.0f;
+      const float scale_upd = p.first_iter ? nrm.y : 1.0f;
+      const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
+      const size_t stride = colblock_stride(d.s_pad);
+      const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
+      for (int c = 0; c < tl.N; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
+        ptx::tmem_ld_wait();
+        if (c + 32 >= tl.N) {
+          // last chunk read: hand the accumulator back to the MMA warp
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[a]));
+        }
+        const int n = tl.n0 + c;
+        size_t off[4];
+        const size_t base = (size_t)(n >> 6) * stride + row_off;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) off[q] = base + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
+        float v[32];
+        if (mode == kGram) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
+          store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
+        } else if (mode == kPoly) {
+          float x[32];
+          load_bf16x32(d.c_in, off, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
+          store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
+        } else {
+          float x[32];
+          load_bf16x32(d.c_in, off, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
+          if (mode == kUpdate) store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
+          else store_final(d, p.out_bf16, m, n, v);
+        }
+      }
+      ++acc_it;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_d, kTmemCols);
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -316,10 +371,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
 cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s) {
   if (total_tiles <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kGemmSmemBytes);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  ns_gemm_kernel<<<total_tiles, kGemmThreads, kGemmSmemBytes, s>>>(b);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = total_tiles < sms ? total_tiles : sms;   // persistent: one CTA per SM
+  ns_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(b);
   return cudaGetLastError();
 }
 
