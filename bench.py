@@ -24,7 +24,6 @@ from __future__ import annotations
 import argparse
 import json
 import math
-import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -66,32 +65,6 @@ def heaviest_rank(plan) -> int:
     for s in plan.tail_shards:
         tail[s.owner] += s.numel
     return min(range(world), key=lambda r: (-cost[r], tail[r], r))
-
-
-def _gen_matrix(args):
-    name, pid = args
-    return pid, W.grad_storage(W.get(name), pid)
-
-
-def generate_grads(w, shards, numel):
-    """Flat gradient buffer of one rank (bf16 bits or fp32), generated per matrix
-    in a spawn-started process pool (started before any CUDA call)."""
-    dtype = np.uint16 if w.grad_dtype == "bf16" else np.float32
-    buf = np.zeros(numel, dtype)
-    jobs = [(w.name, s.param_id) for s in shards]
-    by_id = {s.param_id: s for s in shards}
-    nproc = max(1, min(len(jobs), (os.cpu_count() or 2), 16))
-    if nproc > 1 and sum(s.rows * s.cols for s in shards) > 8_000_000:
-        with mp.get_context("spawn").Pool(nproc) as pool:
-            for pid, g in pool.imap_unordered(_gen_matrix, jobs):
-                s = by_id[pid]
-                buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
-    else:
-        for j in jobs:
-            pid, g = _gen_matrix(j)
-            s = by_id[pid]
-            buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
-    return buf
 
 
 class ClockSampler:
@@ -255,7 +228,7 @@ def run_ours(args):
     tail_numel = plan.rank_tail_elems[sim_rank]
 
     t_gen = time.time()
-    grad_np = generate_grads(w, shards, numel)       # before any CUDA call (spawn pool)
+    grad_np = W.owner_grad_buffer(w, shards, numel)   # before any CUDA call (spawn pool)
     t_gen = time.time() - t_gen
 
     import torch
@@ -387,11 +360,12 @@ def run_ours(args):
 
     # ---------------------------------------------------------- figures
     peaks, peak_src = load_peaks()
-    flops = sum(ns_flops(s.rows, s.cols, w.ns_steps) for s in shards)
+    flops, flops_exec = mfsdp.muon_step_flops(shards, w.ns_steps)
     elems = sum(s.rows * s.cols for s in shards)
     gsz = 2 if bf16 else 4
     mom_bytes = elems * (gsz + 4 + 4 + 2)
-    ns_tflops = flops / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
+    ns_tflops = flops / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0           # dense-equivalent
+    ns_tflops_exec = flops_exec / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0  # executed MMA work
     mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
     adam_gbs = 28 * tail_numel / (adam_ms * 1e-3) / 1e9 if adam_ms > 0 and tail_numel else 0.0
     peak_tf = peaks["bf16_tflops_sustained"]
@@ -422,13 +396,18 @@ def run_ours(args):
                    "parallelism": f"owner sets x{world}"},
         "phases": {"momentum_ms": round(mom_ms, 4), "momentum_gbs": round(mom_gbs, 1),
                    "momentum_frac_hbm": round(mom_gbs / hbm, 4),
-                   "newton_schulz_ms": round(ns_ms, 4), "newton_schulz_tflops": round(ns_tflops, 1),
-                   "newton_schulz_frac_bf16": round(ns_tflops / peak_tf, 4),
+                   "newton_schulz_ms": round(ns_ms, 4),
+                   "newton_schulz_tflops_executed": round(ns_tflops_exec, 1),
+                   "newton_schulz_frac_bf16_executed": round(ns_tflops_exec / peak_tf, 4),
+                   "newton_schulz_tflops_dense_equivalent": round(ns_tflops, 1),
+                   "newton_schulz_frac_bf16_dense_equivalent": round(ns_tflops / peak_tf, 4),
+                   "flops_dense": flops, "flops_executed": flops_exec,
                    "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1)},
-        "roofline": {"kernel": "ns_gemm_kernel", "bound": "tensor", "achieved": round(ns_tflops, 1),
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops / peak_tf, 4), "traffic": None,
+        "roofline": {"kernel": "ns_gemm_kernel", "bound": "tensor", "achieved": round(ns_tflops_exec, 1),
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4), "traffic": None,
                      "peak_source": f"{peak_src} bf16_tflops_sustained",
-                     "flops_per_launch": round(flops / max(ns_launches, 1)), "launches_per_step": ns_launches},
+                     "flops": "executed tensor-core FLOPs (symmetric Gram/polynomial: upper-triangle blocks only)",
+                     "flops_per_launch": round(flops_exec / max(ns_launches, 1)), "launches_per_step": ns_launches},
         "clocks": clocks,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},

@@ -216,6 +216,16 @@ int mfsdp_muon_owner_step_static_scratch(const mfsdp_matrix_shard* shards, int32
                                          double a, double b, double c, double eps,
                                          void* stream);
 
+/* FLOP counts of mfsdp_muon_owner_step for these shards, host only:
+ * *dense = sum over matrices of ns_steps * (4 s^2 l + 2 s^3) (the algorithmic
+ * count); *executed = the tensor-core FLOPs the kernels issue (dimensions
+ * padded to multiples of 128; the symmetric Gram and polynomial products
+ * computed on their upper-triangle 128 x 128 blocks only; matrices whose
+ * momentum turns out to be zero, which skip all products, still counted).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
+int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t ns_steps,
+                          uint64_t* dense, uint64_t* executed);
+
 /* Reads the device status word a previous mfsdp_muon_owner_step left in
  * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
  * if one of its kernels gave up on a bounded wait (its outputs are then

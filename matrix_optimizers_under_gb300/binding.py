@@ -38,7 +38,8 @@ PHASE_NEWTON_SCHULZ = 2
 
 EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
-            "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch")
+            "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
+            "mfsdp_muon_step_flops")
 
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -84,6 +85,9 @@ _lib.mfsdp_muon_owner_step_phases.argtypes = _STEP_ARGS + [_i32]
 _lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_static_scratch.argtypes = _STEP_ARGS[:15] + [_vp]
 _lib.mfsdp_muon_owner_step_static_scratch.restype = ctypes.c_int
+_lib.mfsdp_muon_step_flops.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, ctypes.POINTER(_u64),
+                                       ctypes.POINTER(_u64)]
+_lib.mfsdp_muon_step_flops.restype = ctypes.c_int
 _lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.mfsdp_muon_device_status.restype = ctypes.c_int
 _lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _d, _d, _d, _d, _d, _i64, _vp]
@@ -170,6 +174,14 @@ def muon_workspace_layout(shards: Sequence[MatrixShard]) -> List[Tuple[int, ...]
     out = (_i64 * max(8 * len(shards), 1))()
     _check(_lib.mfsdp_muon_workspace_layout(_shard_array(shards), len(shards), out), "muon_workspace_layout")
     return [tuple(out[8 * i: 8 * i + 8]) for i in range(len(shards))]
+
+
+def muon_step_flops(shards: Sequence[MatrixShard], ns_steps: int = 5) -> Tuple[int, int]:
+    """(dense, executed) FLOPs of one owner step (see include/mfsdp.h)."""
+    dn, ex = _u64(0), _u64(0)
+    _check(_lib.mfsdp_muon_step_flops(_shard_array(shards), len(shards), int(ns_steps), ctypes.byref(dn),
+                                      ctypes.byref(ex)), "muon_step_flops")
+    return int(dn.value), int(ex.value)
 
 
 def _ptr(t) -> Optional[int]:

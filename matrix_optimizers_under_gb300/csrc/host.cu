@@ -97,6 +97,42 @@ size_t dtype_size(int32_t dt) { return dt == MFSDP_DTYPE_BF16 ? 2 : 4; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_CUDA; }
 
+// Output tiling of one product of one matrix.  The Gram and polynomial outputs
+// are symmetric: only the 128 x 128 blocks on or above the diagonal are
+// computed, paired along the row into 128 x 256 tiles (the last one of a row
+// 128 wide when the count is odd), and mirrored by the epilogue.
+struct GemmTiling {
+  int tiles, tiles_m, tiles_n, n_last, symmetric;
+};
+
+GemmTiling gemm_tiling(int mode, int s_pad, int l_pad) {
+  GemmTiling t;
+  t.tiles_m = s_pad / kBlockM;
+  if (mode == kGram || mode == kPoly) {
+    const int nb = s_pad / kBlockM;
+    t.symmetric = 1;
+    t.tiles_n = (nb + 1) / 2;      // widest row (row block 0)
+    t.n_last = 0;                  // widths follow from the block count
+    t.tiles = 0;
+    for (int i = 0; i < nb; ++i) t.tiles += (nb - i + 1) / 2;
+  } else {
+    t.symmetric = 0;
+    t.tiles_n = (l_pad + kBlockN - 1) / kBlockN;
+    t.n_last = l_pad - (t.tiles_n - 1) * kBlockN;
+    t.tiles = t.tiles_m * t.tiles_n;
+  }
+  return t;
+}
+
+// Tensor-core FLOPs one product of one matrix executes (padded, symmetric blocks only).
+uint64_t executed_flops(int mode, int s_pad, int l_pad) {
+  const uint64_t nb = (uint64_t)s_pad / kBlockM;
+  const uint64_t blk = (uint64_t)kBlockM * kBlockM * 2;
+  if (mode == kGram) return nb * (nb + 1) / 2 * blk * (uint64_t)l_pad;
+  if (mode == kPoly) return nb * (nb + 1) / 2 * blk * (uint64_t)s_pad;
+  return 2ull * s_pad * s_pad * (uint64_t)l_pad;
+}
+
 int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
                           int32_t grad_dtype, float* momentum, float beta, int32_t nesterov, float eps, uint8_t* ws,
                           cudaStream_t stream);
@@ -337,9 +373,15 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
         gb.c = c;
         gb.norm = norm;
         gb.status = status;
+        // Longest K first: the persistent CTAs take tiles round-robin, so the
+        // last rounds hold the cheapest tiles.
+        std::vector<int> order(cnt);
+        for (int k = 0; k < cnt; ++k) order[k] = base + k;
+        auto kb_of = [&](int i) { return mode == kGram ? L.mats[i].l_pad : L.mats[i].s_pad; };
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return kb_of(x) > kb_of(y); });
         int tiles = 0;
         for (int k = 0; k < cnt; ++k) {
-          const int i = base + k;
+          const int i = order[k];
           const MatLayout& m = L.mats[i];
           uint8_t* xc = ws + ((it & 1) ? m.x1 : m.x0);   // current iterate
           uint8_t* xn = ws + ((it & 1) ? m.x0 : m.x1);   // next iterate
@@ -351,10 +393,11 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
           d.norm_idx = i;
           d.transposed = m.transposed;
           d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
-          d.tiles_m = m.s_pad / kBlockM;
-          const int ncols = (mode == kUpdate) ? m.l_pad : m.s_pad;
-          d.tiles_n = (ncols + kBlockN - 1) / kBlockN;
-          d.n_last = ncols - (d.tiles_n - 1) * kBlockN;
+          const GemmTiling tg = gemm_tiling(mode, m.s_pad, m.l_pad);
+          d.tiles_m = tg.tiles_m;
+          d.tiles_n = tg.tiles_n;
+          d.n_last = tg.n_last;
+          d.symmetric = tg.symmetric;
           if (mode == kGram) {
             d.a_op = xc; d.b_op = xc; d.c_in = nullptr; d.out = ws + m.a;
             d.k_blocks = m.l_pad / kBlockK;
@@ -368,7 +411,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
             d.k_blocks = m.s_pad / kBlockK;
           }
           gb.tile_start[k] = tiles;
-          tiles += d.tiles_m * d.tiles_n;
+          tiles += tg.tiles;
         }
         gb.tile_start[cnt] = tiles;
         st = cuda_status(launch_ns_gemm(gb, tiles, stream));
@@ -381,6 +424,25 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
 
 }  // namespace
 }  // namespace mfsdp
+
+extern "C" int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t ns_steps,
+                                     uint64_t* dense, uint64_t* executed) {
+  if (ns_steps < 0 || ns_steps > 64 || !dense || !executed) return MFSDP_ERR_INVALID_ARG;
+  Layout L;
+  const int st = make_layout(shards, n_shards, &L);
+  if (st != MFSDP_OK) return st;
+  uint64_t dn = 0, ex = 0;
+  for (int i = 0; i < n_shards; ++i) {
+    const MatLayout& m = L.mats[i];
+    const uint64_t s = (uint64_t)m.s, l = (uint64_t)m.l;
+    dn += (uint64_t)ns_steps * (4 * s * s * l + 2 * s * s * s);
+    ex += (uint64_t)ns_steps * (executed_flops(kGram, m.s_pad, m.l_pad) + executed_flops(kPoly, m.s_pad, m.l_pad) +
+                                executed_flops(kUpdate, m.s_pad, m.l_pad));
+  }
+  *dense = dn;
+  *executed = ex;
+  return MFSDP_OK;
+}
 
 extern "C" int mfsdp_muon_device_status(const void* workspace, void* stream_ptr, int32_t* detail) {
   if (!workspace) return MFSDP_ERR_INVALID_ARG;

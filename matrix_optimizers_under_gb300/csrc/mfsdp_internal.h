@@ -22,7 +22,7 @@ constexpr int kStages = 4;         // smem pipeline depth
 constexpr int kStageBytesA = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBytesB = kBlockN * kBlockK * 2;   // 32 KB
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
-constexpr int kEpilogueWarps = 4;  // warps 2-5 of the GEMM CTA
+constexpr int kEpilogueWarps = 8;  // warps 2-9 of the GEMM CTA: two per TMEM lane quadrant
 constexpr int kGemmThreads = 64 + 32 * kEpilogueWarps;   // producer warp, MMA warp, epilogue warps
 constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 
@@ -88,11 +88,11 @@ struct GemmMat {
   int32_t s, l;          // true short / long side
   int32_t tiles_m, tiles_n;
   int32_t k_blocks;      // K / kBlockK
-  int32_t n_last;        // width of the last column tile (128 or 256)
+  int32_t n_last;        // width of the last column tile (128 or 256); unused when symmetric
   int32_t norm_idx;      // index into the norm table
   int32_t transposed;    // kUpdateFinal: stored matrix is l x s
   int32_t vec_ok;        // kUpdateFinal: row-major stores may use 16-byte vectors
-  int32_t pad;
+  int32_t symmetric;     // kGram / kPoly: upper-triangle tiles only, mirrored on store
 };
 struct GemmBatch {
   int32_t n;

@@ -9,7 +9,12 @@
 //     B = b A + c A A        (kPoly,   K = s; A is symmetric so A A = A A^T)
 //     X <- a X + B X         (kUpdate, K = s)
 // with the Frobenius prescale 1/(||U||+eps) folded into the first iteration's
-// epilogues (A scaled by its square, the new X by it).
+// epilogues (A scaled by its square, the new X by it).  A and B are symmetric:
+// their products compute only the 128 x 128 blocks on or above the diagonal
+// (paired into 128 x 256 tiles) and the epilogue writes every off-diagonal
+// block twice, directly and transposed, so the stored A and B are exactly
+// symmetric and the Gram and polynomial products execute ~53 % of the dense
+// FLOPs.
 //
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
@@ -23,8 +28,9 @@
 // Persistent, warp-specialised CTAs (one per SM) walk the launch's tile list
 // round-robin.  Warp 0 (one lane) streams K in 64-element stages through a
 // 4-deep mbarrier ring of 48 KB stages; warp 1 (one lane) issues 128 x N x 16
-// UMMAs into one of two 256-column TMEM accumulators; warps 2-5 drain the other
-// accumulator (tcgen05.ld, one TMEM lane quadrant each), apply the fused
+// UMMAs into one of two 256-column TMEM accumulators; warps 2-9 drain the other
+// accumulator (tcgen05.ld; two warps per TMEM lane quadrant, each taking half
+// the columns, the epilogue input prefetched ahead of the data), apply the fused
 // polynomial epilogue in fp32 and store bf16 -- or, on the last iteration, the
 // update in the caller's dtype and layout, transposed back for tall matrices.
 // So one tile's epilogue runs under the next tile's main loop.  Every wait is
@@ -67,19 +73,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Byte offset of the q-th 16-byte chunk of columns [n, n + 32) of row m in a
+// blocked matrix (n a multiple of 32).
+__device__ __forceinline__ size_t chunk_off(size_t stride, size_t row_off, int m, int n, int q) {
+  return (size_t)(n >> 6) * stride + row_off + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
+}
+
+__device__ __forceinline__ void load_chunk(const uint8_t* base, size_t stride, size_t row_off, int m, int n,
+                                           uint4 (&w)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = *reinterpret_cast<const uint4*>(base + chunk_off(stride, row_off, m, n, q));
+}
+
 // Unpack 32 bf16 (four 16-byte chunks) into fp32.
-__device__ __forceinline__ void load_bf16x32(const uint8_t* base, const size_t (&off)[4], float (&x)[32]) {
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&x)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 w = *reinterpret_cast<const uint4*>(base + off[q]);
-    x[8 * q + 0] = bf_lo(w.x); x[8 * q + 1] = bf_hi(w.x);
-    x[8 * q + 2] = bf_lo(w.y); x[8 * q + 3] = bf_hi(w.y);
-    x[8 * q + 4] = bf_lo(w.z); x[8 * q + 5] = bf_hi(w.z);
-    x[8 * q + 6] = bf_lo(w.w); x[8 * q + 7] = bf_hi(w.w);
+    x[8 * q + 0] = bf_lo(w[q].x); x[8 * q + 1] = bf_hi(w[q].x);
+    x[8 * q + 2] = bf_lo(w[q].y); x[8 * q + 3] = bf_hi(w[q].y);
+    x[8 * q + 4] = bf_lo(w[q].z); x[8 * q + 5] = bf_hi(w[q].z);
+    x[8 * q + 6] = bf_lo(w[q].w); x[8 * q + 7] = bf_hi(w[q].w);
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(uint8_t* base, const size_t (&off)[4], const float (&v)[32]) {
+__device__ __forceinline__ void store_chunk(uint8_t* base, size_t stride, size_t row_off, int m, int n,
+                                            const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 w;
@@ -87,7 +105,7 @@ __device__ __forceinline__ void store_bf16x32(uint8_t* base, const size_t (&off)
     w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
     w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
     w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(base + off[q]) = w;
+    *reinterpret_cast<uint4*>(base + chunk_off(stride, row_off, m, n, q)) = w;
   }
 }
 
@@ -149,12 +167,36 @@ __device__ __forceinline__ Tile decode_tile(const GemmBatch& p, int t) {
   r.mi = find_mat(p.tile_start, p.n, t);
   const GemmMat& d = p.mat[r.mi];
   const int local = t - p.tile_start[r.mi];
-  const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // m fastest: neighbours share B-operand columns
-  r.m0 = mt * kBlockM;
-  r.n0 = nt * kBlockN;
-  r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
+  if (d.symmetric) {
+    // Row block I holds blocks I .. nb-1 in pairs: ceil((nb - I) / 2) tiles.
+    const int nb = d.s_pad / kBlockM;
+    int rem = local, I = 0;
+    while (I < nb - 1 && rem >= ((nb - I + 1) >> 1)) {
+      rem -= (nb - I + 1) >> 1;
+      ++I;
+    }
+    r.m0 = I * kBlockM;
+    r.n0 = (I + 2 * rem) * kBlockM;
+    r.N = min(kBlockN, d.s_pad - r.n0);
+  } else {
+    const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // m fastest: neighbours share B-operand columns
+    r.m0 = mt * kBlockM;
+    r.n0 = nt * kBlockN;
+    r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
+  }
   r.zero = p.norm[d.norm_idx].x == 0.0f;
   return r;
+}
+
+// Operand sources of stage kb of a tile (bounds: see the file header).
+__device__ __forceinline__ const uint8_t* a_block(const GemmMat& d, const Tile& tl, int kb, size_t kstride) {
+  return d.a_op + (size_t)kb * kstride + (size_t)(tl.m0 >> 3) * 1024;
+}
+__device__ __forceinline__ const uint8_t* b_block_kmajor(const GemmMat& d, const Tile& tl, int kb, size_t kstride) {
+  return d.b_op + (size_t)kb * kstride + (size_t)(tl.n0 >> 3) * 1024;
+}
+__device__ __forceinline__ const uint8_t* b_block_mn(const GemmMat& d, const Tile& tl, int kb, size_t kstride, int j) {
+  return d.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -233,16 +275,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           const uint32_t fb = ptx::smem_u32(&full_bar[s]);
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
           ptx::mbar_arrive_expect_tx(fb, kStageBytesA + b_bytes);
-          ptx::bulk_g2s(sa, d.a_op + (size_t)kb * kstride + (size_t)(tl.m0 >> 3) * 1024, kStageBytesA, fb, pol);
+          ptx::bulk_g2s(sa, a_block(d, tl, kb, kstride), kStageBytesA, fb, pol);
           if (!b_mn) {
-            ptx::bulk_g2s(sb, d.b_op + (size_t)kb * kstride + (size_t)(tl.n0 >> 3) * 1024, b_bytes, fb, pol);
+            ptx::bulk_g2s(sb, b_block_kmajor(d, tl, kb, kstride), b_bytes, fb, pol);
           } else {
             // X as the MN-major operand: K rows [64 kb, 64 kb + 64) of column
             // blocks n0/64 ..; each block's 8 atoms are one 8 KB run.
-            for (int j = 0; j < tl.N / 64; ++j) {
-              const uint8_t* src = d.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
-              ptx::bulk_g2s(sb + (uint32_t)j * 8192u, src, 8192u, fb, pol);
-            }
+            for (int j = 0; j < tl.N / 64; ++j)
+              ptx::bulk_g2s(sb + (uint32_t)j * 8192u, b_block_mn(d, tl, kb, kstride, j), 8192u, fb, pol);
           }
         }
       }
@@ -296,21 +336,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue
-    const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+    // Eight warps: warp w reads TMEM lane quadrant w % 4 (the hardware rule)
+    // and one half of the tile's columns.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile(p, t);
       const GemmMat& d = p.mat[tl.mi];
       const int m = tl.m0 + quad * 32 + lane;          // this thread's output row
+      const int cw = tl.N >> 1;                         // columns per warp
+      const int c0 = half * cw;
       if (tl.zero) {
         if (mode == kUpdateFinal) {
           float z[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = 0.f;
-          for (int c = 0; c < tl.N; c += 32) store_final(d, p.out_bf16, m, tl.n0 + c, z);
+          for (int c = c0; c < c0 + cw; c += 32) store_final(d, p.out_bf16, m, tl.n0 + c, z);
         }
         continue;
       }
+      const size_t stride = colblock_stride(d.s_pad);
+      const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
+      const bool has_c = (mode != kGram);
+      // The epilogue input (A or X) does not depend on the accumulator: fetch
+      // the first chunk before waiting for the MMAs, the next one while the
+      // current one is processed.
+      uint4 xin[4];
+      if (has_c) load_chunk(d.c_in, stride, row_off, m, tl.n0 + c0, xin);
       const uint32_t a = acc_it & 1, ause = acc_it >> 1;
       if (!wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, abort_v, p.status)) break;
       ptx::tc_fence_after();
@@ -318,41 +371,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const float scale_gram = p.first_iter ? nrm.y * nrm.y : 1.0f;
       const float scale_upd = p.first_iter ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
-      const size_t stride = colblock_stride(d.s_pad);
-      const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
-      for (int c = 0; c < tl.N; c += 32) {
+      for (int c = c0; c < c0 + cw; c += 32) {
+        const bool more = c + 32 < c0 + cw;
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
+        uint4 xnext[4];
+        if (has_c && more) load_chunk(d.c_in, stride, row_off, m, tl.n0 + c + 32, xnext);
         ptx::tmem_ld_wait();
-        if (c + 32 >= tl.N) {
+        if (!more) {
           // last chunk read: hand the accumulator back to the MMA warp
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[a]));
         }
         const int n = tl.n0 + c;
-        size_t off[4];
-        const size_t base = (size_t)(n >> 6) * stride + row_off;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) off[q] = base + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
         float v[32];
         if (mode == kGram) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
-          store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
-        } else if (mode == kPoly) {
-          float x[32];
-          load_bf16x32(d.c_in, off, x);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
-          store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
         } else {
           float x[32];
-          load_bf16x32(d.c_in, off, x);
+          unpack_bf16x32(xin, x);
+          if (mode == kPoly) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
-          if (mode == kUpdate) store_bf16x32(static_cast<uint8_t*>(d.out), off, v);
-          else store_final(d, p.out_bf16, m, n, v);
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
+          }
+        }
+        if (mode == kUpdateFinal) {
+          store_final(d, p.out_bf16, m, n, v);
+        } else {
+          uint8_t* out = static_cast<uint8_t*>(d.out);
+          store_chunk(out, stride, row_off, m, n, v);
+          if (d.symmetric && (n >> 7) > (tl.m0 >> 7)) {
+            // off-diagonal block: also write its transpose, element (n + j, m)
+            const size_t mcol = (size_t)(m & 7) * 2;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+              *reinterpret_cast<__nv_bfloat16*>(out + blocked_chunk(d.s_pad, n + j, m & ~7) + mcol) = h;
+            }
+          }
+        }
+        if (more) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) xin[q] = xnext[q];
         }
       }
       ++acc_it;

@@ -21,6 +21,8 @@ round-to-nearest-even; the same bytes feed the GPU and the oracle.
 from __future__ import annotations
 
 import dataclasses
+import multiprocessing as mp
+import os
 from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
@@ -240,3 +242,32 @@ def ragged_params(seed: int, n: int, max_dim: int = 640) -> List[Tuple[int, int,
         else:
             out.append((int(rng.integers(1, 5000)), 1, KIND_TAIL))
     return out
+
+
+def _gen_one(args):
+    name, pid = args
+    return pid, grad_storage(get(name), pid)
+
+
+def owner_grad_buffer(w: Workload, shards, numel: int, workers: Optional[int] = None) -> np.ndarray:
+    """Flat gradient buffer of one rank as stored (bf16 bits or fp32), each shard
+    (objects with param_id, offset, rows, cols) filled with its seeded gradient;
+    padding is zero.  Large owner sets are generated per matrix in a
+    spawn-started process pool -- call this before any CUDA work in the process."""
+    dtype = np.uint16 if w.grad_dtype == "bf16" else np.float32
+    buf = np.zeros(numel, dtype)
+    jobs = [(w.name, s.param_id) for s in shards]
+    by_id = {s.param_id: s for s in shards}
+    n = workers if workers is not None else max(1, min(len(jobs), os.cpu_count() or 2, 16))
+    if n > 1 and sum(s.rows * s.cols for s in shards) > 8_000_000:
+        with mp.get_context("spawn").Pool(n) as pool:
+            results = pool.imap_unordered(_gen_one, jobs)
+            for pid, g in results:
+                s = by_id[pid]
+                buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
+    else:
+        for j in jobs:
+            pid, g = _gen_one(j)
+            s = by_id[pid]
+            buf[s.offset:s.offset + s.rows * s.cols] = g.reshape(-1)
+    return buf

@@ -167,3 +167,20 @@ def test_adamw_error_paths(mfsdp):
     assert call(g=None) == mfsdp.ERR_INVALID_ARG
     assert call(v=V + 8) == mfsdp.ERR_MISALIGNED
     assert call(m=P + 1024) == mfsdp.ERR_OVERLAP
+
+
+def test_step_flops(mfsdp):
+    shards = [mfsdp.make_shard(0, 4096, 14336), mfsdp.make_shard(0, 1024, 4096), mfsdp.make_shard(0, 300, 130)]
+    dense, executed = mfsdp.muon_step_flops(shards, 5)
+    want_dense = sum(5 * (4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3) for r, c in
+                     [(4096, 14336), (1024, 4096), (300, 130)])
+    assert dense == want_dense
+
+    def ex(s, l):   # padded dims; upper-triangle 128x128 blocks for the symmetric products
+        sp, lp = -(-s // 128) * 128, -(-l // 128) * 128
+        nb = sp // 128
+        blocks = nb * (nb + 1) // 2
+        return 5 * (blocks * 128 * 128 * 2 * lp + blocks * 128 * 128 * 2 * sp + 2 * sp * sp * lp)
+    assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300)
+    assert executed < dense     # the symmetric skipping outweighs the padding here
+    assert mfsdp.muon_step_flops([], 5) == (0, 0)

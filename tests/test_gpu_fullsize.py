@@ -1,0 +1,104 @@
+"""Full-size parity: the large owner sets run on the GPU exactly as bench.py runs
+them (one call of the owner step over the whole owner set, bf16 update), and a
+sample of their matrices -- one of every shape and orientation, plus all-zero
+experts -- is checked against the fp64 oracle; the sampled matrices are also
+re-run standalone and must match bit for bit (MatrixFSDP -- Abstract: the
+update matches full-matrix Muon).  The AdamW tail is checked element by element
+at its full size.
+
+These need minutes of oracle time on the host cores; they are marked slow as
+well as gpu.
+"""
+import numpy as np
+import pytest
+
+from oracle import adamw_ref, bf16_bits_to_f64, muon_matrix_ref
+from matrix_optimizers_under_gb300 import workloads as W
+from tests import helpers as H
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+A, B, C = W.NS_COEFFS
+
+
+def _sample(shards, w):
+    """One matrix per (rows, cols), the first in the owner set, plus up to two zero matrices."""
+    seen, out = set(), []
+    for s in shards:
+        if s.param_id in w.zero_params:
+            continue
+        if (s.rows, s.cols) not in seen:
+            seen.add((s.rows, s.cols))
+            out.append(s)
+    out += [s for s in shards if s.param_id in w.zero_params][:2]
+    return out
+
+
+@pytest.mark.parametrize("name", ["llama_1p3b_rank", "llama3_8b_rank", "moe_skewed"])
+def test_full_owner_set(mfsdp, name):
+    w = W.get(name)
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan)
+    shards = plan.rank_matrices(r)
+    numel = plan.rank_matrix_elems[r]
+    grad_np = W.owner_grad_buffer(w, shards, numel)
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    grad = torch.from_numpy(grad_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    kw = dict(beta=w.beta, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
+    mfsdp.muon_owner_step(shards, grad, mom, upd, ws, **kw)
+    st, detail = mfsdp.muon_device_status(ws)
+    assert st == mfsdp.OK, (st, detail)
+    torch.cuda.synchronize()
+    del ws
+
+    errs = {}
+    for s in _sample(shards, w):
+        n = s.rows * s.cols
+        seg = slice(s.offset, s.offset + n)
+        O = upd[seg].float().cpu().numpy().astype(np.float64).reshape(s.rows, s.cols)
+        M = mom[seg].cpu().numpy().reshape(s.rows, s.cols)
+        G = bf16_bits_to_f64(grad_np[seg]).reshape(s.rows, s.cols)
+        M_ref, O_ref = muon_matrix_ref(G, np.zeros_like(G), w.beta, False, w.ns_steps, A, B, C, w.ns_eps)
+        assert np.array_equal(M, M_ref.astype(np.float32)), "step-1 momentum must equal G exactly"
+        if s.param_id in w.zero_params:
+            assert np.all(O == 0.0)
+            continue
+        errs[(s.rows, s.cols)] = H.rel_fro(O, O_ref)
+        assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
+        # standalone run of the same matrix: bitwise the same update
+        alone = [mfsdp.make_shard(0, s.rows, s.cols, param_id=s.param_id)]
+        g1 = grad[seg].clone()
+        m1 = torch.zeros(n, dtype=torch.float32, device=dev)
+        u1 = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        ws1 = torch.empty(mfsdp.muon_workspace_bytes(alone), dtype=torch.uint8, device=dev)
+        mfsdp.muon_owner_step(alone, g1, m1, u1, ws1, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(u1.view(torch.int16), upd[seg].view(torch.int16)), s.param_id
+        del g1, m1, u1, ws1
+    print(name, {k: round(v, 5) for k, v in errs.items()})
+
+
+def test_full_size_adamw_tail(mfsdp):
+    """The 50M-element packed tail of the MoE owner set, element by element."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = W.get("moe_skewed")
+    tid = [i for i, p in enumerate(w.params) if p.kind == W.KIND_TAIL][0]
+    p0 = W.tail_param_f32(w, tid)
+    g = W.grad_f32(w, tid)
+    dev = torch.device("cuda:0")
+    tp, tg = torch.from_numpy(p0.copy()).to(dev), torch.from_numpy(g).to(dev)
+    tm, tv = torch.zeros_like(tp), torch.zeros_like(tp)
+    mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
+                          wd=w.weight_decay, step=1)
+    rp, rm, rv = adamw_ref(p0, g, np.zeros_like(p0), np.zeros_like(p0), w.lr, w.betas[0], w.betas[1], w.adam_eps,
+                           w.weight_decay, 1)
+    assert H.adam_err(tp.cpu().numpy(), rp) <= H.ADAM_REL
+    assert H.adam_err(tm.cpu().numpy(), rm) <= H.ADAM_REL
+    assert H.adam_err(tv.cpu().numpy(), rv) <= H.ADAM_REL
