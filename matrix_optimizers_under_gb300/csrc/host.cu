@@ -60,7 +60,7 @@ int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
     MatLayout& m = L->mats[i];
     m.s = (int)std::min(shards[i].rows, shards[i].cols);
     m.l = (int)std::max(shards[i].rows, shards[i].cols);
-    m.s_pad = (int)round_up((size_t)m.s, kPad);
+    m.s_pad = (int)round_up((size_t)m.s, kPadS);
     m.l_pad = (int)round_up((size_t)m.l, kPad);
     m.transposed = shards[i].rows > shards[i].cols ? 1 : 0;
     m.tiles_k1 = (m.s_pad / kTile) * (m.l_pad / kTile);
@@ -97,24 +97,23 @@ size_t dtype_size(int32_t dt) { return dt == MFSDP_DTYPE_BF16 ? 2 : 4; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_CUDA; }
 
-// Output tiling of one product of one matrix.  The Gram and polynomial outputs
-// are symmetric: only the 128 x 128 blocks on or above the diagonal are
-// computed, paired along the row into 128 x 256 tiles (the last one of a row
-// 128 wide when the count is odd), and mirrored by the epilogue.
+// Output tiling of one product of one matrix, in tiles of the 256 rows a CTA
+// pair computes together.  The Gram and polynomial outputs are symmetric: only
+// the 256 x 256 tiles on or above the diagonal are computed, and mirrored by
+// the epilogue.
 struct GemmTiling {
   int tiles, tiles_m, tiles_n, n_last, symmetric;
 };
 
 GemmTiling gemm_tiling(int mode, int s_pad, int l_pad) {
   GemmTiling t;
-  t.tiles_m = s_pad / kBlockM;
+  t.tiles_m = s_pad / kPairM;
   if (mode == kGram || mode == kPoly) {
-    const int nb = s_pad / kBlockM;
+    const int nb2 = s_pad / kPairM;
     t.symmetric = 1;
-    t.tiles_n = (nb + 1) / 2;      // widest row (row block 0)
-    t.n_last = 0;                  // widths follow from the block count
-    t.tiles = 0;
-    for (int i = 0; i < nb; ++i) t.tiles += (nb - i + 1) / 2;
+    t.tiles_n = nb2;
+    t.n_last = kBlockN;
+    t.tiles = nb2 * (nb2 + 1) / 2;
   } else {
     t.symmetric = 0;
     t.tiles_n = (l_pad + kBlockN - 1) / kBlockN;
@@ -124,12 +123,13 @@ GemmTiling gemm_tiling(int mode, int s_pad, int l_pad) {
   return t;
 }
 
-// Tensor-core FLOPs one product of one matrix executes (padded, symmetric blocks only).
+// Tensor-core FLOPs one product of one matrix executes (padded dimensions;
+// symmetric products: the 256 x 256 pair tiles on or above the diagonal).
 uint64_t executed_flops(int mode, int s_pad, int l_pad) {
-  const uint64_t nb = (uint64_t)s_pad / kBlockM;
-  const uint64_t blk = (uint64_t)kBlockM * kBlockM * 2;
-  if (mode == kGram) return nb * (nb + 1) / 2 * blk * (uint64_t)l_pad;
-  if (mode == kPoly) return nb * (nb + 1) / 2 * blk * (uint64_t)s_pad;
+  const uint64_t nb2 = (uint64_t)s_pad / kPairM;
+  const uint64_t tile = (uint64_t)kPairM * kPairM * 2;
+  if (mode == kGram) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)l_pad;
+  if (mode == kPoly) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)s_pad;
   return 2ull * s_pad * s_pad * (uint64_t)l_pad;
 }
 

@@ -14,8 +14,10 @@ namespace mfsdp {
 constexpr int kMaxBatch = 128;     // matrices per grouped launch
 constexpr int kTile = 64;          // momentum-kernel tile edge (elements)
 constexpr int kPartialsPerTile = 8;  // momentum kernel: one norm partial per warp
-constexpr int kPad = 128;          // workspace matrices are padded to multiples of this
-constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows (UMMA M)
+constexpr int kPad = 128;          // workspace: the long side is padded to a multiple of this
+constexpr int kPadS = 256;         // workspace: the short side is padded to a multiple of this (one CTA pair)
+constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows per CTA (UMMA M)
+constexpr int kPairM = 2 * kBlockM;  // rows of the tile a CTA pair shares (B operand multicast)
 constexpr int kBlockN = 256;       // Newton-Schulz GEMM tile columns (UMMA N)
 constexpr int kBlockK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kStages = 4;         // smem pipeline depth

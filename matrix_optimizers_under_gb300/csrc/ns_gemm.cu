@@ -157,44 +157,51 @@ __device__ __forceinline__ void store_final(const GemmMat& d, int out_bf16, int 
 
 struct Tile {
   int mi;        // matrix index in the batch
-  int m0, n0;    // output tile origin
+  int m0, n0;    // origin of the pair's 256-row output tile
+  int mc;        // this CTA's 128 rows: [mc, mc + 128)
   int N;         // tile width (256, or 128 for the last column tile)
   bool zero;     // the matrix's momentum is exactly zero: no products
 };
 
-__device__ __forceinline__ Tile decode_tile(const GemmBatch& p, int t) {
+// Pair tile t of the launch.  Symmetric products: 256 x 256 tiles on or above
+// the diagonal, row pair-block I holding tiles I .. nb2-1; others: 256-row
+// tiles, rows fastest.
+__device__ __forceinline__ Tile decode_tile(const GemmBatch& p, int t, uint32_t rank) {
   Tile r;
   r.mi = find_mat(p.tile_start, p.n, t);
   const GemmMat& d = p.mat[r.mi];
   const int local = t - p.tile_start[r.mi];
   if (d.symmetric) {
-    // Row block I holds blocks I .. nb-1 in pairs: ceil((nb - I) / 2) tiles.
-    const int nb = d.s_pad / kBlockM;
+    const int nb2 = d.s_pad / kPairM;
     int rem = local, I = 0;
-    while (I < nb - 1 && rem >= ((nb - I + 1) >> 1)) {
-      rem -= (nb - I + 1) >> 1;
+    while (I < nb2 - 1 && rem >= nb2 - I) {
+      rem -= nb2 - I;
       ++I;
     }
-    r.m0 = I * kBlockM;
-    r.n0 = (I + 2 * rem) * kBlockM;
-    r.N = min(kBlockN, d.s_pad - r.n0);
+    r.m0 = I * kPairM;
+    r.n0 = (I + rem) * kPairM;
+    r.N = kBlockN;
   } else {
-    const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // m fastest: neighbours share B-operand columns
-    r.m0 = mt * kBlockM;
+    const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // rows fastest: neighbours share B-operand columns
+    r.m0 = mt * kPairM;
     r.n0 = nt * kBlockN;
     r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
   }
+  r.mc = r.m0 + (int)rank * kBlockM;
   r.zero = p.norm[d.norm_idx].x == 0.0f;
   return r;
 }
 
 // Operand sources of stage kb of a tile (bounds: see the file header).
 __device__ __forceinline__ const uint8_t* a_block(const GemmMat& d, const Tile& tl, int kb, size_t kstride) {
-  return d.a_op + (size_t)kb * kstride + (size_t)(tl.m0 >> 3) * 1024;
+  return d.a_op + (size_t)kb * kstride + (size_t)(tl.mc >> 3) * 1024;
 }
-__device__ __forceinline__ const uint8_t* b_block_kmajor(const GemmMat& d, const Tile& tl, int kb, size_t kstride) {
-  return d.b_op + (size_t)kb * kstride + (size_t)(tl.n0 >> 3) * 1024;
+// K-major B: rows [n0 + half * N/2, + N/2).
+__device__ __forceinline__ const uint8_t* b_half_kmajor(const GemmMat& d, const Tile& tl, int kb, size_t kstride,
+                                                       uint32_t half) {
+  return d.b_op + (size_t)kb * kstride + (size_t)((tl.n0 + (int)half * (tl.N >> 1)) >> 3) * 1024;
 }
+// MN-major X: 64-column block n0/64 + j, K rows [64 kb, 64 kb + 64).
 __device__ __forceinline__ const uint8_t* b_block_mn(const GemmMat& d, const Tile& tl, int kb, size_t kstride, int j) {
   return d.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
 }
@@ -229,9 +236,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.tile_start[p.n];
+  const uint32_t rank = ptx::cluster_ctarank();          // 0 or 1 within the CTA pair
+  const int cid = (int)ptx::cluster_id_x(), ncl = (int)ptx::cluster_count_x();
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const int mode = p.mode;
   const bool b_mn = (mode == kUpdate || mode == kUpdateFinal);
+  constexpr uint16_t kPair = 0x3;                        // both CTAs of the cluster
 
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), kTmemCols);
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 2);   // this CTA's MMAs and the peer's
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[a]), 1);
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();    // both CTAs' barriers exist before any multicast or remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
   volatile int* abort_v = &abort_flag;
@@ -260,29 +270,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // This CTA loads its own 128 rows of the A operand and one half of the
+      // B operand; the B half goes to both CTAs of the pair (multicast), so
+      // each operand byte is read from L2 once per pair.
       const uint64_t pol = ptx::policy_evict_last();
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < total && !*abort_v; t += gridDim.x) {
-        const Tile tl = decode_tile(p, t);
+      for (int t = cid; t < total && !*abort_v; t += ncl) {
+        const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
         const GemmMat& d = p.mat[tl.mi];
         const size_t kstride = colblock_stride(d.s_pad);   // every operand has s_pad rows per column block
-        const uint32_t b_bytes = (uint32_t)tl.N * kBlockK * 2;
+        const uint32_t b_bytes = (uint32_t)tl.N * kBlockK * 2;   // whole B tile: both halves land here
         for (int kb = 0; kb < d.k_blocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t use = it / kStages;
+          // stage s is free in both CTAs (both MMAs have read it)
           if (!wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, abort_v, p.status)) break;
           const uint32_t fb = ptx::smem_u32(&full_bar[s]);
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
           ptx::mbar_arrive_expect_tx(fb, kStageBytesA + b_bytes);
           ptx::bulk_g2s(sa, a_block(d, tl, kb, kstride), kStageBytesA, fb, pol);
           if (!b_mn) {
-            ptx::bulk_g2s(sb, b_block_kmajor(d, tl, kb, kstride), b_bytes, fb, pol);
+            const uint32_t hb = b_bytes >> 1;
+            ptx::bulk_g2s_multicast(sb + rank * hb, b_half_kmajor(d, tl, kb, kstride, rank), hb, fb, kPair, pol);
           } else {
-            // X as the MN-major operand: K rows [64 kb, 64 kb + 64) of column
-            // blocks n0/64 ..; each block's 8 atoms are one 8 KB run.
-            for (int j = 0; j < tl.N / 64; ++j)
-              ptx::bulk_g2s(sb + (uint32_t)j * 8192u, b_block_mn(d, tl, kb, kstride, j), 8192u, fb, pol);
+            // X as the MN-major operand: 64-column blocks of 8 KB; this CTA
+            // fetches the blocks of its half of the tile's columns.
+            const int nblk = tl.N / 64, per = nblk >> 1;
+            for (int j = (int)rank * per; j < ((int)rank + 1) * per; ++j)
+              ptx::bulk_g2s_multicast(sb + (uint32_t)j * 8192u, b_block_mn(d, tl, kb, kstride, j), 8192u, fb, kPair,
+                                      pol);
           }
         }
       }
@@ -296,8 +313,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     if (lane == 0) {
       // --------------------------------------------------------- MMA issuer
       uint32_t it = 0, acc_it = 0;
-      for (int t = blockIdx.x; t < total && !*abort_v; t += gridDim.x) {
-        const Tile tl = decode_tile(p, t);
+      for (int t = cid; t < total && !*abort_v; t += ncl) {
+        const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
         const GemmMat& d = p.mat[tl.mi];
         const uint32_t a = acc_it & 1, ause = acc_it >> 1;
@@ -323,13 +340,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                                         : ptx::smem_desc_sw128(sb + (uint32_t)k * 32u, 16u, 1024u);
             ptx::umma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          ptx::umma_commit(ptx::smem_u32(&empty_bar[s]));   // frees the stage once these MMAs finish
+          // frees stage s in both CTAs once these MMAs have read it
+          ptx::umma_commit_multicast(ptx::smem_u32(&empty_bar[s]), kPair);
         }
         if (!ok) break;
         ptx::umma_commit(ptx::smem_u32(&tfull_bar[a]));     // accumulator complete
         ++acc_it;
       }
-      // Every MMA this thread issued has completed before TMEM is released.
+      // Every MMA this thread issued has completed (and its commits have
+      // arrived) before TMEM is released.
       ptx::umma_commit(ptx::smem_u32(&drain_bar));
       ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, kWaitLimitNs);
     }
@@ -341,10 +360,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(p, t);
+    for (int t = cid; t < total; t += ncl) {
+      const Tile tl = decode_tile(p, t, rank);
       const GemmMat& d = p.mat[tl.mi];
-      const int m = tl.m0 + quad * 32 + lane;          // this thread's output row
+      const int m = tl.mc + quad * 32 + lane;          // this thread's output row
       const int cw = tl.N >> 1;                         // columns per warp
       const int c0 = half * cw;
       if (tl.zero) {
@@ -359,6 +378,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const size_t stride = colblock_stride(d.s_pad);
       const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
       const bool has_c = (mode != kGram);
+      const int rblk = tl.mc >> 7;                     // this CTA's 128-row block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
       // the first chunk before waiting for the MMAs, the next one while the
       // current one is processed.
@@ -385,6 +405,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[a]));
         }
         const int n = tl.n0 + c;
+        const int cblk = n >> 7;
+        // Symmetric products: a block below the diagonal (only inside a
+        // diagonal pair tile) is written by its mirror image; a block above
+        // it is written directly and transposed.
+        const bool below = d.symmetric && cblk < rblk;
+        const bool mirror = d.symmetric && cblk > rblk;
         float v[32];
         if (mode == kGram) {
 #pragma unroll
@@ -402,11 +428,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
         if (mode == kUpdateFinal) {
           store_final(d, p.out_bf16, m, n, v);
-        } else {
+        } else if (!below) {
           uint8_t* out = static_cast<uint8_t*>(d.out);
           store_chunk(out, stride, row_off, m, n, v);
-          if (d.symmetric && (n >> 7) > (tl.m0 >> 7)) {
-            // off-diagonal block: also write its transpose, element (n + j, m)
+          if (mirror) {
+            // element (n + j, m)
             const size_t mcol = (size_t)(m & 7) * 2;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -424,8 +450,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
   }
 
+  // Teardown: no CTA of the pair leaves (or frees TMEM) while its peer may
+  // still multicast into its shared memory or arrive on its barriers.
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -436,15 +464,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
 cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s) {
   if (total_tiles <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  // Persistent: as many CTA pairs as can be resident at once (one CTA per SM).
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+  cfg.gridDim = dim3((unsigned)(2 * (sms / 2)), 1, 1);
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_kernel, &cfg);
   if (e != cudaSuccess) return e;
-  const int grid = total_tiles < sms ? total_tiles : sms;   // persistent: one CTA per SM
-  ns_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(b);
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int clusters = total_tiles < max_clusters ? total_tiles : max_clusters;
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel, b);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -89,7 +89,7 @@ def test_workspace_layout(mfsdp):
     shards = [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131072, 300, 130), mfsdp.make_shard(200000, 1, 9)]
     lay = mfsdp.muon_workspace_layout(shards)
     total = mfsdp.muon_workspace_bytes(shards)
-    assert [l[4:] for l in lay] == [(256, 512, 256, 512), (256, 384, 130, 300), (128, 128, 1, 9)]
+    assert [l[4:] for l in lay] == [(256, 512, 256, 512), (256, 384, 130, 300), (256, 128, 1, 9)]
     end = 0
     for x0, x1, a, b, sp, lp, _, _ in lay:
         assert x0 % 1024 == 0 and x0 >= end
@@ -176,11 +176,11 @@ def test_step_flops(mfsdp):
                      [(4096, 14336), (1024, 4096), (300, 130)])
     assert dense == want_dense
 
-    def ex(s, l):   # padded dims; upper-triangle 128x128 blocks for the symmetric products
-        sp, lp = -(-s // 128) * 128, -(-l // 128) * 128
-        nb = sp // 128
-        blocks = nb * (nb + 1) // 2
-        return 5 * (blocks * 128 * 128 * 2 * lp + blocks * 128 * 128 * 2 * sp + 2 * sp * sp * lp)
+    def ex(s, l):   # short side padded to 256, long to 128; upper-triangle 256x256 tiles when symmetric
+        sp, lp = -(-s // 256) * 256, -(-l // 128) * 128
+        nb2 = sp // 256
+        tiles = nb2 * (nb2 + 1) // 2
+        return 5 * (tiles * 256 * 256 * 2 * lp + tiles * 256 * 256 * 2 * sp + 2 * sp * sp * lp)
     assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300)
     assert executed < dense     # the symmetric skipping outweighs the padding here
     assert mfsdp.muon_step_flops([], 5) == (0, 0)
