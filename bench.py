@@ -42,6 +42,12 @@ from matrix_optimizers_under_gb300 import workloads as W  # noqa: E402
 METRIC = "owner-step ms; Newton–Schulz TFLOP/s (% BF16 peak); AdamW-tail GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) per ns_gemm_kernel launch on the llama3_8b_rank owner set, the
+# mean over one owner step's 15 launches, from the ncu capture summarised in
+# profiles/launches_llama3_8b_rank.md; keyed by the library version it was taken on, so
+# that a changed kernel reports null until it is captured again.
+NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9}
+
 
 # --------------------------------------------------------------------------- helpers
 def load_peaks():
@@ -55,6 +61,23 @@ def load_peaks():
 def ns_flops(rows: int, cols: int, steps: int) -> int:
     s, l = min(rows, cols), max(rows, cols)
     return steps * (4 * s * s * l + 2 * s ** 3)
+
+
+def simulated_rank(heavy: int, rank: int, planner_world: int) -> int:
+    """Owner set a GPU benches under torchrun: the heaviest planner rank on GPU 0,
+    the next ones on the other GPUs (weak scaling: one owner set per GPU)."""
+    return (heavy + rank) % planner_world
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The slowest rank's figure (the step ends when every owner set is done)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def heaviest_rank(plan) -> int:
@@ -221,7 +244,7 @@ def run_ours(args):
 
     plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
     heavy = heaviest_rank(plan)
-    sim_rank = heavy if world == 1 else (heavy + rank) % w.world
+    sim_rank = simulated_rank(heavy, rank, w.world)
     shards = plan.rank_matrices(sim_rank)
     tails = plan.rank_tails(sim_rank)
     numel = plan.rank_matrix_elems[sim_rank]
@@ -305,37 +328,40 @@ def run_ours(args):
     mom_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     ns_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     adam_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
-    step_ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(total_ms / args.steps, dev)
     st, detail = mfsdp.muon_device_status(ws)
     if st != mfsdp.OK:
         raise RuntimeError(f"device status after timed region: {mfsdp.status_string(st)} ({detail})")
 
     # ---------------------------------------------------------- end to end
+    # Through the host-buffer entry point: each step copies the gradient in from
+    # pinned host memory and the update back out, shard group by shard group,
+    # overlapped with the compute of the neighbouring groups; the AdamW tail's
+    # gradient comes in and its parameters go back out too.
     e2e_steps = max(1, min(args.steps, 5))
     h2d = grad_host.numel() * grad_host.element_size() + (tg_host.numel() * 4 if tail_numel else 0)
     d2h = upd_host.numel() * 2 + (tp_host.numel() * 4 if tail_numel else 0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        grad.copy_(grad_host, non_blocking=True)
+
+    def one_step_host():
+        step_counter[0] += 1
+        mfsdp.muon_owner_step_host(shards, grad_host, grad, mom, upd, upd_host, ws, groups=args.e2e_groups, **kw)
         if tail_numel:
             tg.copy_(tg_host, non_blocking=True)
-        one_step()
-        upd_host.copy_(upd, non_blocking=True)
-        if tail_numel:
+            mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
+                                  wd=w.weight_decay, step=step_counter[0])
             tp_host.copy_(tp, non_blocking=True)
+
+    one_step_host()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        one_step_host()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
 
     # ---------------------------------------------------------- supplementary: a large AdamW tail
     sup = {}
@@ -404,13 +430,15 @@ def run_ours(args):
                    "flops_dense": flops, "flops_executed": flops_exec,
                    "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1)},
         "roofline": {"kernel": "ns_gemm_kernel", "bound": "tensor", "achieved": round(ns_tflops_exec, 1),
-                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4), "traffic": None,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4),
+                     "traffic": NS_GEMM_TRAFFIC.get((mfsdp.version(), w.name)),
                      "peak_source": f"{peak_src} bf16_tflops_sustained",
                      "flops": "executed tensor-core FLOPs (symmetric Gram/polynomial: upper-triangle blocks only)",
                      "flops_per_launch": round(flops_exec / max(ns_launches, 1)), "launches_per_step": ns_launches},
         "clocks": clocks,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
+                "pipeline_groups": args.e2e_groups},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,
@@ -432,6 +460,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b_rank", choices=W.ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-supplementary", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=4,
+                    help="shard groups the host-buffer step overlaps copies with (1 = no overlap)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -184,6 +184,31 @@ int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_sha
                                  void* workspace, size_t workspace_bytes, void* stream,
                                  int32_t phases);
 
+/* The owner step with the gradient coming from, and the update going to,
+ * pinned host memory.  The shards are cut, in offset order, into `groups`
+ * groups of roughly equal Newton-Schulz cost; group g's gradient range is
+ * copied host->device on an internal stream while group g-1 computes on
+ * `stream`, and its update range is copied device->host on another internal
+ * stream while group g+1 computes.  Each group runs the same kernels as
+ * mfsdp_muon_owner_step on its own shards (results are bit-identical).
+ *   grad_host / update_host  pinned host buffers (cudaHostAlloc / registered),
+ *                            numel elements of grad_dtype / update_dtype.
+ *   grad_dev / update_dev    device staging buffers of numel elements; every
+ *                            other argument as for mfsdp_muon_owner_step.
+ *   groups >= 1 (1 = no overlap).
+ * The call returns once everything is queued; work queued on `stream` later
+ * runs after the last copy.  The helper streams and events are created and
+ * destroyed inside the call.  Errors: as mfsdp_muon_owner_step, plus
+ * INVALID_ARG for a NULL host buffer or groups < 1. */
+int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                               const void* grad_host, void* grad_dev, int32_t grad_dtype,
+                               float* momentum,
+                               void* update_dev, void* update_host, int32_t update_dtype,
+                               int64_t numel,
+                               double beta, int32_t nesterov, int32_t ns_steps,
+                               double a, double b, double c, double eps,
+                               void* workspace, size_t workspace_bytes, int32_t groups, void* stream);
+
 /* mfsdp_muon_owner_step for callers that cannot allocate device memory (no
  * counterpart in the paper: an addition of this library).  Some callers have
  * no allocator to provide the workspace from -- a plug-in inside a framework

@@ -39,7 +39,7 @@ PHASE_NEWTON_SCHULZ = 2
 EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
-            "mfsdp_muon_step_flops")
+            "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host")
 
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -83,6 +83,9 @@ _lib.mfsdp_muon_owner_step.argtypes = _STEP_ARGS
 _lib.mfsdp_muon_owner_step.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_phases.argtypes = _STEP_ARGS + [_i32]
 _lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
+_lib.mfsdp_muon_owner_step_host.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32,
+                                            _i64, _d, _i32, _i32, _d, _d, _d, _d, _vp, _sz, _i32, _vp]
+_lib.mfsdp_muon_owner_step_host.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_static_scratch.argtypes = _STEP_ARGS[:15] + [_vp]
 _lib.mfsdp_muon_owner_step_static_scratch.restype = ctypes.c_int
 _lib.mfsdp_muon_step_flops.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, ctypes.POINTER(_u64),
@@ -228,6 +231,26 @@ def muon_owner_step(shards: Sequence[MatrixShard], grad, momentum, update, works
         _check(_lib.mfsdp_muon_owner_step(*args), "muon_owner_step")
     else:
         _check(_lib.mfsdp_muon_owner_step_phases(*args, int(phases)), "muon_owner_step_phases")
+
+
+def muon_owner_step_host(shards: Sequence[MatrixShard], grad_host, grad_dev, momentum, update_dev, update_host,
+                         workspace, *, groups: int = 4, beta: float = 0.95, nesterov: bool = False,
+                         ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315), eps: float = 1e-7,
+                         numel: Optional[int] = None, stream=None) -> None:
+    """The owner step with the gradient read from and the update written to pinned
+    host tensors, the copies of each shard group overlapped with the compute of
+    its neighbours (see include/mfsdp.h).  grad_dev/update_dev are device staging
+    tensors of the same length."""
+    arr = _shard_array(shards)
+    n = int(numel if numel is not None else grad_dev.numel())
+    a, b, c = coeffs
+    _check(_lib.mfsdp_muon_owner_step_host(arr, len(shards), _ptr(grad_host), _ptr(grad_dev), _dtype_code(grad_dev),
+                                           _ptr(momentum), _ptr(update_dev), _ptr(update_host), _dtype_code(update_dev),
+                                           n, float(beta), int(bool(nesterov)), int(ns_steps), float(a), float(b),
+                                           float(c), float(eps), _ptr(workspace),
+                                           int(workspace.numel() if workspace is not None else 0), int(groups),
+                                           _stream(stream)),
+           "muon_owner_step_host")
 
 
 def muon_owner_step_static_scratch(shards: Sequence[MatrixShard], grad, momentum, update, *, beta: float = 0.95,

@@ -161,7 +161,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.1.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.5.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -183,20 +183,18 @@ extern "C" int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int
   return MFSDP_OK;
 }
 
-extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_shards,
-                                            const void* grad, int32_t grad_dtype, float* momentum, void* update,
-                                            int32_t update_dtype, int64_t numel, double beta_d, int32_t nesterov,
-                                            int32_t ns_steps, double a_d, double b_d, double c_d, double eps_d,
-                                            void* workspace, size_t workspace_bytes, void* stream_ptr,
-                                            int32_t phases) {
-  // ------------------------------------------------------------ validation
-  if (phases <= 0 || (phases & ~(MFSDP_PHASE_MOMENTUM | MFSDP_PHASE_NEWTON_SCHULZ)) != 0)
-    return MFSDP_ERR_INVALID_ARG;
+namespace mfsdp {
+namespace {
+
+// Every check of the owner-step arguments (host only, nothing queued).
+int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
+                  const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
+                  int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps,
+                  const void* workspace, size_t workspace_bytes, Layout* L) {
   if (n_shards < 0 || (n_shards > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
-  if (!std::isfinite(beta_d) || !std::isfinite(a_d) || !std::isfinite(b_d) || !std::isfinite(c_d) ||
-      !std::isfinite(eps_d) || eps_d < 0.0)
+  if (!std::isfinite(beta) || !std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) ||
+      eps < 0.0)
     return MFSDP_ERR_INVALID_ARG;
-  const float beta = (float)beta_d, a = (float)a_d, b = (float)b_d, c = (float)c_d, eps = (float)eps_d;
   if (grad_dtype != MFSDP_DTYPE_F32 && grad_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
   if (update_dtype != MFSDP_DTYPE_F32 && update_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
   if (numel < 0 || ns_steps < 0 || ns_steps > 64 || (nesterov != 0 && nesterov != 1)) return MFSDP_ERR_INVALID_ARG;
@@ -204,22 +202,18 @@ extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, in
   if (!grad || !momentum || !update || !workspace) return MFSDP_ERR_INVALID_ARG;
   if (!aligned(grad, 16) || !aligned(momentum, 16) || !aligned(update, 16) || !aligned(workspace, 256))
     return MFSDP_ERR_MISALIGNED;
-
-  Layout L;
-  int st = make_layout(shards, n_shards, &L);
+  const int st = make_layout(shards, n_shards, L);
   if (st != MFSDP_OK) return st;
   for (int i = 0; i < n_shards; ++i) {
     const mfsdp_matrix_shard& sh = shards[i];
     if (sh.offset < 0 || sh.offset > numel || sh.rows * sh.cols > numel - sh.offset) return MFSDP_ERR_OUT_OF_BOUNDS;
   }
-  {
-    std::vector<int> ord(n_shards);
-    for (int i = 0; i < n_shards; ++i) ord[i] = i;
-    std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
-    for (int k = 1; k < n_shards; ++k) {
-      const mfsdp_matrix_shard& p0 = shards[ord[k - 1]];
-      if (p0.offset + p0.rows * p0.cols > shards[ord[k]].offset) return MFSDP_ERR_OVERLAP;
-    }
+  std::vector<int> ord(n_shards);
+  for (int i = 0; i < n_shards; ++i) ord[i] = i;
+  std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
+  for (int k = 1; k < n_shards; ++k) {
+    const mfsdp_matrix_shard& p0 = shards[ord[k - 1]];
+    if (p0.offset + p0.rows * p0.cols > shards[ord[k]].offset) return MFSDP_ERR_OVERLAP;
   }
   const size_t gbytes = (size_t)numel * dtype_size(grad_dtype), mbytes = (size_t)numel * 4,
                ubytes = (size_t)numel * dtype_size(update_dtype);
@@ -227,14 +221,31 @@ extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, in
   if (ranges_overlap(momentum, mbytes, grad, gbytes) || ranges_overlap(momentum, mbytes, update, ubytes) ||
       (!in_place && ranges_overlap(grad, gbytes, update, ubytes)))
     return MFSDP_ERR_OVERLAP;
-  if (workspace_bytes < L.bytes) return MFSDP_ERR_WORKSPACE_TOO_SMALL;
-  if (ranges_overlap(workspace, L.bytes, grad, gbytes) || ranges_overlap(workspace, L.bytes, momentum, mbytes) ||
-      ranges_overlap(workspace, L.bytes, update, ubytes))
+  if (workspace_bytes < L->bytes) return MFSDP_ERR_WORKSPACE_TOO_SMALL;
+  if (ranges_overlap(workspace, L->bytes, grad, gbytes) || ranges_overlap(workspace, L->bytes, momentum, mbytes) ||
+      ranges_overlap(workspace, L->bytes, update, ubytes))
     return MFSDP_ERR_OVERLAP;
+  return MFSDP_OK;
+}
 
+}  // namespace
+}  // namespace mfsdp
+
+extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                                            const void* grad, int32_t grad_dtype, float* momentum, void* update,
+                                            int32_t update_dtype, int64_t numel, double beta_d, int32_t nesterov,
+                                            int32_t ns_steps, double a_d, double b_d, double c_d, double eps_d,
+                                            void* workspace, size_t workspace_bytes, void* stream_ptr,
+                                            int32_t phases) {
+  if (phases <= 0 || (phases & ~(MFSDP_PHASE_MOMENTUM | MFSDP_PHASE_NEWTON_SCHULZ)) != 0)
+    return MFSDP_ERR_INVALID_ARG;
+  Layout L;
+  int st = validate_step(shards, n_shards, grad, grad_dtype, momentum, update, update_dtype, numel, beta_d, nesterov,
+                         ns_steps, a_d, b_d, c_d, eps_d, workspace, workspace_bytes, &L);
+  if (st != MFSDP_OK || n_shards == 0) return st;
+  const float beta = (float)beta_d, a = (float)a_d, b = (float)b_d, c = (float)c_d, eps = (float)eps_d;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-
   if (phases & MFSDP_PHASE_MOMENTUM) {
     st = launch_momentum_phase(shards, n_shards, L, grad, grad_dtype, momentum, beta, nesterov, eps, ws, stream);
     if (st != MFSDP_OK) return st;
@@ -244,6 +255,106 @@ extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, in
     if (st != MFSDP_OK) return st;
   }
   return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad_host,
+                                          void* grad_dev, int32_t grad_dtype, float* momentum, void* update_dev,
+                                          void* update_host, int32_t update_dtype, int64_t numel, double beta_d,
+                                          int32_t nesterov, int32_t ns_steps, double a_d, double b_d, double c_d,
+                                          double eps_d, void* workspace, size_t workspace_bytes, int32_t groups,
+                                          void* stream_ptr) {
+  if (groups < 1) return MFSDP_ERR_INVALID_ARG;
+  Layout L;
+  int st = validate_step(shards, n_shards, grad_dev, grad_dtype, momentum, update_dev, update_dtype, numel, beta_d,
+                         nesterov, ns_steps, a_d, b_d, c_d, eps_d, workspace, workspace_bytes, &L);
+  if (st != MFSDP_OK || n_shards == 0) return st;
+  if (!grad_host || !update_host) return MFSDP_ERR_INVALID_ARG;
+  const float beta = (float)beta_d, a = (float)a_d, b = (float)b_d, c = (float)c_d, eps = (float)eps_d;
+  const size_t gsz = dtype_size(grad_dtype), usz = dtype_size(update_dtype);
+
+  // Groups: shards in offset order, cut where the running Newton-Schulz cost
+  // crosses k/groups of the total, so the groups' compute is balanced and each
+  // group's segments form one contiguous range of the flat buffers.
+  std::vector<int> ord(n_shards);
+  for (int i = 0; i < n_shards; ++i) ord[i] = i;
+  std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
+  std::vector<double> cost(n_shards);
+  double total = 0.0;
+  for (int i = 0; i < n_shards; ++i) {
+    const double s = (double)std::min(shards[i].rows, shards[i].cols), l = (double)std::max(shards[i].rows, shards[i].cols);
+    cost[i] = 4.0 * s * s * l + 2.0 * s * s * s + s * l;   // + s*l: the momentum pass
+    total += cost[i];
+  }
+  const int ng = std::min<int>(groups, n_shards);
+  std::vector<std::vector<mfsdp_matrix_shard>> grp(ng);
+  double run = 0.0;
+  for (int k = 0; k < n_shards; ++k) {
+    const int i = ord[k];
+    int g = (int)(run / total * ng);
+    g = std::min(std::max(g, 0), ng - 1);
+    grp[g].push_back(shards[i]);
+    run += cost[i];
+  }
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> ev;   // ev[0]: entry; per group: copied in, computed, copied out
+  auto cleanup = [&]() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  };
+  if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess) {
+    cleanup();
+    return MFSDP_ERR_CUDA;
+  }
+  ev.resize(1 + 3 * (size_t)ng, nullptr);
+  for (auto& e : ev) {
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      e = nullptr;
+      cleanup();
+      return MFSDP_ERR_CUDA;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t ce = cudaEventRecord(ev[0], stream);            // earlier work on `stream` comes first
+  ce = ce == cudaSuccess ? cudaStreamWaitEvent(s_in, ev[0], 0) : ce;
+  for (int g = 0; g < ng && ce == cudaSuccess && st == MFSDP_OK; ++g) {
+    const std::vector<mfsdp_matrix_shard>& sh = grp[g];
+    if (sh.empty()) continue;
+    int64_t lo = sh.front().offset, hi = 0;
+    for (const auto& x : sh) {
+      lo = std::min(lo, x.offset);
+      hi = std::max(hi, x.offset + x.rows * x.cols);
+    }
+    cudaEvent_t e_in = ev[1 + 3 * g], e_done = ev[2 + 3 * g], e_out = ev[3 + 3 * g];
+    ce = cudaMemcpyAsync(static_cast<uint8_t*>(grad_dev) + (size_t)lo * gsz,
+                         static_cast<const uint8_t*>(grad_host) + (size_t)lo * gsz, (size_t)(hi - lo) * gsz,
+                         cudaMemcpyHostToDevice, s_in);
+    if (ce == cudaSuccess) ce = cudaEventRecord(e_in, s_in);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, e_in, 0);
+    if (ce != cudaSuccess) break;
+    Layout Lg;
+    st = make_layout(sh.data(), (int)sh.size(), &Lg);        // fits: never larger than the whole set's layout
+    if (st != MFSDP_OK) break;
+    st = launch_momentum_phase(sh.data(), (int)sh.size(), Lg, grad_dev, grad_dtype, momentum, beta, nesterov, eps, ws,
+                               stream);
+    if (st != MFSDP_OK) break;
+    st = launch_ns_phase(sh.data(), (int)sh.size(), Lg, update_dev, update_dtype, ns_steps, a, b, c, ws, stream);
+    if (st != MFSDP_OK) break;
+    ce = cudaEventRecord(e_done, stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s_out, e_done, 0);
+    if (ce == cudaSuccess)
+      ce = cudaMemcpyAsync(static_cast<uint8_t*>(update_host) + (size_t)lo * usz,
+                           static_cast<const uint8_t*>(update_dev) + (size_t)lo * usz, (size_t)(hi - lo) * usz,
+                           cudaMemcpyDeviceToHost, s_out);
+    if (ce == cudaSuccess) ce = cudaEventRecord(e_out, s_out);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, e_out, 0);   // `stream` ends after every copy
+  }
+  cleanup();
+  if (ce != cudaSuccess) return MFSDP_ERR_CUDA;
+  return st;
 }
 
 extern "C" int mfsdp_muon_owner_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad,

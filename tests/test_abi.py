@@ -152,6 +152,23 @@ def test_step_error_paths(mfsdp):
     assert step(mfsdp, [], phases=mfsdp.PHASE_NEWTON_SCHULZ, grad=None, mom=None, upd=None, ws=None) == mfsdp.OK
 
 
+def test_host_entry_error_paths(mfsdp):
+    lib = mfsdp.raw_lib()
+    ok = [mfsdp.make_shard(0, 256, 512)]
+    arr = (mfsdp.MatrixShard * 1)(*ok)
+    wsb = mfsdp.muon_workspace_bytes(ok)
+    H1, H2 = 0x50000000, 0x60000000
+
+    def call(gh=H1, uh=H2, groups=4, grad=G, ws=WS):
+        return lib.mfsdp_muon_owner_step_host(arr, 1, gh, grad, BF, M, U, uh, BF, 1 << 20, 0.95, 0, 5, 3.4445,
+                                              -4.775, 2.0315, 1e-7, ws, wsb, groups, None)
+    assert call(groups=0) == mfsdp.ERR_INVALID_ARG
+    assert call(gh=None) == mfsdp.ERR_INVALID_ARG
+    assert call(uh=None) == mfsdp.ERR_INVALID_ARG
+    assert call(grad=G + 2) == mfsdp.ERR_MISALIGNED
+    assert call(ws=G) == mfsdp.ERR_OVERLAP
+
+
 def test_adamw_error_paths(mfsdp):
     lib = mfsdp.raw_lib()
     P, Gp, Mm, V = 0x10000000, 0x20000000, 0x30000000, 0x40000000

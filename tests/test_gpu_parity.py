@@ -268,6 +268,31 @@ def test_phase_split_matches_full_step(mfsdp):
     assert np.array_equal(mom.cpu().numpy(), m1)
 
 
+@pytest.mark.parametrize("groups", [1, 2, 3, 8])
+def test_host_buffer_pipeline_matches_resident_step(mfsdp, groups):
+    """Gradient from pinned host memory, update back to it, copies overlapped with
+    compute group by group: bit-identical to the resident step."""
+    dev = _dev()
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    mom0 = np.zeros(numel, np.float32)
+    u_ref, m_ref, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.bfloat16)
+    gh = torch.from_numpy(grad.view(np.int16)).view(torch.bfloat16).pin_memory()
+    uh = torch.full((numel,), float("nan"), dtype=torch.bfloat16).pin_memory()
+    gd = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    ud = torch.full((numel,), float("nan"), dtype=torch.bfloat16, device=dev)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step_host(shards, gh, gd, mom, ud, uh, ws, groups=groups)
+    torch.cuda.synchronize()
+    out = H.bf16_bits_to_f32(uh.view(torch.int16).numpy().view(np.uint16))
+    for s in shards:
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        assert np.array_equal(out[seg].view(np.uint32), u_ref[seg].view(np.uint32)), (groups, s.param_id)
+    assert np.array_equal(mom.cpu().numpy(), m_ref)
+
+
 def test_determinism(mfsdp):
     w = W.get("gpt2_block")
     plan, r, shards, numel = owner_set(mfsdp, w)
