@@ -184,6 +184,33 @@ int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_sha
                                  void* workspace, size_t workspace_bytes, void* stream,
                                  int32_t phases);
 
+/* The owner step followed by applying the update to the weights, fused into
+ * the last Newton-Schulz epilogue.  The pages stop at the orthogonalised
+ * update; applying it is the step right after, in Muon's decoupled form:
+ *   W <- W * (1 - lr * weight_decay) - lr * scale * O
+ * with scale_mode 0: scale = 1; 1: sqrt(max(1, rows/cols)); 2:
+ * 0.2 * sqrt(max(rows, cols)).  The products run in fp32 from the same fp32
+ * accumulator the update comes from (bf16 weights are rounded once).
+ *   weights  device, numel elements of weight_dtype (F32 or BF16), the same
+ *            offsets as the gradient; read and written.  Must not overlap the
+ *            other buffers.
+ *   update   may be NULL (O is then not stored); otherwise as for
+ *            mfsdp_muon_owner_step, and the O it receives is bit-identical.
+ *   ns_steps >= 1.  A matrix with all-zero momentum has O = 0, so its
+ *            weights only decay.
+ * Errors: as mfsdp_muon_owner_step, plus INVALID_ARG (NULL weights, bad
+ * scale_mode, non-finite lr/weight_decay, ns_steps < 1). */
+int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int32_t n_shards,
+                                const void* grad, int32_t grad_dtype,
+                                float* momentum,
+                                void* update, int32_t update_dtype,
+                                void* weights, int32_t weight_dtype,
+                                int64_t numel,
+                                double beta, int32_t nesterov, int32_t ns_steps,
+                                double a, double b, double c, double eps,
+                                double lr, double weight_decay, int32_t scale_mode,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* The owner step with the gradient coming from, and the update going to,
  * pinned host memory.  The shards are cut, in offset order, into `groups`
  * groups of roughly equal Newton-Schulz cost; group g's gradient range is

@@ -39,7 +39,11 @@ PHASE_NEWTON_SCHULZ = 2
 EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
-            "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host")
+            "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply")
+
+SCALE_NONE = 0      # scale = 1
+SCALE_MUON = 1      # scale = sqrt(max(1, rows/cols))
+SCALE_RMS = 2       # scale = 0.2 * sqrt(max(rows, cols))
 
 STATIC_SCRATCH_BYTES = 64 << 20
 
@@ -86,6 +90,9 @@ _lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_host.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32,
                                             _i64, _d, _i32, _i32, _d, _d, _d, _d, _vp, _sz, _i32, _vp]
 _lib.mfsdp_muon_owner_step_host.restype = ctypes.c_int
+_lib.mfsdp_muon_owner_step_apply.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32,
+                                             _i64, _d, _i32, _i32, _d, _d, _d, _d, _d, _d, _i32, _vp, _sz, _vp]
+_lib.mfsdp_muon_owner_step_apply.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_static_scratch.argtypes = _STEP_ARGS[:15] + [_vp]
 _lib.mfsdp_muon_owner_step_static_scratch.restype = ctypes.c_int
 _lib.mfsdp_muon_step_flops.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, ctypes.POINTER(_u64),
@@ -231,6 +238,24 @@ def muon_owner_step(shards: Sequence[MatrixShard], grad, momentum, update, works
         _check(_lib.mfsdp_muon_owner_step(*args), "muon_owner_step")
     else:
         _check(_lib.mfsdp_muon_owner_step_phases(*args, int(phases)), "muon_owner_step_phases")
+
+
+def muon_owner_step_apply(shards: Sequence[MatrixShard], grad, momentum, update, weights, workspace, *, lr: float,
+                          weight_decay: float = 0.0, scale_mode: int = SCALE_MUON, beta: float = 0.95,
+                          nesterov: bool = False, ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315),
+                          eps: float = 1e-7, numel: Optional[int] = None, stream=None) -> None:
+    """The owner step, then W <- W*(1 - lr*wd) - lr*scale*O fused into the last
+    epilogue (see include/mfsdp.h).  update may be None."""
+    arr = _shard_array(shards)
+    n = int(numel if numel is not None else grad.numel())
+    a, b, c = coeffs
+    _check(_lib.mfsdp_muon_owner_step_apply(arr, len(shards), _ptr(grad), _dtype_code(grad), _ptr(momentum),
+                                            _ptr(update), _dtype_code(update) if update is not None else DTYPE_BF16,
+                                            _ptr(weights), _dtype_code(weights), n, float(beta), int(bool(nesterov)),
+                                            int(ns_steps), float(a), float(b), float(c), float(eps), float(lr),
+                                            float(weight_decay), int(scale_mode), _ptr(workspace),
+                                            int(workspace.numel() if workspace is not None else 0), _stream(stream)),
+           "muon_owner_step_apply")
 
 
 def muon_owner_step_host(shards: Sequence[MatrixShard], grad_host, grad_dev, momentum, update_dev, update_host,

@@ -136,9 +136,23 @@ uint64_t executed_flops(int mode, int s_pad, int l_pad) {
 int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
                           int32_t grad_dtype, float* momentum, float beta, int32_t nesterov, float eps, uint8_t* ws,
                           cudaStream_t stream);
+// Optional last-epilogue application of the update to the weights.
+struct ApplyArgs {
+  void* w;            // flat weights, same offsets as the gradient
+  int32_t w_dtype;
+  double lr, wd;
+  int32_t scale_mode; // 0: 1; 1: sqrt(max(1, rows/cols)); 2: 0.2*sqrt(max(rows, cols))
+};
+
 int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, void* update,
                     int32_t update_dtype, int32_t ns_steps, float a, float b, float c, uint8_t* ws,
-                    cudaStream_t stream);
+                    cudaStream_t stream, const ApplyArgs* apply = nullptr);
+
+double shape_scale(int64_t rows, int64_t cols, int32_t mode) {
+  if (mode == 1) return std::sqrt(std::max(1.0, (double)rows / (double)cols));
+  if (mode == 2) return 0.2 * std::sqrt((double)std::max(rows, cols));
+  return 1.0;
+}
 
 }  // namespace
 }  // namespace mfsdp
@@ -161,7 +175,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.5.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.6.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -255,6 +269,41 @@ extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, in
     if (st != MFSDP_OK) return st;
   }
   return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad,
+                                           int32_t grad_dtype, float* momentum, void* update, int32_t update_dtype,
+                                           void* weights, int32_t weight_dtype, int64_t numel, double beta,
+                                           int32_t nesterov, int32_t ns_steps, double a, double b, double c,
+                                           double eps, double lr, double weight_decay, int32_t scale_mode,
+                                           void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  if (weight_dtype != MFSDP_DTYPE_F32 && weight_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
+  if (scale_mode < 0 || scale_mode > 2 || !std::isfinite(lr) || !std::isfinite(weight_decay) || ns_steps < 1)
+    return MFSDP_ERR_INVALID_ARG;
+  // The weights stand in for the update buffer in the common checks when no
+  // update is requested; both are checked against each other below.
+  void* checked = update ? update : weights;
+  const int32_t checked_dtype = update ? update_dtype : weight_dtype;
+  Layout L;
+  int st = validate_step(shards, n_shards, grad, grad_dtype, momentum, checked, checked_dtype, numel, beta, nesterov,
+                         ns_steps, a, b, c, eps, workspace, workspace_bytes, &L);
+  if (st != MFSDP_OK || n_shards == 0) return st;
+  if (!weights) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(weights, 16)) return MFSDP_ERR_MISALIGNED;
+  const size_t wbytes = (size_t)numel * dtype_size(weight_dtype);
+  if (ranges_overlap(weights, wbytes, grad, (size_t)numel * dtype_size(grad_dtype)) ||
+      ranges_overlap(weights, wbytes, momentum, (size_t)numel * 4) ||
+      ranges_overlap(weights, wbytes, workspace, L.bytes) ||
+      (update && ranges_overlap(weights, wbytes, update, (size_t)numel * dtype_size(update_dtype))))
+    return MFSDP_ERR_OVERLAP;
+  const float fb = (float)beta, fe = (float)eps;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  st = launch_momentum_phase(shards, n_shards, L, grad, grad_dtype, momentum, fb, nesterov, fe, ws, stream);
+  if (st != MFSDP_OK) return st;
+  ApplyArgs ap{weights, weight_dtype, lr, weight_decay, scale_mode};
+  return launch_ns_phase(shards, n_shards, L, update, update_dtype, ns_steps, (float)a, (float)b, (float)c, ws, stream,
+                         &ap);
 }
 
 extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad_host,
@@ -430,7 +479,7 @@ int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const 
 
 int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, void* update,
                     int32_t update_dtype, int32_t ns_steps, float a, float b, float c, uint8_t* ws,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const ApplyArgs* apply) {
   float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   const size_t usz = dtype_size(update_dtype);
@@ -484,6 +533,10 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
         gb.c = c;
         gb.norm = norm;
         gb.status = status;
+        if (apply) {
+          gb.decay = (float)(1.0 - apply->lr * apply->wd);
+          gb.w_bf16 = apply->w_dtype == MFSDP_DTYPE_BF16;
+        }
         // Longest K first: the persistent CTAs take tiles round-robin, so the
         // last rounds hold the cheapest tiles.
         std::vector<int> order(cnt);
@@ -517,8 +570,16 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
             d.k_blocks = m.s_pad / kBlockK;
           } else {
             d.a_op = ws + m.b; d.b_op = xc; d.c_in = xc;
-            d.out = last ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz)
-                         : static_cast<void*>(xn);
+            if (!last) {
+              d.out = xn;
+            } else {
+              d.out = update ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz)
+                             : nullptr;
+              if (apply) {
+                d.w = static_cast<uint8_t*>(apply->w) + (size_t)shards[i].offset * dtype_size(apply->w_dtype);
+                d.lr_scale = (float)(apply->lr * shape_scale(shards[i].rows, shards[i].cols, apply->scale_mode));
+              }
+            }
             d.k_blocks = m.s_pad / kBlockK;
           }
           gb.tile_start[k] = tiles;

@@ -85,7 +85,8 @@ struct GemmMat {
   const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
   const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
   const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly, X for kUpdate*)
-  void* out;             // blocked bf16 output, or the caller's buffer at the shard offset
+  void* out;             // blocked bf16 output, or the caller's buffer at the shard offset (may be null)
+  void* w;               // kUpdateFinal with apply: the weights at the shard offset, else null
   int32_t s_pad, l_pad;
   int32_t s, l;          // true short / long side
   int32_t tiles_m, tiles_n;
@@ -95,6 +96,8 @@ struct GemmMat {
   int32_t transposed;    // kUpdateFinal: stored matrix is l x s
   int32_t vec_ok;        // kUpdateFinal: row-major stores may use 16-byte vectors
   int32_t symmetric;     // kGram / kPoly: upper-triangle tiles only, mirrored on store
+  float lr_scale;        // apply: lr * shape scale of this matrix
+  int32_t pad;
 };
 struct GemmBatch {
   int32_t n;
@@ -102,6 +105,8 @@ struct GemmBatch {
   int32_t first_iter;    // fold the 1/(||U||+eps) prescale into this launch
   int32_t out_bf16;      // kUpdateFinal: output dtype
   float a, b, c;
+  float decay;           // apply: 1 - lr * weight_decay
+  int32_t w_bf16;        // apply: weight dtype
   int32_t pad;
   const float2* norm;
   int32_t* status;       // device status word (timeouts)

@@ -109,14 +109,32 @@ __device__ __forceinline__ void store_chunk(uint8_t* base, size_t stride, size_t
   }
 }
 
-// Final update for 32 consecutive X columns [n, n+32) of X row m, written in
-// the caller's layout: stored (m, n) when not transposed, (n, m) otherwise.
-__device__ __forceinline__ void store_final(const GemmMat& d, int out_bf16, int m, int n, const float (&v)[32]) {
+// One element of the final step at a stored position: the update O (when the
+// caller asked for it) and, when applying, W <- decay * W - lr_scale * O.
+__device__ __forceinline__ void final_elem(const GemmMat& d, const GemmBatch& p, int64_t o, float v) {
+  if (d.out) {
+    if (p.out_bf16) static_cast<__nv_bfloat16*>(d.out)[o] = __float2bfloat16_rn(v);
+    else static_cast<float*>(d.out)[o] = v;
+  }
+  if (d.w) {
+    if (p.w_bf16) {
+      __nv_bfloat16* w = static_cast<__nv_bfloat16*>(d.w) + o;
+      *w = __float2bfloat16_rn(fmaf(-d.lr_scale, v, p.decay * __bfloat162float(*w)));
+    } else {
+      float* w = static_cast<float*>(d.w) + o;
+      *w = fmaf(-d.lr_scale, v, p.decay * *w);
+    }
+  }
+}
+
+// Final update for 32 consecutive X columns [n, n+32) of X row m, in the
+// caller's layout: stored (m, n) when not transposed, (n, m) otherwise.
+__device__ __forceinline__ void store_final(const GemmMat& d, const GemmBatch& p, int m, int n, const float (&v)[32]) {
   if (m >= d.s) return;
   if (!d.transposed) {
     const int64_t row0 = (int64_t)m * d.l;
-    if (d.vec_ok && n + 32 <= d.l) {
-      if (out_bf16) {
+    if (d.vec_ok && !d.w && n + 32 <= d.l) {
+      if (p.out_bf16) {
         uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(d.out) + row0 + n);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -134,24 +152,15 @@ __device__ __forceinline__ void store_final(const GemmMat& d, int out_bf16, int 
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (n + j < d.l) {
-          if (out_bf16) static_cast<__nv_bfloat16*>(d.out)[row0 + n + j] = __float2bfloat16_rn(v[j]);
-          else static_cast<float*>(d.out)[row0 + n + j] = v[j];
-        }
-      }
+      for (int j = 0; j < 32; ++j)
+        if (n + j < d.l) final_elem(d, p, row0 + n + j, v[j]);
     }
   } else {
     // stored matrix is l x s: element (n + j, m); the warp's 32 rows m are
     // contiguous in memory, so each j is one coalesced store.
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (n + j < d.l) {
-        const int64_t o = (int64_t)(n + j) * d.s + m;
-        if (out_bf16) static_cast<__nv_bfloat16*>(d.out)[o] = __float2bfloat16_rn(v[j]);
-        else static_cast<float*>(d.out)[o] = v[j];
-      }
-    }
+    for (int j = 0; j < 32; ++j)
+      if (n + j < d.l) final_elem(d, p, (int64_t)(n + j) * d.s + m, v[j]);
   }
 }
 
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           float z[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = 0.f;
-          for (int c = c0; c < c0 + cw; c += 32) store_final(d, p.out_bf16, m, tl.n0 + c, z);
+          for (int c = c0; c < c0 + cw; c += 32) store_final(d, p, m, tl.n0 + c, z);
         }
         continue;
       }
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
         if (mode == kUpdateFinal) {
-          store_final(d, p.out_bf16, m, n, v);
+          store_final(d, p, m, n, v);
         } else if (!below) {
           uint8_t* out = static_cast<uint8_t*>(d.out);
           store_chunk(out, stride, row_off, m, n, v);

@@ -93,3 +93,29 @@ def muon_owner_step_ref(shards: Sequence[Dict[str, int]], grad_flat: np.ndarray,
         M_all[o:o + r * c_] = M_new.reshape(-1)
         out[sh["param_id"]] = O
     return M_all, out
+
+
+# ---------------------------------------------------------------------------
+# Applying the update to the weights.
+#
+# The pages stop at the orthogonalised update ("the update matches full-matrix
+# Muon").  Applying it is the step right after; the pages give neither the
+# learning rate nor a shape-dependent scale, so the reading here is Muon's
+# decoupled form W <- W*(1 - lr*wd) - lr*scale*O with three scale choices:
+#   mode 0: scale = 1
+#   mode 1: scale = sqrt(max(1, rows/cols))        (Muon's reference scaling)
+#   mode 2: scale = 0.2*sqrt(max(rows, cols))       (scaling that matches AdamW's
+#                                                   update RMS, Liu et al. 2025)
+def muon_scale_ref(rows: int, cols: int, mode: int) -> float:
+    if mode == 0:
+        return 1.0
+    if mode == 1:
+        return float(np.sqrt(max(1.0, rows / cols)))
+    if mode == 2:
+        return 0.2 * float(np.sqrt(max(rows, cols)))
+    raise ValueError(mode)
+
+
+def muon_apply_ref(W: np.ndarray, O: np.ndarray, lr: float, wd: float, scale: float) -> np.ndarray:
+    """W*(1 - lr*wd) - lr*scale*O in float64."""
+    return np.asarray(W, np.float64) * (1.0 - lr * wd) - lr * scale * np.asarray(O, np.float64)

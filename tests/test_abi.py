@@ -169,6 +169,27 @@ def test_host_entry_error_paths(mfsdp):
     assert call(ws=G) == mfsdp.ERR_OVERLAP
 
 
+def test_apply_entry_error_paths(mfsdp):
+    lib = mfsdp.raw_lib()
+    ok = [mfsdp.make_shard(0, 256, 512)]
+    arr = (mfsdp.MatrixShard * 1)(*ok)
+    wsb = mfsdp.muon_workspace_bytes(ok)
+    Wt = 0x70000000
+
+    def call(w=Wt, wdt=F32, upd=U, mode=1, ns=5, lr=0.02):
+        return lib.mfsdp_muon_owner_step_apply(arr, 1, G, BF, M, upd, BF, w, wdt, 1 << 20, 0.95, 0, ns, 3.4445,
+                                               -4.775, 2.0315, 1e-7, lr, 0.1, mode, WS, wsb, None)
+    assert call(wdt=5) == mfsdp.ERR_UNSUPPORTED_DTYPE
+    assert call(mode=3) == mfsdp.ERR_INVALID_ARG
+    assert call(ns=0) == mfsdp.ERR_INVALID_ARG
+    assert call(lr=float("nan")) == mfsdp.ERR_INVALID_ARG
+    assert call(w=None) == mfsdp.ERR_INVALID_ARG
+    assert call(w=Wt + 4) == mfsdp.ERR_MISALIGNED
+    assert call(w=G) == mfsdp.ERR_OVERLAP
+    assert call(w=U) == mfsdp.ERR_OVERLAP
+    assert call(w=None, upd=None) == mfsdp.ERR_INVALID_ARG
+
+
 def test_adamw_error_paths(mfsdp):
     lib = mfsdp.raw_lib()
     P, Gp, Mm, V = 0x10000000, 0x20000000, 0x30000000, 0x40000000

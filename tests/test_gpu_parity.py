@@ -293,6 +293,58 @@ def test_host_buffer_pipeline_matches_resident_step(mfsdp, groups):
     assert np.array_equal(mom.cpu().numpy(), m_ref)
 
 
+@pytest.mark.parametrize("wdt", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_apply_update_to_weights(mfsdp, wdt, mode):
+    """W <- W*(1 - lr*wd) - lr*scale*O fused into the last epilogue."""
+    from oracle import muon_apply_ref, muon_scale_ref
+    dev = _dev()
+    w = W.get("gpt2_block")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    grad = H.build_grad_buffer(w, shards, numel)
+    zero = shards[1]                                   # one matrix with zero gradient: weights only decay
+    grad[zero.offset:zero.offset + zero.rows * zero.cols] = 0
+    mom0 = np.zeros(numel, np.float32)
+    u_ref, _, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32)
+    lr, wd = 0.02, 0.1
+    rng = np.random.default_rng(17)
+    W0 = (rng.standard_normal(numel) * 0.02).astype(np.float32)
+    tdt = torch.float32 if wdt == "f32" else torch.bfloat16
+    Wt = torch.from_numpy(W0).to(dev).to(tdt)
+    W0v = from_dev(Wt).astype(np.float64)              # the exact starting weights (bf16-rounded if bf16)
+    g = to_dev_grad(grad)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.full((numel,), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step_apply(shards, g, mom, upd, Wt, ws, lr=lr, weight_decay=wd, scale_mode=mode)
+    torch.cuda.synchronize()
+    O = from_dev(upd)
+    Wn = from_dev(Wt).astype(np.float64)
+    decay = np.float64(np.float32(1.0 - lr * wd))
+    for s in shards:
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        assert np.array_equal(O[seg].view(np.uint32), u_ref[seg].view(np.uint32)), "O must not change"
+        scale = muon_scale_ref(s.rows, s.cols, mode)
+        expect = W0v[seg] * decay - lr * scale * O[seg].astype(np.float64)   # from the GPU's own O
+        tol = (2.0 ** -23 * 4 if wdt == "f32" else 2.0 ** -8) * (np.abs(W0v[seg]) + lr * scale * np.abs(O[seg]))
+        assert np.all(np.abs(Wn[seg] - expect) <= tol + 1e-30), (s.param_id, mode)
+        if s is zero:
+            assert np.all(O[seg] == 0)
+        elif wdt == "f32":
+            G = grad_f64(grad, s)
+            _, O_ref = muon_matrix_ref(G, np.zeros_like(G), w.beta, False, w.ns_steps, A, B, C, W.NS_EPS)
+            W_ref = muon_apply_ref(W0v[seg].reshape(s.rows, s.cols), O_ref, lr, wd, scale)
+            dW = Wn[seg].reshape(s.rows, s.cols) - W0v[seg].reshape(s.rows, s.cols) * decay
+            assert H.rel_fro(dW, W_ref - W0v[seg].reshape(s.rows, s.cols) * decay) <= H.ns_tol(s.rows, s.cols)
+    # without an update buffer the weights come out the same
+    Wt2 = torch.from_numpy(W0).to(dev).to(tdt)
+    mom2 = torch.zeros(numel, dtype=torch.float32, device=dev)
+    mfsdp.muon_owner_step_apply(shards, g, mom2, None, Wt2, ws, lr=lr, weight_decay=wd, scale_mode=mode)
+    torch.cuda.synchronize()
+    assert torch.equal(Wt2.view(torch.int16 if wdt == "bf16" else torch.int32),
+                       Wt.view(torch.int16 if wdt == "bf16" else torch.int32))
+
+
 def test_determinism(mfsdp):
     w = W.get("gpt2_block")
     plan, r, shards, numel = owner_set(mfsdp, w)

@@ -153,3 +153,23 @@ def test_step_one_nesterov_and_heavy_ball_agree_after_normalisation():
     _, O1 = muon_matrix_ref(G, np.zeros_like(G), 0.95, False, 5, A, B, C, 0.0)
     _, O2 = muon_matrix_ref(G, np.zeros_like(G), 0.95, True, 5, A, B, C, 0.0)
     np.testing.assert_allclose(O1, O2, atol=1e-12)
+
+
+def test_apply_scale_forms():
+    from oracle import muon_scale_ref
+    assert muon_scale_ref(4096, 1024, 0) == 1.0
+    assert muon_scale_ref(4096, 1024, 1) == 2.0          # sqrt(4096/1024)
+    assert muon_scale_ref(1024, 4096, 1) == 1.0          # wide matrices are not scaled down
+    assert muon_scale_ref(4096, 1024, 2) == pytest.approx(12.8)   # 0.2 * sqrt(4096)
+    assert muon_scale_ref(100, 2500, 2) == pytest.approx(10.0)    # 0.2 * sqrt(2500)
+
+
+def test_apply_special_cases():
+    from oracle import muon_apply_ref
+    rng = np.random.default_rng(8)
+    W, O = rng.standard_normal((2, 6, 9))
+    np.testing.assert_array_equal(muon_apply_ref(W, O, 0.0, 0.1, 3.0), W)          # lr = 0
+    np.testing.assert_allclose(muon_apply_ref(W, O, 0.02, 0.0, 1.0), W - 0.02 * O, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(muon_apply_ref(W, np.zeros_like(O), 0.02, 0.5, 7.0), 0.99 * W, rtol=1e-15)
+    # one step on W = O with lr*wd = 0 and scale = 1/lr cancels exactly
+    np.testing.assert_allclose(muon_apply_ref(O, O, 0.5, 0.0, 2.0), 0 * O, atol=1e-15)
