@@ -23,3 +23,5 @@ from .planner import plan_owners_ref, lpt_makespan_ref  # noqa: F401
 from .muon import (bf16_bits_to_f64, momentum_ref, newton_schulz_ref,  # noqa: F401
                    muon_owner_step_ref, muon_matrix_ref, muon_scale_ref, muon_apply_ref)
 from .adamw import adamw_ref  # noqa: F401
+from .segments import (model_layout_ref, placement_segments_ref, segment_reduce_ref,  # noqa: F401
+                       segment_gather_ref)
