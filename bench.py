@@ -384,6 +384,34 @@ def run_ours(args):
         sup["adamw_50M"] = {"ms": round(a_ms, 4), "gbs": round(28 * n_big / a_ms / 1e6, 1)}
         del bp, bg, bm, bv
 
+    # ---------------------------------------------------------- supplementary: owner-segment reduce
+    # The reduce that lands every owned matrix on this owner before the step:
+    # w.world simulated ranks' local gradients (bf16, unsharded model layout)
+    # summed in rank order into this rank's flat gradient buffer.  The sources
+    # are left uninitialised; only the time is taken.
+    if rank == 0 and not args.no_supplementary and w.world > 1:
+        model = mfsdp.model_placements(w.param_table(), w.align_elems)
+        _, model_total = mfsdp.model_layout(w.param_table(), w.align_elems)
+        mp, _ = mfsdp.placements(plan)
+        segs = mfsdp.placement_segments(model, mp, sim_rank)
+        srcs = [torch.empty(model_total, dtype=torch.bfloat16, device=dev) for _ in range(w.world)]
+        red_dst = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            mfsdp.segment_copy(srcs, segs, mfsdp.SEGMENT_REDUCE, red_dst)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(reps):
+            mfsdp.segment_copy(srcs, segs, mfsdp.SEGMENT_REDUCE, red_dst)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        r_ms = s0.elapsed_time(s1) / reps
+        moved = sum(g.numel for g in segs) * 2 * (w.world + 1)
+        sup["owner_segment_reduce"] = {"ranks": w.world, "ms": round(r_ms, 4),
+                                       "gbs": round(moved / r_ms / 1e6, 1), "bytes": moved}
+        del srcs, red_dst
+
     # ---------------------------------------------------------- figures
     peaks, peak_src = load_peaks()
     flops, flops_exec = mfsdp.muon_step_flops(shards, w.ns_steps)
@@ -399,6 +427,8 @@ def run_ours(args):
     ns_launches = 3 * w.ns_steps * batches
     if "adamw_50M" in sup:
         sup["adamw_50M"]["frac_hbm"] = round(sup["adamw_50M"]["gbs"] / hbm, 4)
+    if "owner_segment_reduce" in sup:
+        sup["owner_segment_reduce"]["frac_hbm"] = round(sup["owner_segment_reduce"]["gbs"] / hbm, 4)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

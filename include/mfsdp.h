@@ -307,6 +307,67 @@ int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* v, int64_t 
                           double lr, double beta1, double beta2, double eps, double wd,
                           int64_t step, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Owner segments: the reduce that lands each whole matrix on its owner, and
+ * owner-shard resharding (Abstract: "the ordinary backward reduction then
+ * lands the full Muon input on the owner"; "deterministic owner-segment P2P
+ * collectives"; "owner-shard checkpoint resharding").  On one GPU the
+ * data-parallel ranks' buffers are separate flat device buffers.
+ * ------------------------------------------------------------------------ */
+
+/* Where one parameter sits: owner (rank or source-buffer index), element
+ * offset and length in that owner's flat buffer.  A matrix shard maps to
+ * (param_id, owner, offset, rows*cols), a tail shard to itself. */
+typedef struct {
+  int32_t param_id;
+  int32_t owner;
+  int64_t offset;
+  int64_t numel;
+} mfsdp_placement;
+
+/* One contiguous run of elements to move. */
+typedef struct {
+  int64_t src_offset;
+  int64_t dst_offset;
+  int64_t numel;
+  int32_t src_index;   /* GATHER: which source buffer; ignored by REDUCE */
+  int32_t reserved;
+} mfsdp_segment;
+
+#define MFSDP_SEGMENT_REDUCE 0
+#define MFSDP_SEGMENT_GATHER 1
+
+/* Unsharded flat layout of a model's parameters (each rank's local gradient
+ * before the reduce): declaration order, each offset rounded up to
+ * align_elems.  offsets[n_params] out; *total = end rounded up to align_elems.
+ * Host only.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
+int mfsdp_model_layout(const mfsdp_param* params, int32_t n_params, int64_t align_elems,
+                       int64_t* offsets, int64_t* total);
+
+/* Segments that fill dst_owner's buffer of placement `dst` from placement
+ * `src`: for every entry of dst with owner == dst_owner (in dst-offset
+ * order), the entry of src with the same param_id gives src_index (= its
+ * owner) and src_offset.  out has capacity n_dst; *n_out receives the count.
+ * Host only.  Errors: INVALID_ARG (a param missing from src, a param twice in
+ * src, or different lengths). */
+int mfsdp_placement_segments(const mfsdp_placement* src, int32_t n_src, const mfsdp_placement* dst,
+                             int32_t n_dst, int32_t dst_owner, mfsdp_segment* out, int32_t* n_out);
+
+/* Moves the segments into `dst`.
+ *   mode REDUCE: dst[dst_offset+i] = sum over k = 0..n_src-1, in that order,
+ *     of srcs[k][src_offset+i], accumulated in fp32 and rounded once to
+ *     dst_dtype (bitwise reproducible).
+ *   mode GATHER: dst[dst_offset+i] = srcs[src_index][src_offset+i] (converted).
+ * srcs[n_src] (1..64) device buffers of src_numel[k] elements of src_dtype;
+ * dst device, dst_numel elements of dst_dtype; dtypes F32 or BF16; every base
+ * pointer 16-byte aligned.  Segments must stay inside their buffers, must not
+ * overlap each other in dst, and dst must not overlap any source.  Elements of
+ * dst outside the segments are left alone.  Errors: INVALID_ARG, MISALIGNED,
+ * OUT_OF_BOUNDS, OVERLAP, UNSUPPORTED_DTYPE, CUDA_ERROR. */
+int mfsdp_segment_copy(const void* const* srcs, const int64_t* src_numel, int32_t n_src, int32_t src_dtype,
+                       const mfsdp_segment* segs, int32_t n_segs, int32_t mode,
+                       void* dst, int32_t dst_dtype, int64_t dst_numel, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* mfsdp_status_string(int status);
 

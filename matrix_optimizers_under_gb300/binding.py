@@ -39,7 +39,11 @@ PHASE_NEWTON_SCHULZ = 2
 EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner_step", "mfsdp_muon_owner_step_phases",
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
-            "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply")
+            "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
+            "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy")
+
+SEGMENT_REDUCE = 0
+SEGMENT_GATHER = 1
 
 SCALE_NONE = 0      # scale = 1
 SCALE_MUON = 1      # scale = sqrt(max(1, rows/cols))
@@ -167,6 +171,74 @@ def _shard_array(shards: Sequence[MatrixShard]):
     for i, s in enumerate(shards):
         arr[i] = s
     return arr
+
+
+class Placement(ctypes.Structure):
+    _fields_ = [("param_id", ctypes.c_int32), ("owner", ctypes.c_int32), ("offset", ctypes.c_int64),
+                ("numel", ctypes.c_int64)]
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("src_offset", ctypes.c_int64), ("dst_offset", ctypes.c_int64), ("numel", ctypes.c_int64),
+                ("src_index", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return dict(src_index=self.src_index, src_offset=self.src_offset, dst_offset=self.dst_offset,
+                    numel=self.numel)
+
+
+def placements(plan: "Plan") -> Tuple[List[Placement], List[Placement]]:
+    """The plan's matrix shards and tail shards as placements (param, owner, offset, numel)."""
+    def mk(pid, owner, off, n):
+        p = Placement()
+        p.param_id, p.owner, p.offset, p.numel = pid, owner, off, n
+        return p
+    return ([mk(s.param_id, s.owner, s.offset, s.rows * s.cols) for s in plan.matrix_shards],
+            [mk(s.param_id, s.owner, s.offset, s.numel) for s in plan.tail_shards])
+
+
+def model_layout(params: Sequence[Tuple[int, int, int]], align_elems: int = 128) -> Tuple[List[int], int]:
+    """Offsets of the parameters in the unsharded flat layout, and its extent."""
+    n = len(params)
+    arr = (CParam * max(n, 1))()
+    for i, (r, c, k) in enumerate(params):
+        arr[i].rows, arr[i].cols, arr[i].kind = int(r), int(c), int(k)
+    offs = (ctypes.c_int64 * max(n, 1))()
+    total = ctypes.c_int64(0)
+    _check(_lib.mfsdp_model_layout(arr, n, int(align_elems), offs, ctypes.byref(total)), "model_layout")
+    return list(offs[:n]), int(total.value)
+
+
+def model_placements(params: Sequence[Tuple[int, int, int]], align_elems: int = 128) -> List[Placement]:
+    """Every parameter in the unsharded layout, as placements with owner 0."""
+    offs, _ = model_layout(params, align_elems)
+    out = []
+    for i, (r, c, _) in enumerate(params):
+        p = Placement()
+        p.param_id, p.owner, p.offset, p.numel = i, 0, offs[i], r * c
+        out.append(p)
+    return out
+
+
+def placement_segments(src: Sequence[Placement], dst: Sequence[Placement], dst_owner: int) -> List[Segment]:
+    """Segments that fill dst_owner's buffer of `dst` from `src` (see include/mfsdp.h)."""
+    a = (Placement * max(len(src), 1))(*src)
+    b = (Placement * max(len(dst), 1))(*dst)
+    out = (Segment * max(len(dst), 1))()
+    n = ctypes.c_int32(0)
+    _check(_lib.mfsdp_placement_segments(a, len(src), b, len(dst), int(dst_owner), out, ctypes.byref(n)),
+           "placement_segments")
+    return [out[i] for i in range(n.value)]
+
+
+def segment_copy(srcs, segs: Sequence[Segment], mode: int, dst, stream=None) -> None:
+    """REDUCE (sum of all sources in order) or GATHER the segments into dst."""
+    n = len(srcs)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in srcs])
+    sizes = (ctypes.c_int64 * max(n, 1))(*[int(t.numel()) for t in srcs])
+    arr = (Segment * max(len(segs), 1))(*segs)
+    _check(_lib.mfsdp_segment_copy(ptrs, sizes, n, _dtype_code(srcs[0]), arr, len(segs), int(mode), _ptr(dst),
+                                   _dtype_code(dst), int(dst.numel()), _stream(stream)), "segment_copy")
 
 
 def make_shard(offset: int, rows: int, cols: int, param_id: int = 0, owner: int = 0) -> MatrixShard:
@@ -306,6 +378,16 @@ def adamw_tail_step(p, g, m, v, *, lr: float, beta1: float, beta2: float, eps: f
     n = int(p.numel())
     _check(_lib.mfsdp_adamw_tail_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), n, float(lr), float(beta1), float(beta2),
                                       float(eps), float(wd), int(step), _stream(stream)), "adamw_tail_step")
+
+
+_lib.mfsdp_model_layout.argtypes = [ctypes.POINTER(CParam), _i32, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+_lib.mfsdp_model_layout.restype = ctypes.c_int
+_lib.mfsdp_placement_segments.argtypes = [ctypes.POINTER(Placement), _i32, ctypes.POINTER(Placement), _i32, _i32,
+                                          ctypes.POINTER(Segment), ctypes.POINTER(_i32)]
+_lib.mfsdp_placement_segments.restype = ctypes.c_int
+_lib.mfsdp_segment_copy.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(_i64), _i32, _i32,
+                                    ctypes.POINTER(Segment), _i32, _i32, _vp, _i32, _i64, _vp]
+_lib.mfsdp_segment_copy.restype = ctypes.c_int
 
 
 def raw_lib() -> ctypes.CDLL:

@@ -654,3 +654,123 @@ extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* 
   k.eps = (float)eps;
   return cuda_status(launch_adamw(p, g, m, v, n, k, static_cast<cudaStream_t>(stream_ptr)));
 }
+
+// ------------------------------------------------------------------ owner segments
+extern "C" int mfsdp_model_layout(const mfsdp_param* params, int32_t n_params, int64_t align_elems, int64_t* offsets,
+                                  int64_t* total) {
+  if (n_params < 0 || align_elems < 1 || !total || (n_params > 0 && (!params || !offsets)))
+    return MFSDP_ERR_INVALID_ARG;
+  int64_t off = 0;
+  for (int i = 0; i < n_params; ++i) {
+    if (params[i].rows < 1 || params[i].cols < 1 || params[i].rows > INT64_MAX / params[i].cols)
+      return MFSDP_ERR_UNSUPPORTED_SHAPE;
+    off = (off + align_elems - 1) / align_elems * align_elems;
+    offsets[i] = off;
+    off += params[i].rows * params[i].cols;
+  }
+  *total = (off + align_elems - 1) / align_elems * align_elems;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_placement_segments(const mfsdp_placement* src, int32_t n_src, const mfsdp_placement* dst,
+                                        int32_t n_dst, int32_t dst_owner, mfsdp_segment* out, int32_t* n_out) {
+  if (n_src < 0 || n_dst < 0 || !n_out || (n_src > 0 && !src) || (n_dst > 0 && (!dst || !out)))
+    return MFSDP_ERR_INVALID_ARG;
+  std::vector<int> by_param;
+  for (int i = 0; i < n_src; ++i) {
+    const int pid = src[i].param_id;
+    if (pid < 0 || src[i].numel < 0 || src[i].offset < 0) return MFSDP_ERR_INVALID_ARG;
+    if ((int)by_param.size() <= pid) by_param.resize(pid + 1, -1);
+    if (by_param[pid] >= 0) return MFSDP_ERR_INVALID_ARG;   // a parameter placed twice
+    by_param[pid] = i;
+  }
+  std::vector<int> mine;
+  for (int i = 0; i < n_dst; ++i)
+    if (dst[i].owner == dst_owner) mine.push_back(i);
+  std::sort(mine.begin(), mine.end(), [&](int x, int y) { return dst[x].offset < dst[y].offset; });
+  int k = 0;
+  for (int i : mine) {
+    const int pid = dst[i].param_id;
+    if (pid < 0 || pid >= (int)by_param.size() || by_param[pid] < 0) return MFSDP_ERR_INVALID_ARG;
+    const mfsdp_placement& f = src[by_param[pid]];
+    if (f.numel != dst[i].numel) return MFSDP_ERR_INVALID_ARG;
+    mfsdp_segment& g = out[k++];
+    std::memset(&g, 0, sizeof(g));
+    g.src_offset = f.offset;
+    g.dst_offset = dst[i].offset;
+    g.numel = f.numel;
+    g.src_index = f.owner;
+  }
+  *n_out = k;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_segment_copy(const void* const* srcs, const int64_t* src_numel, int32_t n_src, int32_t src_dtype,
+                                  const mfsdp_segment* segs, int32_t n_segs, int32_t mode, void* dst,
+                                  int32_t dst_dtype, int64_t dst_numel, void* stream_ptr) {
+  if (n_src < 1 || n_src > kMaxSources || !srcs || !src_numel || n_segs < 0 || (n_segs > 0 && !segs) ||
+      (mode != MFSDP_SEGMENT_REDUCE && mode != MFSDP_SEGMENT_GATHER) || dst_numel < 0)
+    return MFSDP_ERR_INVALID_ARG;
+  if ((src_dtype != MFSDP_DTYPE_F32 && src_dtype != MFSDP_DTYPE_BF16) ||
+      (dst_dtype != MFSDP_DTYPE_F32 && dst_dtype != MFSDP_DTYPE_BF16))
+    return MFSDP_ERR_UNSUPPORTED_DTYPE;
+  if (n_segs == 0) return MFSDP_OK;
+  if (!dst) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(dst, 16)) return MFSDP_ERR_MISALIGNED;
+  for (int k = 0; k < n_src; ++k) {
+    if (!srcs[k] || src_numel[k] < 0) return MFSDP_ERR_INVALID_ARG;
+    if (!aligned(srcs[k], 16)) return MFSDP_ERR_MISALIGNED;
+    if (ranges_overlap(dst, (size_t)dst_numel * dtype_size(dst_dtype), srcs[k],
+                       (size_t)src_numel[k] * dtype_size(src_dtype)))
+      return MFSDP_ERR_OVERLAP;
+  }
+  int64_t min_src = INT64_MAX;
+  for (int k = 0; k < n_src; ++k) min_src = std::min(min_src, src_numel[k]);
+  for (int i = 0; i < n_segs; ++i) {
+    const mfsdp_segment& g = segs[i];
+    if (g.numel < 0 || g.src_offset < 0 || g.dst_offset < 0) return MFSDP_ERR_INVALID_ARG;
+    if (mode == MFSDP_SEGMENT_GATHER && (g.src_index < 0 || g.src_index >= n_src)) return MFSDP_ERR_INVALID_ARG;
+    const int64_t lim = mode == MFSDP_SEGMENT_GATHER ? src_numel[g.src_index] : min_src;
+    if (g.src_offset > lim || g.numel > lim - g.src_offset) return MFSDP_ERR_OUT_OF_BOUNDS;
+    if (g.dst_offset > dst_numel || g.numel > dst_numel - g.dst_offset) return MFSDP_ERR_OUT_OF_BOUNDS;
+  }
+  {
+    std::vector<int> ord(n_segs);
+    for (int i = 0; i < n_segs; ++i) ord[i] = i;
+    std::sort(ord.begin(), ord.end(), [&](int x, int y) { return segs[x].dst_offset < segs[y].dst_offset; });
+    for (int k = 1; k < n_segs; ++k)
+      if (segs[ord[k - 1]].dst_offset + segs[ord[k - 1]].numel > segs[ord[k]].dst_offset) return MFSDP_ERR_OVERLAP;
+  }
+  // Chunk counts (2048 elements per CTA) must fit a launch grid.
+  int64_t all_chunks = 0;
+  for (int i = 0; i < n_segs; ++i) all_chunks += (segs[i].numel + kSegChunk - 1) / kSegChunk;
+  if (all_chunks > (int64_t)INT32_MAX / 2) return MFSDP_ERR_UNSUPPORTED_SHAPE;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  for (int base = 0; base < n_segs; base += kMaxSegBatch) {
+    const int cnt = std::min(kMaxSegBatch, n_segs - base);
+    SegBatch b;
+    std::memset(&b, 0, sizeof(b));
+    b.n = cnt;
+    b.mode = mode;
+    b.n_src = n_src;
+    b.src_bf16 = src_dtype == MFSDP_DTYPE_BF16;
+    b.dst_bf16 = dst_dtype == MFSDP_DTYPE_BF16;
+    b.dst = dst;
+    for (int k = 0; k < n_src; ++k) b.src[k] = srcs[k];
+    int64_t chunks = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const mfsdp_segment& g = segs[base + i];
+      b.seg[i].src_offset = g.src_offset;
+      b.seg[i].dst_offset = g.dst_offset;
+      b.seg[i].numel = g.numel;
+      b.seg[i].src_index = g.src_index;
+      b.chunk_start[i] = (int32_t)chunks;
+      chunks += (g.numel + kSegChunk - 1) / kSegChunk;
+    }
+    b.chunk_start[cnt] = (int32_t)chunks;
+    const int st = cuda_status(launch_segments(b, (int)chunks, stream));
+    if (st != MFSDP_OK) return st;
+  }
+  return MFSDP_OK;
+}

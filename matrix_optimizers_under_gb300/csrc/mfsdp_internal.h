@@ -130,6 +130,28 @@ struct EmitBatch {
   EmitMat mat[kMaxBatch];
 };
 
+// ------------------------------------------- owner segments (reduce / gather)
+constexpr int kMaxSegBatch = 256;  // segments per launch
+constexpr int kMaxSources = 64;    // source buffers (simulated ranks)
+constexpr int kSegChunk = 2048;    // elements per CTA (256 threads x 8)
+struct SegDesc {
+  int64_t src_offset, dst_offset, numel;
+  int32_t src_index;
+  int32_t pad;
+};
+struct SegBatch {
+  int32_t n;
+  int32_t mode;          // 0: reduce over all sources in order; 1: gather from src[src_index]
+  int32_t n_src;
+  int32_t src_bf16;
+  int32_t dst_bf16;
+  int32_t pad;
+  void* dst;
+  const void* src[kMaxSources];
+  int32_t chunk_start[kMaxSegBatch + 1];
+  SegDesc seg[kMaxSegBatch];
+};
+
 // Status word bits written by kernels that give up on a bounded wait.
 constexpr int32_t kStatusTimeout = 1;
 
@@ -137,6 +159,7 @@ cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
 cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s);
+cudaError_t launch_segments(const SegBatch& b, int total_chunks, cudaStream_t s);
 // fp32 scalars of one AdamW step, formed in double on the host.
 struct AdamScalars {
   float decay;         // 1 - lr*wd
