@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # mean over one owner step's 15 launches, from the ncu capture summarised in
 # profiles/launches_llama3_8b_rank.md; keyed by the library version it was taken on, so
 # that a changed kernel reports null until it is captured again.
-NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9}
+NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9}
 
 
 # --------------------------------------------------------------------------- helpers
