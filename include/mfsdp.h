@@ -119,7 +119,8 @@ int mfsdp_plan_owners(const mfsdp_param* params, int32_t n_params, int32_t world
 /* Bytes of device workspace mfsdp_muon_owner_step needs for these shards
  * (0 on invalid input).  Holds, per matrix, X (two bf16 ping-pong copies of
  * the s x l iterate) and the s x s bf16 matrices A = X X^T and B = bA + cA^2,
- * each padded to multiples of 128, plus norm partials and a status word. */
+ * each padded to multiples of 128 (the short side to 256), plus norm
+ * partials, the Newton-Schulz tile and completion counters and a status word. */
 size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards);
 
 /* Owner-local Muon step over one rank's owned matrices (Abstract: the reduced
@@ -281,8 +282,16 @@ int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, in
 /* Reads the device status word a previous mfsdp_muon_owner_step left in
  * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
  * if one of its kernels gave up on a bounded wait (its outputs are then
- * undefined).  *detail (may be NULL) receives the raw word: bits 0-7 the
- * waiting role, bits 8-31 the pipeline stage. */
+ * undefined).  Every wait of the Newton-Schulz kernel gives up after 2 s; the
+ * first one to do so records the word and every other CTA then stops too.
+ * *detail (may be NULL) receives the raw word: bits 0-7 the waiting role
+ * (1 producer: a free pipeline stage; 2 MMA issuer: a stage's operands;
+ * 3 MMA issuer: a drained accumulator; 4 epilogue: a finished accumulator;
+ * 5 scheduler: the earlier products of a tile's matrix; 7 scheduler: a free
+ * slot of a tile ring; 8 any role: the next tile), bits 8-31 the
+ * Newton-Schulz product index (3 * iteration + 0 Gram / 1 polynomial /
+ * 2 update) where the role knows it, else 0.  The status word is cleared by
+ * every call that runs the momentum phase. */
 int mfsdp_muon_device_status(const void* workspace, void* stream, int32_t* detail);
 
 /* Layout of the workspace, for inspection: for shard i, out[8*i + 0..7] =

@@ -9,10 +9,11 @@
 // Launch sequence of mfsdp_muon_owner_step on one stream:
 //   momentum/segment-view kernel (grouped over all shards)
 //   norm finalise
-//   ns_steps x { Gram, polynomial, update }   (each one grouped launch)
+//   ns_steps x { Gram, polynomial, update }   (one persistent launch)
 // Grouped launches carry their per-matrix table as a kernel parameter, at most
 // kMaxBatch matrices per launch.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -38,6 +39,7 @@ struct MatLayout {
 struct Layout {
   std::vector<MatLayout> mats;
   size_t norm_off = 0;
+  size_t done_off = 0;     // Newton-Schulz tile counter, then one completion counter per matrix
   size_t partial_off = 0;
   int partials = 0;
   size_t bytes = 0;
@@ -70,6 +72,8 @@ int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
   size_t off = kHeaderBytes;
   L->norm_off = off;
   off = round_up(off + sizeof(float2) * (size_t)n, 256);
+  L->done_off = off;
+  off = round_up(off + sizeof(int32_t) * (size_t)(n + 1), 256);
   L->partial_off = off;
   L->partials = partials * kPartialsPerTile;
   off = round_up(off + sizeof(float) * (size_t)L->partials, 1024);
@@ -96,6 +100,11 @@ bool ranges_overlap(const void* p, size_t pb, const void* q, size_t qb) {
 size_t dtype_size(int32_t dt) { return dt == MFSDP_DTYPE_BF16 ? 2 : 4; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_CUDA; }
+
+// The workspace header holds the device status word; an entry point clears it
+// once, before its first kernel, so a failure anywhere in the call stays
+// visible to mfsdp_muon_device_status.
+int clear_status(uint8_t* ws, cudaStream_t stream) { return cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream)); }
 
 // Output tiling of one product of one matrix, in tiles of the 256 rows a CTA
 // pair computes together.  The Gram and polynomial outputs are symmetric: only
@@ -131,6 +140,25 @@ uint64_t executed_flops(int mode, int s_pad, int l_pad) {
   if (mode == kGram) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)l_pad;
   if (mode == kPoly) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)s_pad;
   return 2ull * s_pad * s_pad * (uint64_t)l_pad;
+}
+
+// The Newton-Schulz launch indexes its tiles and counts completions in int32:
+// a batch's tiles over all iterations, and one matrix's completion count
+// (2 * kEpilogueWarps per tile), must fit.
+bool ns_counts_fit(const Layout& L, int32_t ns_steps) {
+  const int n = (int)L.mats.size();
+  for (int base = 0; base < n; base += kMaxBatch) {
+    int64_t batch = 0;
+    for (int i = base; i < std::min(n, base + kMaxBatch); ++i) {
+      const MatLayout& m = L.mats[i];
+      const int64_t per_iter = 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad).tiles +
+                               gemm_tiling(kUpdate, m.s_pad, m.l_pad).tiles;
+      if (per_iter * ns_steps * 2 * kEpilogueWarps > INT32_MAX) return false;
+      batch += per_iter;
+    }
+    if (batch * ns_steps > INT32_MAX - 65536) return false;   // headroom: pairs overshoot the tile counter
+  }
+  return true;
 }
 
 int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
@@ -175,7 +203,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.6.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.7.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -218,6 +246,7 @@ int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void
     return MFSDP_ERR_MISALIGNED;
   const int st = make_layout(shards, n_shards, L);
   if (st != MFSDP_OK) return st;
+  if (!ns_counts_fit(*L, ns_steps)) return MFSDP_ERR_UNSUPPORTED_SHAPE;
   for (int i = 0; i < n_shards; ++i) {
     const mfsdp_matrix_shard& sh = shards[i];
     if (sh.offset < 0 || sh.offset > numel || sh.rows * sh.cols > numel - sh.offset) return MFSDP_ERR_OUT_OF_BOUNDS;
@@ -261,6 +290,8 @@ extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, in
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (phases & MFSDP_PHASE_MOMENTUM) {
+    st = clear_status(ws, stream);
+    if (st != MFSDP_OK) return st;
     st = launch_momentum_phase(shards, n_shards, L, grad, grad_dtype, momentum, beta, nesterov, eps, ws, stream);
     if (st != MFSDP_OK) return st;
   }
@@ -299,6 +330,8 @@ extern "C" int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int
   const float fb = (float)beta, fe = (float)eps;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  st = clear_status(ws, stream);
+  if (st != MFSDP_OK) return st;
   st = launch_momentum_phase(shards, n_shards, L, grad, grad_dtype, momentum, fb, nesterov, fe, ws, stream);
   if (st != MFSDP_OK) return st;
   ApplyArgs ap{weights, weight_dtype, lr, weight_decay, scale_mode};
@@ -367,6 +400,10 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
     }
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (clear_status(ws, stream) != MFSDP_OK) {
+    cleanup();
+    return MFSDP_ERR_CUDA;
+  }
   cudaError_t ce = cudaEventRecord(ev[0], stream);            // earlier work on `stream` comes first
   ce = ce == cudaSuccess ? cudaStreamWaitEvent(s_in, ev[0], 0) : ce;
   for (int g = 0; g < ng && ce == cudaSuccess && st == MFSDP_OK; ++g) {
@@ -425,8 +462,7 @@ int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const 
   float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
   float* partials = reinterpret_cast<float*>(ws + L.partial_off);
   const size_t gsz = dtype_size(grad_dtype);
-  int st = cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
-  if (st != MFSDP_OK) return st;
+  int st = MFSDP_OK;
   for (int base = 0; base < n_shards; base += kMaxBatch) {
     const int cnt = std::min(kMaxBatch, n_shards - base);
     MomBatch mb;
@@ -516,80 +552,81 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
   }
 
   // ------------------------------------------------------- Newton-Schulz
-  for (int it = 0; it < ns_steps; ++it) {
-    const bool last = (it == ns_steps - 1);
-    for (int mode = kGram; mode <= kUpdate; ++mode) {
-      const int eff_mode = (mode == kUpdate && last) ? kUpdateFinal : mode;
-      for (int base = 0; base < n_shards; base += kMaxBatch) {
-        const int cnt = std::min(kMaxBatch, n_shards - base);
-        GemmBatch gb;
-        std::memset(&gb, 0, sizeof(gb));
-        gb.n = cnt;
-        gb.mode = eff_mode;
-        gb.first_iter = it == 0;
-        gb.out_bf16 = update_dtype == MFSDP_DTYPE_BF16;
-        gb.a = a;
-        gb.b = b;
-        gb.c = c;
-        gb.norm = norm;
-        gb.status = status;
-        if (apply) {
-          gb.decay = (float)(1.0 - apply->lr * apply->wd);
-          gb.w_bf16 = apply->w_dtype == MFSDP_DTYPE_BF16;
-        }
-        // Longest K first: the persistent CTAs take tiles round-robin, so the
-        // last rounds hold the cheapest tiles.
-        std::vector<int> order(cnt);
-        for (int k = 0; k < cnt; ++k) order[k] = base + k;
-        auto kb_of = [&](int i) { return mode == kGram ? L.mats[i].l_pad : L.mats[i].s_pad; };
-        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return kb_of(x) > kb_of(y); });
-        int tiles = 0;
-        for (int k = 0; k < cnt; ++k) {
-          const int i = order[k];
-          const MatLayout& m = L.mats[i];
-          uint8_t* xc = ws + ((it & 1) ? m.x1 : m.x0);   // current iterate
-          uint8_t* xn = ws + ((it & 1) ? m.x0 : m.x1);   // next iterate
-          GemmMat& d = gb.mat[k];
-          d.s_pad = m.s_pad;
-          d.l_pad = m.l_pad;
-          d.s = m.s;
-          d.l = m.l;
-          d.norm_idx = i;
-          d.transposed = m.transposed;
-          d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
-          const GemmTiling tg = gemm_tiling(mode, m.s_pad, m.l_pad);
-          d.tiles_m = tg.tiles_m;
-          d.tiles_n = tg.tiles_n;
-          d.n_last = tg.n_last;
-          d.symmetric = tg.symmetric;
-          if (mode == kGram) {
-            d.a_op = xc; d.b_op = xc; d.c_in = nullptr; d.out = ws + m.a;
-            d.k_blocks = m.l_pad / kBlockK;
-          } else if (mode == kPoly) {
-            d.a_op = ws + m.a; d.b_op = ws + m.a; d.c_in = ws + m.a; d.out = ws + m.b;
-            d.k_blocks = m.s_pad / kBlockK;
-          } else {
-            d.a_op = ws + m.b; d.b_op = xc; d.c_in = xc;
-            if (!last) {
-              d.out = xn;
-            } else {
-              d.out = update ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz)
-                             : nullptr;
-              if (apply) {
-                d.w = static_cast<uint8_t*>(apply->w) + (size_t)shards[i].offset * dtype_size(apply->w_dtype);
-                d.lr_scale = (float)(apply->lr * shape_scale(shards[i].rows, shards[i].cols, apply->scale_mode));
-              }
-            }
-            d.k_blocks = m.s_pad / kBlockK;
-          }
-          gb.tile_start[k] = tiles;
-          tiles += tg.tiles;
-        }
-        gb.tile_start[cnt] = tiles;
-        st = cuda_status(launch_ns_gemm(gb, tiles, stream));
-        if (st != MFSDP_OK) return st;
-      }
+  // One persistent launch per batch runs all 3 * ns_steps products; its tile
+  // counter and completion counters start at zero.
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + L.done_off);
+  for (int base = 0; base < n_shards; base += kMaxBatch) {
+    const int cnt = std::min(kMaxBatch, n_shards - base);
+    NsBatch nb;
+    std::memset(&nb, 0, sizeof(nb));
+    nb.n = cnt;
+    nb.ns_steps = ns_steps;
+    nb.phase_begin = 0;
+    nb.phase_end = 3 * ns_steps;
+    nb.out_bf16 = update_dtype == MFSDP_DTYPE_BF16;
+    nb.a = a;
+    nb.b = b;
+    nb.c = c;
+    nb.norm = norm;
+    nb.status = status;
+    nb.next_tile = counters;
+    nb.done = counters + 1 + base;
+    if (apply) {
+      nb.decay = (float)(1.0 - apply->lr * apply->wd);
+      nb.w_bf16 = apply->w_dtype == MFSDP_DTYPE_BF16;
     }
+    for (int k = 0; k < cnt; ++k) {
+      const int i = base + k;
+      const MatLayout& m = L.mats[i];
+      NsMat& d = nb.mat[k];
+      d.x[0] = ws + m.x0;
+      d.x[1] = ws + m.x1;
+      d.a = ws + m.a;
+      d.b = ws + m.b;
+      d.out = update ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz) : nullptr;
+      if (apply) {
+        d.w = static_cast<uint8_t*>(apply->w) + (size_t)shards[i].offset * dtype_size(apply->w_dtype);
+        d.lr_scale = (float)(apply->lr * shape_scale(shards[i].rows, shards[i].cols, apply->scale_mode));
+      }
+      d.s_pad = m.s_pad;
+      d.l_pad = m.l_pad;
+      d.s = m.s;
+      d.l = m.l;
+      const GemmTiling ts = gemm_tiling(kGram, m.s_pad, m.l_pad), tu = gemm_tiling(kUpdate, m.s_pad, m.l_pad);
+      d.tiles_sym = ts.tiles;
+      d.tiles_m = tu.tiles_m;
+      d.tiles_n = tu.tiles_n;
+      d.n_last = tu.n_last;
+      d.norm_idx = i;
+      d.transposed = m.transposed;
+      d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
+    }
+    // Inside each product, longest K first: the persistent pairs take tiles
+    // round-robin, so the last rounds hold the cheapest tiles.
+    int32_t off = 0;
+    for (int prod = kGram; prod <= kUpdate; ++prod) {
+      std::vector<int> order(cnt);
+      for (int k = 0; k < cnt; ++k) order[k] = k;
+      auto kb_of = [&](int k) { return prod == kGram ? nb.mat[k].l_pad : nb.mat[k].s_pad; };
+      std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return kb_of(x) > kb_of(y); });
+      nb.mode_start[prod] = off;
+      int32_t tiles = 0;
+      for (int j = 0; j < cnt; ++j) {
+        const NsMat& d = nb.mat[order[j]];
+        nb.order[prod][j] = (uint8_t)order[j];
+        nb.tile_start[prod][j] = tiles;
+        tiles += prod == kUpdate ? d.tiles_m * d.tiles_n : d.tiles_sym;
+      }
+      nb.tile_start[prod][cnt] = tiles;
+      off += tiles;
+    }
+    nb.iter_tiles = off;
+    nb.tile_begin = 0;
+    nb.tile_end = off * ns_steps;
+    st = cuda_status(cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(n_shards + 1), stream));
+    if (st != MFSDP_OK) return st;
+    st = cuda_status(launch_ns(nb, stream));
+    if (st != MFSDP_OK) return st;
   }
   return MFSDP_OK;
 }

@@ -25,7 +25,8 @@ constexpr int kStageBytesA = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBytesB = kBlockN * kBlockK * 2;   // 32 KB
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kEpilogueWarps = 8;  // warps 2-9 of the GEMM CTA: two per TMEM lane quadrant
-constexpr int kGemmThreads = 64 + 32 * kEpilogueWarps;   // producer warp, MMA warp, epilogue warps
+constexpr int kSchedulerWarp = 2 + kEpilogueWarps;        // warp 10: hands out ready tiles
+constexpr int kGemmThreads = 32 * (kSchedulerWarp + 1);   // producer, MMA, epilogue warps, scheduler
 constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
 
 // Bytes between consecutive 64-column blocks of a blocked matrix with rows_pad rows.
@@ -81,38 +82,55 @@ enum GemmMode : int32_t {
   kUpdateFinal = 3,  // same, written to the caller's update buffer
 };
 
-struct GemmMat {
-  const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
-  const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
-  const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly, X for kUpdate*)
-  void* out;             // blocked bf16 output, or the caller's buffer at the shard offset (may be null)
-  void* w;               // kUpdateFinal with apply: the weights at the shard offset, else null
+// One matrix of a Newton-Schulz launch: its workspace buffers and the tiling
+// of its three products.
+struct NsMat {
+  uint8_t* x[2];         // blocked bf16 iterates (s_pad x l_pad): iteration i reads x[i & 1], writes x[(i + 1) & 1]
+  uint8_t* a;            // blocked bf16 A = X X^T (s_pad x s_pad)
+  uint8_t* b;            // blocked bf16 B = b A + c A A
+  void* out;             // the caller's update at the shard offset (may be null)
+  void* w;               // apply: the weights at the shard offset, else null
   int32_t s_pad, l_pad;
   int32_t s, l;          // true short / long side
-  int32_t tiles_m, tiles_n;
-  int32_t k_blocks;      // K / kBlockK
-  int32_t n_last;        // width of the last column tile (128 or 256); unused when symmetric
+  int32_t tiles_sym;     // Gram / polynomial: 256 x 256 pair tiles on or above the diagonal
+  int32_t tiles_m, tiles_n;   // update: 256-row x 256-column pair tiles
+  int32_t n_last;        // update: width of the last column tile (128 or 256)
   int32_t norm_idx;      // index into the norm table
-  int32_t transposed;    // kUpdateFinal: stored matrix is l x s
-  int32_t vec_ok;        // kUpdateFinal: row-major stores may use 16-byte vectors
-  int32_t symmetric;     // kGram / kPoly: upper-triangle tiles only, mirrored on store
+  int32_t transposed;    // final update: stored matrix is l x s
+  int32_t vec_ok;        // final update: row-major stores may use 16-byte vectors
   float lr_scale;        // apply: lr * shape scale of this matrix
-  int32_t pad;
 };
-struct GemmBatch {
+
+// One launch runs the products [phase_begin, phase_end) of the sequence
+//   for it in 0 .. ns_steps-1: Gram (3 it), polynomial (3 it + 1), update (3 it + 2)
+// over up to kMaxBatch matrices.  Its tiles form one list, product-major
+// (tile_begin .. tile_end-1 of the whole sequence's list), handed out in list
+// order to whichever CTA pair asks next.  Inside product k of
+// an iteration, matrix order[k][j] holds tiles [tile_start[k][j],
+// tile_start[k][j+1]) after mode_start[k].  A tile may start once every tile
+// of the earlier products of its matrix in this launch has been stored:
+// done[matrix] counts the epilogue warps that finished one.
+struct NsBatch {
   int32_t n;
-  int32_t mode;
-  int32_t first_iter;    // fold the 1/(||U||+eps) prescale into this launch
-  int32_t out_bf16;      // kUpdateFinal: output dtype
+  int32_t ns_steps;
+  int32_t phase_begin, phase_end;
+  int32_t tile_begin, tile_end;
+  int32_t iter_tiles;    // tiles of one iteration (three products, all matrices)
+  int32_t mode_start[3];
+  int32_t out_bf16;      // final update dtype
+  int32_t w_bf16;        // apply: weight dtype
   float a, b, c;
   float decay;           // apply: 1 - lr * weight_decay
-  int32_t w_bf16;        // apply: weight dtype
-  int32_t pad;
   const float2* norm;
-  int32_t* status;       // device status word (timeouts)
-  int32_t tile_start[kMaxBatch + 1];
-  GemmMat mat[kMaxBatch];
+  int32_t* status;       // device status word (first wait that gave up)
+  int32_t* next_tile;    // tiles handed out so far (dynamic schedule), zeroed before the launch
+  int32_t* done;         // per matrix of the launch, zeroed before it
+  int32_t tile_start[3][kMaxBatch + 1];
+  uint8_t order[3][kMaxBatch];
+  NsMat mat[kMaxBatch];
 };
+static_assert(kMaxBatch <= 256, "matrix order is stored in bytes");
+static_assert(sizeof(NsBatch) < 32000, "kernel parameter limit");
 
 // ------------------------------------------------------------ emit (T = 0)
 struct EmitMat {
@@ -152,13 +170,22 @@ struct SegBatch {
   SegDesc seg[kMaxSegBatch];
 };
 
-// Status word bits written by kernels that give up on a bounded wait.
-constexpr int32_t kStatusTimeout = 1;
+// Status word written by a kernel that gives up on a bounded wait: the first
+// one records (product index << 8) | role, role one of these.
+enum WaitRole : int32_t {
+  kRoleStageFree = 1,   // producer: a pipeline stage to refill
+  kRoleStageFull = 2,   // MMA issuer: a stage's operands
+  kRoleAccFree = 3,     // MMA issuer: an accumulator the epilogue has drained
+  kRoleAccFull = 4,     // epilogue: a finished accumulator
+  kRoleDependency = 5,  // scheduler: earlier products of the tile's matrix
+  kRoleTileFree = 7,    // scheduler: a ring slot every reader has taken
+  kRoleTileFull = 8,    // producer, MMA issuer, epilogue: the next tile index
+};
 
 cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
 cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
-cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s);
+cudaError_t launch_ns(const NsBatch& b, cudaStream_t s);
 cudaError_t launch_segments(const SegBatch& b, int total_chunks, cudaStream_t s);
 // fp32 scalars of one AdamW step, formed in double on the host.
 struct AdamScalars {

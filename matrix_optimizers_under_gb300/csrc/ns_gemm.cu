@@ -1,5 +1,5 @@
-// Newton-Schulz products on 5th-generation tensor cores (tcgen05 / TMEM),
-// grouped over every matrix of an owner set in one launch per product.
+// Newton-Schulz products on 5th-generation tensor cores (tcgen05 / TMEM): every
+// product of every iteration, for every matrix of an owner set, in one launch.
 //
 // MatrixFSDP: Communication-Free Matrix Optimizers Under ZeRO-3 Parameter
 // Sharding -- Abstract: Muon orthogonalises each owned matrix with
@@ -25,8 +25,26 @@
 // stored X serves as the K-major operand of the Gram product and the MN-major
 // operand of the update.
 //
-// Persistent, warp-specialised CTAs (one per SM) walk the launch's tile list
-// round-robin.  Warp 0 (one lane) streams K in 64-element stages through a
+// One launch runs every product of every iteration for up to kMaxBatch
+// matrices.  Its tiles form one product-major list (all Gram tiles of
+// iteration 0, then all polynomial tiles, ...).  Persistent CTA pairs (one CTA
+// per SM) take tiles from it in list order through a global counter, so the
+// tiles in flight are always a contiguous window of the list, which keeps the
+// operands the pairs share in L2.  A tile may start only once the earlier
+// products of its own matrix are stored: each epilogue warp that stores its
+// share of a tile adds one to the matrix's completion counter (release).  In
+// each pair a scheduler warp of the even CTA takes the next index, waits
+// (acquire) until the counter of its matrix covers every tile of the earlier
+// products, and hands the tile to the odd CTA's scheduler (a remote store and
+// mbarrier arrive); each scheduler passes it to its own CTA's roles through a
+// small ring in shared memory.  It runs a few tiles ahead, so taking a tile
+// costs the pipeline nothing while work is ready.  Small matrices run ahead
+// through their iterations while large ones fill the machine, with no launch
+// gap or tail between products.  Every dependency points to an earlier
+// position of the list and tiles are taken in list order, so the lowest
+// unfinished tile belongs to a running pair and can always proceed.
+//
+// Inside a CTA, warp 0 (one lane) streams K in 64-element stages through a
 // 4-deep mbarrier ring of 48 KB stages; warp 1 (one lane) issues 128 x N x 16
 // UMMAs into one of two 256-column TMEM accumulators; warps 2-9 drain the other
 // accumulator (tcgen05.ld; two warps per TMEM lane quadrant, each taking half
@@ -34,8 +52,9 @@
 // polynomial epilogue in fp32 and store bf16 -- or, on the last iteration, the
 // update in the caller's dtype and layout, transposed back for tall matrices.
 // So one tile's epilogue runs under the next tile's main loop.  Every wait is
-// bounded: on expiry the CTA records kStatusTimeout, stops, drains what it
-// issued, frees TMEM and returns.
+// bounded: on expiry the CTA records which wait gave up in the status word,
+// every other CTA sees the word and stops too, and each drains what it issued,
+// frees TMEM and returns.
 //
 // Bounds of every bulk copy (all matrices are padded to multiples of 128, K is
 // a multiple of 64): the A operand of stage kb starts at kb*s_pad*128 +
@@ -56,6 +75,10 @@ namespace {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kAccCols = 256;     // one fp32 accumulator of 128 lanes x 256 columns
 constexpr uint32_t kTmemCols = 512;    // two accumulators: epilogue of tile i overlaps the MMAs of tile i+1
+constexpr int32_t kArrivalsPerTile = 2 * kEpilogueWarps;   // completion-counter adds per pair tile
+constexpr int kTileRing = 4;           // ready tiles handed from a CTA's scheduler to its roles
+constexpr uint32_t kTileReaders = 2 + kEpilogueWarps;   // producer, MMA issuer, epilogue warps
+constexpr int kPairRing = 4;           // tiles handed from the even CTA's scheduler to the odd one's
 
 __device__ __forceinline__ int find_mat(const int32_t* start, int n, int t) {
   int lo = 0, hi = n - 1;
@@ -79,10 +102,12 @@ __device__ __forceinline__ size_t chunk_off(size_t stride, size_t row_off, int m
   return (size_t)(n >> 6) * stride + row_off + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
 }
 
+// The epilogue input was written by other CTAs earlier in the same launch:
+// read it from L2 (ld.global.cg), never from a possibly stale L1 line.
 __device__ __forceinline__ void load_chunk(const uint8_t* base, size_t stride, size_t row_off, int m, int n,
                                            uint4 (&w)[4]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) w[q] = *reinterpret_cast<const uint4*>(base + chunk_off(stride, row_off, m, n, q));
+  for (int q = 0; q < 4; ++q) w[q] = __ldcg(reinterpret_cast<const uint4*>(base + chunk_off(stride, row_off, m, n, q)));
 }
 
 // Unpack 32 bf16 (four 16-byte chunks) into fp32.
@@ -111,7 +136,7 @@ __device__ __forceinline__ void store_chunk(uint8_t* base, size_t stride, size_t
 
 // One element of the final step at a stored position: the update O (when the
 // caller asked for it) and, when applying, W <- decay * W - lr_scale * O.
-__device__ __forceinline__ void final_elem(const GemmMat& d, const GemmBatch& p, int64_t o, float v) {
+__device__ __forceinline__ void final_elem(const NsMat& d, const NsBatch& p, int64_t o, float v) {
   if (d.out) {
     if (p.out_bf16) static_cast<__nv_bfloat16*>(d.out)[o] = __float2bfloat16_rn(v);
     else static_cast<float*>(d.out)[o] = v;
@@ -129,7 +154,7 @@ __device__ __forceinline__ void final_elem(const GemmMat& d, const GemmBatch& p,
 
 // Final update for 32 consecutive X columns [n, n+32) of X row m, in the
 // caller's layout: stored (m, n) when not transposed, (n, m) otherwise.
-__device__ __forceinline__ void store_final(const GemmMat& d, const GemmBatch& p, int m, int n, const float (&v)[32]) {
+__device__ __forceinline__ void store_final(const NsMat& d, const NsBatch& p, int m, int n, const float (&v)[32]) {
   if (m >= d.s) return;
   if (!d.transposed) {
     const int64_t row0 = (int64_t)m * d.l;
@@ -166,91 +191,233 @@ __device__ __forceinline__ void store_final(const GemmMat& d, const GemmBatch& p
 
 struct Tile {
   int mi;        // matrix index in the batch
+  int phase;     // product index in the sequence: 3 * iteration + product
+  int mode;      // kGram, kPoly, kUpdate or kUpdateFinal
+  bool first;    // first iteration: fold the Frobenius prescale into the epilogue
+  bool symmetric;
+  bool b_mn;     // B operand is the MN-major X (update products)
+  bool zero;     // the matrix's momentum is exactly zero: no products
   int m0, n0;    // origin of the pair's 256-row output tile
   int mc;        // this CTA's 128 rows: [mc, mc + 128)
   int N;         // tile width (256, or 128 for the last column tile)
-  bool zero;     // the matrix's momentum is exactly zero: no products
+  int k_blocks;  // K / kBlockK
+  int32_t need;  // completions of this matrix's earlier products (this launch) to wait for
+  const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
+  const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
+  const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly, X for the update)
+  void* out;             // blocked bf16 output, or the caller's buffer (final update)
 };
 
-// Pair tile t of the launch.  Symmetric products: 256 x 256 tiles on or above
-// the diagonal, row pair-block I holding tiles I .. nb2-1; others: 256-row
-// tiles, rows fastest.
-__device__ __forceinline__ Tile decode_tile(const GemmBatch& p, int t, uint32_t rank) {
+// Tile t of the sequence's list.  Symmetric products: 256 x 256 tiles on or
+// above the diagonal, row pair-block I holding tiles I .. nb2-1; update: 256-row
+// tiles, rows fastest (neighbours share B-operand columns).
+__device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t rank) {
   Tile r;
-  r.mi = find_mat(p.tile_start, p.n, t);
-  const GemmMat& d = p.mat[r.mi];
-  const int local = t - p.tile_start[r.mi];
-  if (d.symmetric) {
+  const int it = t / p.iter_tiles;
+  int rem = t - it * p.iter_tiles;
+  const int prod = rem >= p.mode_start[2] ? 2 : (rem >= p.mode_start[1] ? 1 : 0);
+  rem -= p.mode_start[prod];
+  const int k = find_mat(p.tile_start[prod], p.n, rem);
+  r.mi = p.order[prod][k];
+  const int local = rem - p.tile_start[prod][k];
+  const NsMat& d = p.mat[r.mi];
+  const bool last = it == p.ns_steps - 1;
+  r.phase = 3 * it + prod;
+  r.first = it == 0;
+  uint8_t* xc = d.x[it & 1];
+  if (prod == kGram) {
+    r.mode = kGram;
+    r.a_op = xc; r.b_op = xc; r.c_in = nullptr; r.out = d.a;
+    r.k_blocks = d.l_pad / kBlockK;
+  } else if (prod == kPoly) {
+    r.mode = kPoly;
+    r.a_op = d.a; r.b_op = d.a; r.c_in = d.a; r.out = d.b;
+    r.k_blocks = d.s_pad / kBlockK;
+  } else {
+    r.mode = last ? kUpdateFinal : kUpdate;
+    r.a_op = d.b; r.b_op = xc; r.c_in = xc;
+    r.out = last ? d.out : static_cast<void*>(d.x[(it + 1) & 1]);
+    r.k_blocks = d.s_pad / kBlockK;
+  }
+  r.symmetric = prod != kUpdate;
+  r.b_mn = prod == kUpdate;
+  if (r.symmetric) {
     const int nb2 = d.s_pad / kPairM;
-    int rem = local, I = 0;
-    while (I < nb2 - 1 && rem >= nb2 - I) {
-      rem -= nb2 - I;
+    int rem2 = local, I = 0;
+    while (I < nb2 - 1 && rem2 >= nb2 - I) {
+      rem2 -= nb2 - I;
       ++I;
     }
     r.m0 = I * kPairM;
-    r.n0 = (I + rem) * kPairM;
+    r.n0 = (I + rem2) * kPairM;
     r.N = kBlockN;
   } else {
-    const int mt = local % d.tiles_m, nt = local / d.tiles_m;   // rows fastest: neighbours share B-operand columns
+    const int mt = local % d.tiles_m, nt = local / d.tiles_m;
     r.m0 = mt * kPairM;
     r.n0 = nt * kBlockN;
     r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
   }
   r.mc = r.m0 + (int)rank * kBlockM;
   r.zero = p.norm[d.norm_idx].x == 0.0f;
+  // Tiles of this matrix in products [0, ph): whole iterations, then the Gram
+  // (and polynomial) products of the current one.
+  const int per_iter = 2 * d.tiles_sym + d.tiles_m * d.tiles_n;
+  const int done_here = (r.phase / 3) * per_iter + (r.phase % 3) * d.tiles_sym;
+  const int done_before = (p.phase_begin / 3) * per_iter + (p.phase_begin % 3) * d.tiles_sym;
+  r.need = kArrivalsPerTile * (done_here - done_before);
   return r;
 }
 
 // Operand sources of stage kb of a tile (bounds: see the file header).
-__device__ __forceinline__ const uint8_t* a_block(const GemmMat& d, const Tile& tl, int kb, size_t kstride) {
-  return d.a_op + (size_t)kb * kstride + (size_t)(tl.mc >> 3) * 1024;
+__device__ __forceinline__ const uint8_t* a_block(const Tile& tl, int kb, size_t kstride) {
+  return tl.a_op + (size_t)kb * kstride + (size_t)(tl.mc >> 3) * 1024;
 }
 // K-major B: rows [n0 + half * N/2, + N/2).
-__device__ __forceinline__ const uint8_t* b_half_kmajor(const GemmMat& d, const Tile& tl, int kb, size_t kstride,
-                                                       uint32_t half) {
-  return d.b_op + (size_t)kb * kstride + (size_t)((tl.n0 + (int)half * (tl.N >> 1)) >> 3) * 1024;
+__device__ __forceinline__ const uint8_t* b_half_kmajor(const Tile& tl, int kb, size_t kstride, uint32_t half) {
+  return tl.b_op + (size_t)kb * kstride + (size_t)((tl.n0 + (int)half * (tl.N >> 1)) >> 3) * 1024;
 }
 // MN-major X: 64-column block n0/64 + j, K rows [64 kb, 64 kb + 64).
-__device__ __forceinline__ const uint8_t* b_block_mn(const GemmMat& d, const Tile& tl, int kb, size_t kstride, int j) {
-  return d.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
+__device__ __forceinline__ const uint8_t* b_block_mn(const Tile& tl, int kb, size_t kstride, int j) {
+  return tl.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* status) {
+__device__ __forceinline__ int32_t wait_code(int phase, int role) { return (phase << 8) | role; }
+
+// Called between polls of a wait: true when the wait must be abandoned --
+// another role of this CTA gave up, another CTA recorded a failure, or this
+// wait has run for kWaitLimitNs (then it records `code`).
+__device__ __forceinline__ bool give_up(volatile int* abort_flag, int32_t* status, uint64_t t0, int32_t code) {
+  if (*abort_flag) return true;
+  if (*reinterpret_cast<volatile int32_t*>(status) != 0) {
+    *abort_flag = 1;
+    return true;
+  }
+  if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+    *abort_flag = 1;
+    atomicCAS(status, 0, code);
+    return true;
+  }
+  return false;
+}
+
+// Bounded mbarrier wait.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                                              int32_t code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicOr(status, kStatusTimeout);
-      return false;
-    }
+    if (give_up(abort_flag, status, t0, code)) return false;
   }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmBatch p) {
+// Bounded wait until a matrix's completion counter reaches `need` (acquire:
+// the stores it counts are visible to this thread afterwards).
+__device__ __forceinline__ bool wait_done(const int32_t* ctr, int32_t need, volatile int* abort_flag, int32_t* status,
+                                          int32_t code) {
+  if (ptx::ld_acquire_gpu(ctr) >= need) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(64);
+      if (ptx::ld_acquire_gpu(ctr) >= need) return true;
+    }
+    if (give_up(abort_flag, status, t0, code)) return false;
+  }
+}
+
+// Bounded wait on an mbarrier that another CTA of the pair arrives on
+// (acquire at cluster scope).
+__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                      int32_t* status, int32_t code) {
+  if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if (give_up(abort_flag, status, t0, code)) return false;
+  }
+}
+
+// A ring of tile indices: slot k holds the tiles of sequence numbers
+// k, k + size, ...; full[k] (count 1) completes when the writer has stored
+// it, empty[k] when every reader has taken it.  Each CTA's scheduler feeds
+// its own roles through a CTA-local ring; the even CTA's scheduler feeds the
+// odd one's through a ring in the odd CTA (remote store and arrive), whose
+// empty barriers live in the even CTA.
+struct Ring {
+  uint32_t slot0;    // slot 0 (shared address, in the readers' CTA)
+  uint32_t full0;    // full[0], in the readers' CTA
+  uint32_t empty0;   // empty[0], in the writer's CTA
+};
+
+// CTA-local ring: the scheduler stores tile t into slot seq for this CTA's roles.
+__device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32_t t, volatile int* abort_flag,
+                                             int32_t* status) {
+  const uint32_t k = seq % kTileRing, use = seq / kTileRing;
+  if (!wait_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, abort_flag, status, wait_code(0, kRoleTileFree))) return false;
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(r.slot0 + 4u * k), "r"(t) : "memory");
+  ptx::mbar_arrive(r.full0 + 8u * k);   // releases the store (CTA scope)
+  return true;
+}
+
+// A role takes the tile of sequence number seq from its CTA's ring.
+__device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t& t, volatile int* abort_flag,
+                                          int32_t* status) {
+  const uint32_t k = seq % kTileRing, use = seq / kTileRing;
+  if (!wait_or_abort(r.full0 + 8u * k, use & 1, abort_flag, status, wait_code(0, kRoleTileFull))) return false;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
+  ptx::mbar_arrive(r.empty0 + 8u * k);
+  return true;
+}
+
+// Pair ring, even CTA's scheduler side: stores tile t into the odd CTA's slot seq.
+__device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_t t, volatile int* abort_flag,
+                                            int32_t* status) {
+  const uint32_t k = seq % kPairRing, use = seq / kPairRing;
+  if (!wait_cluster_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, abort_flag, status, wait_code(0, kRoleTileFree)))
+    return false;
+  ptx::st_shared_cluster_s32(ptx::mapa_shared(r.slot0 + 4u * k, 1), t);
+  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.full0 + 8u * k, 1));   // releases the store (cluster scope)
+  return true;
+}
+
+// Pair ring, odd CTA's scheduler side.
+__device__ __forceinline__ bool pair_take(const Ring& r, uint32_t seq, int32_t& t, volatile int* abort_flag,
+                                         int32_t* status) {
+  const uint32_t k = seq % kPairRing, use = seq / kPairRing;
+  if (!wait_cluster_or_abort(r.full0 + 8u * k, use & 1, abort_flag, status, wait_code(0, kRoleTileFull))) return false;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
+  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.empty0 + 8u * k, 0));
+  return true;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_constant__ NsBatch p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t tfull_bar[2];    // accumulator ready for the epilogue
   __shared__ __align__(8) uint64_t tempty_bar[2];   // accumulator drained, MMA may reuse it
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t ring_full[kTileRing];
+  __shared__ __align__(8) uint64_t ring_empty[kTileRing];
+  __shared__ int32_t ring_slot[kTileRing];
+  __shared__ __align__(8) uint64_t pair_full[kPairRing];    // used in the odd CTA
+  __shared__ __align__(8) uint64_t pair_empty[kPairRing];   // used in the even CTA
+  __shared__ int32_t pair_slot[kPairRing];                  // used in the odd CTA
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = p.tile_start[p.n];
   const uint32_t rank = ptx::cluster_ctarank();          // 0 or 1 within the CTA pair
-  const int cid = (int)ptx::cluster_id_x(), ncl = (int)ptx::cluster_count_x();
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  const int mode = p.mode;
-  const bool b_mn = (mode == kUpdate || mode == kUpdateFinal);
   constexpr uint16_t kPair = 0x3;                        // both CTAs of the cluster
+  const Ring ring{ptx::smem_u32(&ring_slot[0]), ptx::smem_u32(&ring_full[0]), ptx::smem_u32(&ring_empty[0])};
+  const Ring pair{ptx::smem_u32(&pair_slot[0]), ptx::smem_u32(&pair_full[0]), ptx::smem_u32(&pair_empty[0])};
 
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), kTmemCols);
@@ -266,6 +433,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       ptx::mbar_init(ptx::smem_u32(&tempty_bar[a]), kEpilogueWarps);
     }
     ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    for (int k = 0; k < kTileRing; ++k) {
+      ptx::mbar_init(ptx::smem_u32(&ring_full[k]), 1);
+      ptx::mbar_init(ptx::smem_u32(&ring_empty[k]), kTileReaders);
+    }
+    for (int k = 0; k < kPairRing; ++k) {
+      ptx::mbar_init(ptx::smem_u32(&pair_full[k]), 1);
+      ptx::mbar_init(ptx::smem_u32(&pair_empty[k]), 1);
+    }
     abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -283,32 +458,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       // B operand; the B half goes to both CTAs of the pair (multicast), so
       // each operand byte is read from L2 once per pair.
       const uint64_t pol = ptx::policy_evict_last();
-      uint32_t it = 0;
-      for (int t = cid; t < total && !*abort_v; t += ncl) {
+      uint32_t it = 0, seq = 0;
+      bool ok = true;
+      while (ok) {
+        int32_t t;
+        ok = local_take(ring, seq++, t, abort_v, p.status);
+        if (!ok || t >= p.tile_end) break;
         const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
-        const GemmMat& d = p.mat[tl.mi];
-        const size_t kstride = colblock_stride(d.s_pad);   // every operand has s_pad rows per column block
+        // The operands were stored by other CTAs (generic proxy) before the
+        // scheduler handed the tile out; the bulk copies read them through
+        // the async proxy.
+        if (tl.need > 0) ptx::fence_proxy_async_global();
+        const size_t kstride = colblock_stride(p.mat[tl.mi].s_pad);   // every operand has s_pad rows per column block
         const uint32_t b_bytes = (uint32_t)tl.N * kBlockK * 2;   // whole B tile: both halves land here
-        for (int kb = 0; kb < d.k_blocks; ++kb, ++it) {
+        for (int kb = 0; kb < tl.k_blocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t use = it / kStages;
           // stage s is free in both CTAs (both MMAs have read it)
-          if (!wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, abort_v, p.status)) break;
+          ok = wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, abort_v, p.status,
+                             wait_code(tl.phase, kRoleStageFree));
+          if (!ok) break;
           const uint32_t fb = ptx::smem_u32(&full_bar[s]);
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
           ptx::mbar_arrive_expect_tx(fb, kStageBytesA + b_bytes);
-          ptx::bulk_g2s(sa, a_block(d, tl, kb, kstride), kStageBytesA, fb, pol);
-          if (!b_mn) {
+          ptx::bulk_g2s(sa, a_block(tl, kb, kstride), kStageBytesA, fb, pol);
+          if (!tl.b_mn) {
             const uint32_t hb = b_bytes >> 1;
-            ptx::bulk_g2s_multicast(sb + rank * hb, b_half_kmajor(d, tl, kb, kstride, rank), hb, fb, kPair, pol);
+            ptx::bulk_g2s_multicast(sb + rank * hb, b_half_kmajor(tl, kb, kstride, rank), hb, fb, kPair, pol);
           } else {
             // X as the MN-major operand: 64-column blocks of 8 KB; this CTA
             // fetches the blocks of its half of the tile's columns.
             const int nblk = tl.N / 64, per = nblk >> 1;
             for (int j = (int)rank * per; j < ((int)rank + 1) * per; ++j)
-              ptx::bulk_g2s_multicast(sb + (uint32_t)j * 8192u, b_block_mn(d, tl, kb, kstride, j), 8192u, fb, kPair,
-                                      pol);
+              ptx::bulk_g2s_multicast(sb + (uint32_t)j * 8192u, b_block_mn(tl, kb, kstride, j), 8192u, fb, kPair, pol);
           }
         }
       }
@@ -321,21 +504,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------- MMA issuer
-      uint32_t it = 0, acc_it = 0;
-      for (int t = cid; t < total && !*abort_v; t += ncl) {
+      uint32_t it = 0, acc_it = 0, seq = 0;
+      bool ok = true;
+      while (ok) {
+        int32_t t;
+        ok = local_take(ring, seq++, t, abort_v, p.status);
+        if (!ok || t >= p.tile_end) break;
         const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
-        const GemmMat& d = p.mat[tl.mi];
         const uint32_t a = acc_it & 1, ause = acc_it >> 1;
-        if (!wait_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, abort_v, p.status)) break;
+        ok = wait_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, abort_v, p.status,
+                           wait_code(tl.phase, kRoleAccFree));
+        if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + a * kAccCols;
-        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, (uint32_t)tl.N, b_mn ? 1u : 0u);
-        bool ok = true;
-        for (int kb = 0; kb < d.k_blocks; ++kb, ++it) {
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, (uint32_t)tl.N, tl.b_mn ? 1u : 0u);
+        for (int kb = 0; kb < tl.k_blocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t use = it / kStages;
-          if (!wait_or_abort(ptx::smem_u32(&full_bar[s]), use & 1, abort_v, p.status)) { ok = false; break; }
+          ok = wait_or_abort(ptx::smem_u32(&full_bar[s]), use & 1, abort_v, p.status,
+                             wait_code(tl.phase, kRoleStageFull));
+          if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
 #pragma unroll
@@ -345,8 +534,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             // MN-major operand: 16 K rows = two 8-row atoms (2 KB); 64-column
             // blocks 8 KB apart (leading byte offset), 8-row K groups 1 KB
             // apart (stride byte offset).
-            const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 8192u, 1024u)
-                                        : ptx::smem_desc_sw128(sb + (uint32_t)k * 32u, 16u, 1024u);
+            const uint64_t bdesc = tl.b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 8192u, 1024u)
+                                           : ptx::smem_desc_sw128(sb + (uint32_t)k * 32u, 16u, 1024u);
             ptx::umma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           // frees stage s in both CTAs once these MMAs have read it
@@ -362,21 +551,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, kWaitLimitNs);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSchedulerWarp) {
     // -------------------------------------------------------------- epilogue
     // Eight warps: warp w reads TMEM lane quadrant w % 4 (the hardware rule)
-    // and one half of the tile's columns.
+    // and one half of the tile's columns.  Every wait's outcome is made
+    // warp-uniform before the warp acts on it (tcgen05.ld is warp-wide).
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    uint32_t acc_it = 0;
-    for (int t = cid; t < total; t += ncl) {
+    uint32_t acc_it = 0, seq = 0;
+    while (true) {
+      int32_t t = 0;
+      int got_tile = 1;
+      if (lane == 0) got_tile = local_take(ring, seq, t, abort_v, p.status);
+      ++seq;
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!__shfl_sync(0xffffffffu, got_tile, 0) || t >= p.tile_end) break;
       const Tile tl = decode_tile(p, t, rank);
-      const GemmMat& d = p.mat[tl.mi];
+      const NsMat& d = p.mat[tl.mi];
       const int m = tl.mc + quad * 32 + lane;          // this thread's output row
       const int cw = tl.N >> 1;                         // columns per warp
       const int c0 = half * cw;
       if (tl.zero) {
-        if (mode == kUpdateFinal) {
+        if (tl.mode == kUpdateFinal) {
           float z[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = 0.f;
@@ -386,26 +582,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       const size_t stride = colblock_stride(d.s_pad);
       const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
-      const bool has_c = (mode != kGram);
+      const bool has_c = (tl.mode != kGram);
       const int rblk = tl.mc >> 7;                     // this CTA's 128-row block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
       // the first chunk before waiting for the MMAs, the next one while the
       // current one is processed.
       uint4 xin[4];
-      if (has_c) load_chunk(d.c_in, stride, row_off, m, tl.n0 + c0, xin);
+      if (has_c) load_chunk(tl.c_in, stride, row_off, m, tl.n0 + c0, xin);
       const uint32_t a = acc_it & 1, ause = acc_it >> 1;
-      if (!wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, abort_v, p.status)) break;
+      const bool got = wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, abort_v, p.status,
+                                     wait_code(tl.phase, kRoleAccFull));
+      if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
       const float2 nrm = p.norm[d.norm_idx];
-      const float scale_gram = p.first_iter ? nrm.y * nrm.y : 1.0f;
-      const float scale_upd = p.first_iter ? nrm.y : 1.0f;
+      const float scale_gram = tl.first ? nrm.y * nrm.y : 1.0f;
+      const float scale_upd = tl.first ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
       for (int c = c0; c < c0 + cw; c += 32) {
         const bool more = c + 32 < c0 + cw;
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
         uint4 xnext[4];
-        if (has_c && more) load_chunk(d.c_in, stride, row_off, m, tl.n0 + c + 32, xnext);
+        if (has_c && more) load_chunk(tl.c_in, stride, row_off, m, tl.n0 + c + 32, xnext);
         ptx::tmem_ld_wait();
         if (!more) {
           // last chunk read: hand the accumulator back to the MMA warp
@@ -418,16 +616,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         // Symmetric products: a block below the diagonal (only inside a
         // diagonal pair tile) is written by its mirror image; a block above
         // it is written directly and transposed.
-        const bool below = d.symmetric && cblk < rblk;
-        const bool mirror = d.symmetric && cblk > rblk;
+        const bool below = tl.symmetric && cblk < rblk;
+        const bool mirror = tl.symmetric && cblk > rblk;
         float v[32];
-        if (mode == kGram) {
+        if (tl.mode == kGram) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
         } else {
           float x[32];
           unpack_bf16x32(xin, x);
-          if (mode == kPoly) {
+          if (tl.mode == kPoly) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
           } else {
@@ -435,10 +633,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
           }
         }
-        if (mode == kUpdateFinal) {
+        if (tl.mode == kUpdateFinal) {
           store_final(d, p, m, n, v);
         } else if (!below) {
-          uint8_t* out = static_cast<uint8_t*>(d.out);
+          uint8_t* out = static_cast<uint8_t*>(tl.out);
           store_chunk(out, stride, row_off, m, n, v);
           if (mirror) {
             // element (n + j, m)
@@ -456,7 +654,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
       }
       ++acc_it;
+      if (tl.phase + 1 < p.phase_end) {
+        // Publish this warp's share of the tile: its stores are ordered
+        // before the counter (release), and before the bulk copies that later
+        // tiles issue after reading it (proxy fence).
+        ptx::fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) ptx::red_release_gpu_add(p.done + tl.mi, 1);
+      }
     }
+  } else {
+    if (lane == 0) {
+      // ----------------------------------------------------------- scheduler
+      // Even CTA: takes the pair's tiles in list order, waits until the
+      // earlier products of each tile's matrix are stored, and hands the tile
+      // to the odd CTA's scheduler and to this CTA's roles (the end marker
+      // last).  Odd CTA: forwards what it receives to its own roles.  The
+      // roles' reads of the stored products are ordered after this wait
+      // through the rings' release/acquire chain.
+      uint32_t seq = 0;
+      while (true) {
+        int32_t t;
+        if (rank == 0) {
+          t = p.tile_begin + atomicAdd(p.next_tile, 1);
+          if (t > p.tile_end) t = p.tile_end;           // the end marker
+          if (t < p.tile_end) {
+            const Tile tl = decode_tile(p, t, 0);
+            if (!tl.zero && tl.need > 0 &&
+                !wait_done(p.done + tl.mi, tl.need, abort_v, p.status, wait_code(tl.phase, kRoleDependency)))
+              break;
+          }
+          if (!pair_publish(pair, seq, t, abort_v, p.status)) break;
+        } else {
+          if (!pair_take(pair, seq, t, abort_v, p.status)) break;
+        }
+        if (!local_publish(ring, seq++, t, abort_v, p.status) || t >= p.tile_end) break;
+      }
+    }
+    __syncwarp();
   }
 
   // Teardown: no CTA of the pair leaves (or frees TMEM) while its peer may
@@ -471,10 +707,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 
 }  // namespace
 
-cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s) {
+cudaError_t launch_ns(const NsBatch& b, cudaStream_t s) {
+  const int total_tiles = b.tile_end - b.tile_begin;
   if (total_tiles <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kGemmSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(ns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -487,7 +723,8 @@ cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s) 
   cfg.stream = s;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  // Persistent: as many CTA pairs as can be resident at once (one CTA per SM).
+  // Persistent: as many CTA pairs as can be resident at once (one CTA per
+  // SM) -- the dependency waits rely on every pair being resident.
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -495,12 +732,12 @@ cudaError_t launch_ns_gemm(const GemmBatch& b, int total_tiles, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3((unsigned)(2 * (sms / 2)), 1, 1);
   int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, ns_gemm_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, ns_kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   const int clusters = total_tiles < max_clusters ? total_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, ns_gemm_kernel, b);
+  e = cudaLaunchKernelEx(&cfg, ns_kernel, b);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
