@@ -42,11 +42,13 @@ from matrix_optimizers_under_gb300 import workloads as W  # noqa: E402
 METRIC = "owner-step ms; Newton–Schulz TFLOP/s (% BF16 peak); AdamW-tail GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per ns_gemm_kernel launch on the llama3_8b_rank owner set, the
-# mean over one owner step's 15 launches, from the ncu capture summarised in
+# DRAM bytes (read + write) per Newton-Schulz kernel launch on the llama3_8b_rank owner set
+# (0.5/0.6: the mean over one owner step's 15 per-product launches; 0.7: the one launch that
+# runs all of a step's products), from the ncu capture summarised in
 # profiles/launches_llama3_8b_rank.md; keyed by the library version it was taken on, so
 # that a changed kernel reports null until it is captured again.
-NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9}
+NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9,
+                   ("0.7.0", "llama3_8b_rank"): 50.17e9}
 
 
 # --------------------------------------------------------------------------- helpers
