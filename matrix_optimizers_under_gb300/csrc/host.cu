@@ -203,7 +203,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.7.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -247,6 +247,9 @@ int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void
   const int st = make_layout(shards, n_shards, L);
   if (st != MFSDP_OK) return st;
   if (!ns_counts_fit(*L, ns_steps)) return MFSDP_ERR_UNSUPPORTED_SHAPE;
+  // The Newton-Schulz tensor copies address the workspace in 128-byte rows
+  // with int32 coordinates.
+  if (L->bytes / 128 >= (size_t)INT32_MAX) return MFSDP_ERR_UNSUPPORTED_SHAPE;
   for (int i = 0; i < n_shards; ++i) {
     const mfsdp_matrix_shard& sh = shards[i];
     if (sh.offset < 0 || sh.offset > numel || sh.rows * sh.cols > numel - sh.offset) return MFSDP_ERR_OUT_OF_BOUNDS;
@@ -568,6 +571,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
     nb.b = b;
     nb.c = c;
     nb.norm = norm;
+    nb.ws = ws;
     nb.status = status;
     nb.next_tile = counters;
     nb.done = counters + 1 + base;
@@ -625,7 +629,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
     nb.tile_end = off * ns_steps;
     st = cuda_status(cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(n_shards + 1), stream));
     if (st != MFSDP_OK) return st;
-    st = cuda_status(launch_ns(nb, stream));
+    st = cuda_status(launch_ns(nb, L.bytes, stream));
     if (st != MFSDP_OK) return st;
   }
   return MFSDP_OK;

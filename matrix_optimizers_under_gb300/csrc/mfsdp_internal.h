@@ -16,13 +16,13 @@ constexpr int kTile = 64;          // momentum-kernel tile edge (elements)
 constexpr int kPartialsPerTile = 8;  // momentum kernel: one norm partial per warp
 constexpr int kPad = 128;          // workspace: the long side is padded to a multiple of this
 constexpr int kPadS = 256;         // workspace: the short side is padded to a multiple of this (one CTA pair)
-constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows per CTA (UMMA M)
-constexpr int kPairM = 2 * kBlockM;  // rows of the tile a CTA pair shares (B operand multicast)
+constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows per CTA (its TMEM lanes)
+constexpr int kPairM = 2 * kBlockM;  // rows of the tile a CTA pair computes (pair UMMA, M = 256)
 constexpr int kBlockN = 256;       // Newton-Schulz GEMM tile columns (UMMA N)
 constexpr int kBlockK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kStages = 4;         // smem pipeline depth
-constexpr int kStageBytesA = kBlockM * kBlockK * 2;   // 16 KB
-constexpr int kStageBytesB = kBlockN * kBlockK * 2;   // 32 KB
+constexpr int kStages = 6;         // smem pipeline depth
+constexpr int kStageBytesA = kBlockM * kBlockK * 2;         // 16 KB: this CTA's 128 rows of A
+constexpr int kStageBytesB = (kBlockN / 2) * kBlockK * 2;   // 16 KB: this CTA's half of B's columns
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kEpilogueWarps = 8;  // warps 2-9 of the GEMM CTA: two per TMEM lane quadrant
 constexpr int kSchedulerWarp = 2 + kEpilogueWarps;        // warp 10: hands out ready tiles
@@ -122,6 +122,7 @@ struct NsBatch {
   float a, b, c;
   float decay;           // apply: 1 - lr * weight_decay
   const float2* norm;
+  const uint8_t* ws;     // workspace base: tensor-copy row y is byte 128 y of it
   int32_t* status;       // device status word (first wait that gave up)
   int32_t* next_tile;    // tiles handed out so far (dynamic schedule), zeroed before the launch
   int32_t* done;         // per matrix of the launch, zeroed before it
@@ -185,7 +186,7 @@ enum WaitRole : int32_t {
 cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
 cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
-cudaError_t launch_ns(const NsBatch& b, cudaStream_t s);
+cudaError_t launch_ns(const NsBatch& b, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_segments(const SegBatch& b, int total_chunks, cudaStream_t s);
 // fp32 scalars of one AdamW step, formed in double on the host.
 struct AdamScalars {
