@@ -19,10 +19,11 @@ constexpr int kPadS = 256;         // workspace: the short side is padded to a m
 constexpr int kBlockM = 128;       // Newton-Schulz GEMM tile rows per CTA (its TMEM lanes)
 constexpr int kPairM = 2 * kBlockM;  // rows of the tile a CTA pair computes (pair UMMA, M = 256)
 constexpr int kBlockN = 256;       // Newton-Schulz GEMM tile columns (UMMA N)
-constexpr int kBlockK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kStages = 6;         // smem pipeline depth
-constexpr int kStageBytesA = kBlockM * kBlockK * 2;         // 16 KB: this CTA's 128 rows of A
-constexpr int kStageBytesB = (kBlockN / 2) * kBlockK * 2;   // 16 KB: this CTA's half of B's columns
+constexpr int kAtomK = 64;         // K elements of one 128-byte swizzle row (a column block of the layout)
+constexpr int kBlockK = 128;       // K elements per pipeline stage: two column blocks
+constexpr int kStages = 3;         // smem pipeline depth
+constexpr int kStageBytesA = kBlockM * kBlockK * 2;         // 32 KB: this CTA's 128 rows of A
+constexpr int kStageBytesB = (kBlockN / 2) * kBlockK * 2;   // 32 KB: this CTA's half of B's columns
 constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kEpilogueWarps = 8;  // warps 2-9 of the GEMM CTA: two per TMEM lane quadrant
 constexpr int kSchedulerWarp = 2 + kEpilogueWarps;        // warp 10: hands out ready tiles

@@ -18,8 +18,9 @@
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
 // atoms of one 64-column block contiguous.  So a CTA's share of a pipeline
-// stage is one 16 KB run of rows for each operand (two 8 KB runs for the
-// MN-major X of the update), and a tensor copy of one map that views the whole
+// stage is one 16 KB run of rows per column block for each operand (for the
+// MN-major X of the update, one 16 KB run of 128 K rows per 64-column block),
+// and a tensor copy of one map that views the whole
 // workspace as 128-byte rows lands it in shared memory byte for byte, ready
 // for tcgen05.mma: one map for any mix of shapes in one launch, and the same
 // stored X serves as the K-major operand of the Gram product and the MN-major
@@ -47,8 +48,9 @@
 // A pair computes a 256 x N tile with the pair MMA (tcgen05 cta_group::2,
 // M = 256): each CTA holds 128 rows of A and half of B's N columns in its own
 // shared memory, and its 128 output rows in its own TMEM.  In each CTA, warp 0
-// (one lane) streams K in 64-element stages through a 6-deep mbarrier ring of
-// 32 KB stages; its tensor copies complete on the even CTA's full barrier
+// (one lane) streams K in 128-element stages (two column blocks of the layout)
+// through a 3-deep mbarrier ring of 64 KB stages; its tensor copies complete on
+// the even CTA's full barrier
 // (cta_group::2 copies), which the even producer arms with both CTAs' bytes.
 // The even CTA's warp 1 (one lane) issues 256 x N x 16 pair UMMAs into one of
 // two 256-column accumulators and frees each stage in both CTAs with one
@@ -504,19 +506,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           const uint32_t fb = ptx::mapa_shared(fb_local, 0);
           if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, pair_bytes);
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
-          const int32_t ya = ws_row(p, a_block(tl, kb, kstride));
-          ptx::tma_load_2d_pair(sa, &tmap_16k, 0, ya, fb, pol);
-          if (!tl.b_mn) {
-            const int32_t yb = ws_row(p, b_half_kmajor(tl, kb, kstride, rank));
-            if (nh == 128) ptx::tma_load_2d_pair(sb, &tmap_16k, 0, yb, fb, pol);
-            else ptx::tma_load_2d_pair(sb, &tmap_8k, 0, yb, fb, pol);
-          } else {
-            // X as the MN-major operand: 64-column blocks of 64 K rows (8 KB);
-            // this CTA holds the blocks of its half of the tile's columns.
+          // two column blocks (K atoms) per stage
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            ptx::tma_load_2d_pair(sa + (uint32_t)h * 16384u, &tmap_16k, 0, ws_row(p, a_block(tl, 2 * kb + h, kstride)), fb, pol);
+            if (!tl.b_mn) {
+              const int32_t yb = ws_row(p, b_half_kmajor(tl, 2 * kb + h, kstride, rank));
+              if (nh == 128) ptx::tma_load_2d_pair(sb + (uint32_t)h * 16384u, &tmap_16k, 0, yb, fb, pol);
+              else ptx::tma_load_2d_pair(sb + (uint32_t)h * 8192u, &tmap_8k, 0, yb, fb, pol);
+            }
+          }
+          if (tl.b_mn) {
+            // X as the MN-major operand: per 64-column block, the stage's 128 K
+            // rows are one contiguous 16 KB run.
             const int per = nh / 64;
             for (int jj = 0; jj < per; ++jj)
-              ptx::tma_load_2d_pair(sb + (uint32_t)jj * 8192u, &tmap_8k, 0,
-                                    ws_row(p, b_block_mn(tl, kb, kstride, (int)rank * per + jj)), fb, pol);
+              ptx::tma_load_2d_pair(sb + (uint32_t)jj * 16384u, &tmap_16k, 0,
+                                    ws_row(p, b_block_mn(tl, 2 * kb, kstride, (int)rank * per + jj)), fb, pol);
           }
         }
       }
@@ -558,15 +564,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
+          const uint32_t bh = (uint32_t)(tl.N >> 1) * 128u;   // bytes of one K atom of this CTA's B half
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
-            // K-major operand: advance 16 elements (32 bytes) inside the swizzle row.
-            const uint64_t adesc = ptx::smem_desc_sw128(sa + (uint32_t)k * 32u, 16u, 1024u);
+            const uint32_t h = (uint32_t)k >> 2, kk = (uint32_t)k & 3;
+            // K-major operand: atom h, then 16 elements (32 bytes) inside the swizzle row.
+            const uint64_t adesc = ptx::smem_desc_sw128(sa + h * 16384u + kk * 32u, 16u, 1024u);
             // MN-major operand: 16 K rows = two 8-row atoms (2 KB); 64-column
-            // blocks 8 KB apart (leading byte offset), 8-row K groups 1 KB
+            // blocks 16 KB apart (leading byte offset), 8-row K groups 1 KB
             // apart (stride byte offset).
-            const uint64_t bdesc = tl.b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 8192u, 1024u)
-                                           : ptx::smem_desc_sw128(sb + (uint32_t)k * 32u, 16u, 1024u);
+            const uint64_t bdesc = tl.b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 16384u, 1024u)
+                                           : ptx::smem_desc_sw128(sb + h * bh + kk * 32u, 16u, 1024u);
             ptx::umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           // frees stage s in both CTAs once these MMAs have read it
