@@ -203,7 +203,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.2"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.3"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -439,8 +439,14 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
                            static_cast<const uint8_t*>(update_dev) + (size_t)lo * usz, (size_t)(hi - lo) * usz,
                            cudaMemcpyDeviceToHost, s_out);
     if (ce == cudaSuccess) ce = cudaEventRecord(e_out, s_out);
-    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, e_out, 0);   // `stream` ends after every copy
   }
+  // `stream` ends after every copy out.  The waits come after the loop: inside
+  // it they would hold group g+1's compute until group g's update has left the
+  // device, serialising every copy out with the next group's compute (the
+  // ranges they touch are disjoint: a group's copy out reads only its own
+  // update segments).
+  for (int g = 0; g < ng && ce == cudaSuccess; ++g)
+    if (!grp[g].empty()) ce = cudaStreamWaitEvent(stream, ev[3 + 3 * g], 0);
   cleanup();
   if (ce != cudaSuccess) return MFSDP_ERR_CUDA;
   return st;
