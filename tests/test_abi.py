@@ -222,3 +222,16 @@ def test_step_flops(mfsdp):
     assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300)
     assert executed < dense     # the symmetric skipping outweighs the padding here
     assert mfsdp.muon_step_flops([], 5) == (0, 0)
+
+
+def test_newton_schulz_index_limits(mfsdp):
+    """The one-launch Newton-Schulz kernel indexes tiles and counts completions in
+    int32, and its tensor copies address the workspace in 128-byte rows with int32
+    coordinates.  Owner sets past either limit are refused on the host, before
+    anything is queued (the pointers here are fake)."""
+    big = [mfsdp.make_shard(0, 32768, 1 << 24)]          # 2 * 8256 + 128 * 65536 tiles per iteration
+    assert step(mfsdp, big, numel=32768 << 24, ns=64, wsb=1 << 62) == mfsdp.ERR_UNSUPPORTED_SHAPE
+    wide = [mfsdp.make_shard(0, 16384, 1 << 24)]         # counts fit over 5 steps, workspace > 2^31 rows
+    assert step(mfsdp, wide, numel=16384 << 24, ns=5, wsb=1 << 62) == mfsdp.ERR_UNSUPPORTED_SHAPE
+    # the same shape with a workspace that is too small still reports the shape first
+    assert step(mfsdp, wide, numel=16384 << 24, ns=5, wsb=1 << 20) == mfsdp.ERR_UNSUPPORTED_SHAPE
