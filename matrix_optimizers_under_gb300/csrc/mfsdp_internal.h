@@ -1,5 +1,5 @@
 // Launch descriptors shared by the host orchestration (host.cu) and the
-// kernels.  Every grouped launch carries its per-matrix table by value as a
+// kernels.  Every launch carries its per-matrix table by value as a
 // __grid_constant__ kernel parameter, so a step needs no device-side metadata
 // upload and can be captured in a CUDA graph as plain kernel nodes.
 #pragma once
@@ -11,7 +11,7 @@
 
 namespace mfsdp {
 
-constexpr int kMaxBatch = 128;     // matrices per grouped launch
+constexpr int kMaxBatch = 128;     // matrices per launch
 constexpr int kTile = 64;          // momentum-kernel tile edge (elements)
 constexpr int kPartialsPerTile = 8;  // momentum kernel: one norm partial per warp
 constexpr int kPad = 128;          // workspace: the long side is padded to a multiple of this
