@@ -49,7 +49,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # that a changed kernel reports null until it is captured again.
 NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9,
                    ("0.7.0", "llama3_8b_rank"): 50.17e9, ("0.8.1", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9}
+                   ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
+                   ("0.8.4", "llama3_8b_rank"): 50.02e9}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -356,16 +357,24 @@ def run_ours(args):
                                   wd=w.weight_decay, step=step_counter[0])
             tp_host.copy_(tp, non_blocking=True)
 
-    one_step_host()
+    # As many untimed warm-up steps as the device-resident measurement: with a
+    # single one, the first timed step sometimes took ~200 ms more (a one-off
+    # on the host-memory side) and dominated the mean.
+    for _ in range(max(args.warmup, 1)):
+        one_step_host()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     e0.record(stream)
-    for _ in range(e2e_steps):
+    step_ev[0].record(stream)
+    for k in range(e2e_steps):
         one_step_host()
+        step_ev[k + 1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_steps_ms = [round(step_ev[k].elapsed_time(step_ev[k + 1]), 3) for k in range(e2e_steps)]
 
     # ---------------------------------------------------------- supplementary: a large AdamW tail
     sup = {}
@@ -472,7 +481,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
-                "pipeline_groups": args.e2e_groups},
+                "pipeline_groups": args.e2e_groups, "steps_ms": e2e_steps_ms},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,

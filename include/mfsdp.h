@@ -225,9 +225,12 @@ int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int32_t n_shar
  *                            other argument as for mfsdp_muon_owner_step.
  *   groups >= 1 (1 = no overlap).
  * The call returns once everything is queued; work queued on `stream` later
- * runs after the last copy.  The helper streams and events are created and
- * destroyed inside the call.  Errors: as mfsdp_muon_owner_step, plus
- * INVALID_ARG for a NULL host buffer or groups < 1. */
+ * runs after the last copy.  The two copy streams and their events belong to
+ * the library: created on a device's first call and kept until the process
+ * exits.  Calls on one device enqueue one at a time (a lock held while
+ * queuing, not while the GPU works) and their copies run in call order.
+ * Errors: as mfsdp_muon_owner_step, plus INVALID_ARG for a NULL host buffer
+ * or groups < 1, and CUDA when the current device's index is 64 or more. */
 int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards,
                                const void* grad_host, void* grad_dev, int32_t grad_dtype,
                                float* momentum,

@@ -16,6 +16,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "mfsdp.h"
@@ -25,6 +26,15 @@ namespace mfsdp {
 namespace {
 
 constexpr size_t kHeaderBytes = 256;
+
+// Copy streams and events of the host-buffer step, per device.
+constexpr int kMaxPipeDevices = 64;
+struct CopyPipe {
+  std::mutex mu;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+CopyPipe g_pipe[kMaxPipeDevices];
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -203,7 +213,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.3"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.4"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -382,31 +392,29 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
   }
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  std::vector<cudaEvent_t> ev;   // ev[0]: entry; per group: copied in, computed, copied out
-  auto cleanup = [&]() {
-    for (cudaEvent_t e : ev) cudaEventDestroy(e);
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
-  };
-  if (cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) != cudaSuccess) {
-    cleanup();
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxPipeDevices) return MFSDP_ERR_CUDA;
+  // The device's copy streams and events, kept for the life of the process
+  // (creating streams per call occasionally stalled a call for hundreds of
+  // ms).  Calls on one device enqueue under its lock and share the copy
+  // streams, so their copies run in call order.
+  CopyPipe& pipe = g_pipe[dev];
+  std::lock_guard<std::mutex> lock(pipe.mu);
+  if (!pipe.s_in && (cudaStreamCreateWithFlags(&pipe.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+                     cudaStreamCreateWithFlags(&pipe.s_out, cudaStreamNonBlocking) != cudaSuccess))
     return MFSDP_ERR_CUDA;
+  // ev[0]: entry; per group: copied in, computed, copied out.  Re-recording an
+  // event that earlier calls' enqueued waits refer to is fine: those waits
+  // hold the state the event had when they were enqueued.
+  std::vector<cudaEvent_t>& ev = pipe.ev;
+  while (ev.size() < 1 + 3 * (size_t)ng) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MFSDP_ERR_CUDA;
+    ev.push_back(e);
   }
-  ev.resize(1 + 3 * (size_t)ng, nullptr);
-  for (auto& e : ev) {
-    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
-      e = nullptr;
-      cleanup();
-      return MFSDP_ERR_CUDA;
-    }
-  }
+  cudaStream_t s_in = pipe.s_in, s_out = pipe.s_out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (clear_status(ws, stream) != MFSDP_OK) {
-    cleanup();
-    return MFSDP_ERR_CUDA;
-  }
+  if (clear_status(ws, stream) != MFSDP_OK) return MFSDP_ERR_CUDA;
   cudaError_t ce = cudaEventRecord(ev[0], stream);            // earlier work on `stream` comes first
   ce = ce == cudaSuccess ? cudaStreamWaitEvent(s_in, ev[0], 0) : ce;
   for (int g = 0; g < ng && ce == cudaSuccess && st == MFSDP_OK; ++g) {
@@ -447,7 +455,6 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
   // update segments).
   for (int g = 0; g < ng && ce == cudaSuccess; ++g)
     if (!grp[g].empty()) ce = cudaStreamWaitEvent(stream, ev[3 + 3 * g], 0);
-  cleanup();
   if (ce != cudaSuccess) return MFSDP_ERR_CUDA;
   return st;
 }

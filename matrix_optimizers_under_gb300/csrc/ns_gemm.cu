@@ -768,6 +768,42 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// CTA pairs of ns_kernel that fit on the device at once (one CTA per SM),
+// worked out once per device: the kernel is persistent and the grid is this
+// many pairs (or fewer, for a short tile list).
+cudaError_t resident_pairs(int dev, int* out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int pairs[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pairs[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(ns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (sms / 2)), 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, ns_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    pairs[dev] = n;
+  }
+  *out = pairs[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 // The whole workspace as a 2-D tensor of 128-byte rows, with two boxes: 128
@@ -796,7 +832,11 @@ cudaError_t launch_ns(const NsBatch& b, size_t ws_bytes, cudaStream_t s) {
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(ns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int max_clusters = 0;
+  e = resident_pairs(dev, &max_clusters);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -809,17 +849,6 @@ cudaError_t launch_ns(const NsBatch& b, size_t ws_bytes, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  // Persistent: as many CTA pairs as can be resident at once (one CTA per SM).
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)(2 * (sms / 2)), 1, 1);
-  int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, ns_kernel, &cfg);
-  if (e != cudaSuccess) return e;
-  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   const int clusters = total_tiles < max_clusters ? total_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   e = cudaLaunchKernelEx(&cfg, ns_kernel, b, tmap_8k, tmap_16k);
