@@ -65,15 +65,17 @@
 // every other CTA sees the word and stops too, and each drains what it issued,
 // frees TMEM and returns.
 //
-// Bounds of every tensor copy (all matrices are padded to multiples of 128, K
-// is a multiple of 64): a CTA's A rows of stage kb start at kb*s_pad*128 +
-// (mc/8)*1024 and span 16 KB, ending at most at (K/64-1)*s_pad*128 +
-// (s_pad-128)*128 + 16384 = K*s_pad*2, the end of the operand; its K-major B
-// half likewise ends at most at (K/64-1)*s_pad*128 + n0*128 + N*128 <=
-// K*s_pad*2 since n0 + N <= s_pad; the MN-major X runs (column block
-// n0/64 + j, K rows 64kb..64kb+63) end at most at (l_pad/64-1)*s_pad*128 +
-// (s_pad/64-1)*8192 + 8192 = l_pad*s_pad*2, the end of X.  Every run starts
-// on a 128-byte row of the map, so its x coordinate is 0.
+// Bounds of every tensor copy (the long side is padded to a multiple of 128
+// and the short side to a multiple of 256, so K is a multiple of 128 and a
+// stage covers column blocks 2kb and 2kb+1): a CTA's A rows in column block c
+// start at c*s_pad*128 + (mc/8)*1024 and span 16 KB, ending at most at
+// (K/64-1)*s_pad*128 + (s_pad-128)*128 + 16384 = K*s_pad*2, the end of the
+// operand; its K-major B half likewise ends at most at (K/64-1)*s_pad*128 +
+// n0*128 + N*128 <= K*s_pad*2 since n0 + N <= s_pad; the MN-major X runs
+// (column block n0/64 + j, K rows 128kb..128kb+127, 16 KB) end at most at
+// (l_pad/64-1)*s_pad*128 + (s_pad/128-1)*16384 + 16384 = l_pad*s_pad*2, the
+// end of X.  Every run starts on a 128-byte row of the map, so its x
+// coordinate is 0.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
