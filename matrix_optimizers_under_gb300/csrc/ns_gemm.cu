@@ -699,8 +699,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       ++acc_it;
       if (tl.phase + 1 < p.phase_end) {
         // Publish this warp's share of the tile: its stores are ordered
-        // before the counter (release), and before the bulk copies that later
-        // tiles issue after reading it (proxy fence).
+        // before the counter (release), and before the tensor copies that
+        // later tiles issue after reading it (proxy fence).
         ptx::fence_proxy_async_global();
         __threadfence();
         __syncwarp();

@@ -29,7 +29,7 @@ __device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Orders this thread's generic-proxy global accesses with later async-proxy
-// ones (bulk copies), in both directions.
+// ones (tensor copies), in both directions.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
