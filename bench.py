@@ -50,7 +50,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9,
                    ("0.7.0", "llama3_8b_rank"): 50.17e9, ("0.8.1", "llama3_8b_rank"): 50.02e9,
                    ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.4", "llama3_8b_rank"): 50.02e9}
+                   ("0.8.4", "llama3_8b_rank"): 50.02e9,
+                   ("0.8.5", "llama3_8b_rank"): 50.58e9}
 
 
 # --------------------------------------------------------------------------- helpers
