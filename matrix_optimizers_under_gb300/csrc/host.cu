@@ -19,6 +19,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "mfsdp.h"
 #include "mfsdp_internal.h"
 
@@ -26,6 +28,15 @@ namespace mfsdp {
 namespace {
 
 constexpr size_t kHeaderBytes = 256;
+
+// NVTX range around the host-side queuing of one phase (visible to nsys, and
+// to ncu's --nvtx-include filters; free when no tool is attached).
+struct PhaseRange {
+  explicit PhaseRange(const char* name) { nvtxRangePushA(name); }
+  ~PhaseRange() { nvtxRangePop(); }
+  PhaseRange(const PhaseRange&) = delete;
+  PhaseRange& operator=(const PhaseRange&) = delete;
+};
 
 // Copy streams and events of the host-buffer step, per device.
 constexpr int kMaxPipeDevices = 64;
@@ -420,6 +431,7 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
   for (int g = 0; g < ng && ce == cudaSuccess && st == MFSDP_OK; ++g) {
     const std::vector<mfsdp_matrix_shard>& sh = grp[g];
     if (sh.empty()) continue;
+    const PhaseRange range("mfsdp host-buffer group");
     int64_t lo = sh.front().offset, hi = 0;
     for (const auto& x : sh) {
       lo = std::min(lo, x.offset);
@@ -475,6 +487,7 @@ namespace {
 int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, const void* grad,
                           int32_t grad_dtype, float* momentum, float beta, int32_t nesterov, float eps, uint8_t* ws,
                           cudaStream_t stream) {
+  const PhaseRange range("mfsdp momentum");
   float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
   float* partials = reinterpret_cast<float*>(ws + L.partial_off);
   const size_t gsz = dtype_size(grad_dtype);
@@ -532,6 +545,7 @@ int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const 
 int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout& L, void* update,
                     int32_t update_dtype, int32_t ns_steps, float a, float b, float c, uint8_t* ws,
                     cudaStream_t stream, const ApplyArgs* apply) {
+  const PhaseRange range(ns_steps ? "mfsdp newton-schulz" : "mfsdp emit");
   float2* norm = reinterpret_cast<float2*>(ws + L.norm_off);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   const size_t usz = dtype_size(update_dtype);
@@ -706,6 +720,7 @@ extern "C" int mfsdp_adamw_tail_step(float* p, const float* g, float* m, float* 
   k.step_size = (float)(lr / bc1);
   k.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
   k.eps = (float)eps;
+  const PhaseRange range("mfsdp adamw tail");
   return cuda_status(launch_adamw(p, g, m, v, n, k, static_cast<cudaStream_t>(stream_ptr)));
 }
 
@@ -823,6 +838,7 @@ extern "C" int mfsdp_segment_copy(const void* const* srcs, const int64_t* src_nu
       chunks += (g.numel + kSegChunk - 1) / kSegChunk;
     }
     b.chunk_start[cnt] = (int32_t)chunks;
+    const PhaseRange range("mfsdp segment copy");
     const int st = cuda_status(launch_segments(b, (int)chunks, stream));
     if (st != MFSDP_OK) return st;
   }
