@@ -297,6 +297,16 @@ int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, in
  * every call that runs the momentum phase. */
 int mfsdp_muon_device_status(const void* workspace, void* stream, int32_t* detail);
 
+/* Testing only: the next Newton-Schulz launch of this process (one launch; the
+ * hook then clears itself) gives tile `tile` of its tile list a dependency
+ * that is never satisfied, so the wait for it runs out after 2 s.  The kernel
+ * then ends in bounded time, and mfsdp_muon_device_status reports
+ * MFSDP_ERR_DEVICE_TIMEOUT with role 5 (the scheduler's dependency wait) or 8
+ * (a role of the same CTA pair waiting to be handed that tile).
+ * The context stays usable.  This exercises the bounded-wait path without
+ * faulting or hanging the GPU.  Returns INVALID_ARG for tile < 0. */
+int mfsdp_test_inject_stall(int32_t tile);
+
 /* Layout of the workspace, for inspection: for shard i, out[8*i + 0..7] =
  * { byte offset of X0, of X1, of A, of B, s_pad, l_pad, s, l }.  X0/X1 are
  * s_pad x l_pad, A/B s_pad x s_pad, bf16, stored as 1024-byte atoms of

@@ -40,7 +40,7 @@ EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
             "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
-            "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy")
+            "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall")
 
 SEGMENT_REDUCE = 0
 SEGMENT_GATHER = 1
@@ -104,6 +104,8 @@ _lib.mfsdp_muon_step_flops.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, 
 _lib.mfsdp_muon_step_flops.restype = ctypes.c_int
 _lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.mfsdp_muon_device_status.restype = ctypes.c_int
+_lib.mfsdp_test_inject_stall.argtypes = [_i32]
+_lib.mfsdp_test_inject_stall.restype = ctypes.c_int
 _lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _d, _d, _d, _d, _d, _i64, _vp]
 _lib.mfsdp_adamw_tail_step.restype = ctypes.c_int
 _lib.mfsdp_status_string.argtypes = [ctypes.c_int]
@@ -364,6 +366,13 @@ def muon_owner_step_static_scratch(shards: Sequence[MatrixShard], grad, momentum
                                                      int(bool(nesterov)), int(ns_steps), float(a), float(b), float(c),
                                                      float(eps), _stream(stream)),
            "muon_owner_step_static_scratch")
+
+
+def test_inject_stall(tile: int) -> None:
+    """Testing only: the next Newton-Schulz launch's tile `tile` waits for a
+    dependency that is never satisfied, so its bounded wait runs out (see
+    include/mfsdp.h)."""
+    _check(_lib.mfsdp_test_inject_stall(int(tile)), "test_inject_stall")
 
 
 def muon_device_status(workspace, stream=None) -> Tuple[int, int]:

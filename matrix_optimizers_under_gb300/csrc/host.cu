@@ -16,6 +16,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -37,6 +38,10 @@ struct PhaseRange {
   PhaseRange(const PhaseRange&) = delete;
   PhaseRange& operator=(const PhaseRange&) = delete;
 };
+
+// Test hook (mfsdp_test_inject_stall): the tile whose dependency wait the next
+// Newton-Schulz launch makes unreachable, -1 for none.  One-shot.
+std::atomic<int32_t> g_stall_tile{-1};
 
 // Copy streams and events of the host-buffer step, per device.
 constexpr int kMaxPipeDevices = 64;
@@ -654,6 +659,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
     nb.iter_tiles = off;
     nb.tile_begin = 0;
     nb.tile_end = off * ns_steps;
+    nb.stall_tile = g_stall_tile.exchange(-1);
     st = cuda_status(cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(n_shards + 1), stream));
     if (st != MFSDP_OK) return st;
     st = cuda_status(launch_ns(nb, L.bytes, stream));
@@ -681,6 +687,12 @@ extern "C" int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n
   }
   *dense = dn;
   *executed = ex;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_test_inject_stall(int32_t tile) {
+  if (tile < 0) return MFSDP_ERR_INVALID_ARG;
+  g_stall_tile.store(tile);
   return MFSDP_OK;
 }
 

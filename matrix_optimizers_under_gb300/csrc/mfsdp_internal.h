@@ -116,6 +116,7 @@ struct NsBatch {
   int32_t ns_steps;
   int32_t phase_begin, phase_end;
   int32_t tile_begin, tile_end;
+  int32_t stall_tile;    // test hook: this tile's dependency target is never reached (-1: none)
   int32_t iter_tiles;    // tiles of one iteration (three products, all matrices)
   int32_t mode_start[3];
   int32_t out_bf16;      // final update dtype

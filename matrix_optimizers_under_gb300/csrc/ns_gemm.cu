@@ -79,6 +79,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <mutex>
 
 #include "mfsdp_internal.h"
@@ -724,8 +725,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (t > p.tile_end) t = p.tile_end;           // the end marker
           if (t < p.tile_end) {
             const Tile tl = decode_tile(p, t, 0);
-            if (!tl.zero && tl.need > 0 &&
-                !wait_done(p.done + tl.mi, tl.need, abort_v, p.status, wait_code(tl.phase, kRoleDependency)))
+            const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
+            if (!tl.zero && need > 0 &&
+                !wait_done(p.done + tl.mi, need, abort_v, p.status, wait_code(tl.phase, kRoleDependency)))
               break;
           }
           if (!pair_publish(pair, seq, t, abort_v, p.status)) break;

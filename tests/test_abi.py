@@ -235,3 +235,7 @@ def test_newton_schulz_index_limits(mfsdp):
     assert step(mfsdp, wide, numel=16384 << 24, ns=5, wsb=1 << 62) == mfsdp.ERR_UNSUPPORTED_SHAPE
     # the same shape with a workspace that is too small still reports the shape first
     assert step(mfsdp, wide, numel=16384 << 24, ns=5, wsb=1 << 20) == mfsdp.ERR_UNSUPPORTED_SHAPE
+
+
+def test_inject_stall_rejects_negative_tile(mfsdp):
+    assert mfsdp.raw_lib().mfsdp_test_inject_stall(-1) == mfsdp.ERR_INVALID_ARG

@@ -1,0 +1,61 @@
+"""Failure detection on the GPU without a fault: a bounded wait runs out.
+
+The test hook makes one tile of the next Newton-Schulz launch wait for a
+dependency that nothing satisfies.  The first wait on it to pass its 2 s limit
+(the scheduler's, or its pair's roles waiting to be handed that tile) records
+the status word.  Every other wait of every CTA sees
+the word and stops, so the kernel ends in bounded time.  The host reads
+MFSDP_ERR_DEVICE_TIMEOUT with the waiting role and product in the detail
+word.  The context stays usable: the next step succeeds and matches the
+oracle.
+"""
+import time
+
+import numpy as np
+import pytest
+
+from matrix_optimizers_under_gb300 import workloads as W
+from tests import helpers as H
+from tests.test_gpu_parity import check_matrix, run_step
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ROLE_DEPENDENCY = 5   # the scheduler's wait for the stalled tile's dependency
+ROLE_TILE_FULL = 8    # a role of the stalled pair waiting for that tile to be handed out
+
+
+def test_bounded_wait_gives_up_and_reports(mfsdp):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    w = W.get("tiny")
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan)
+    shards, numel = plan.rank_matrices(r), plan.rank_matrix_elems[r]
+    grad_np = H.build_grad_buffer(w, shards, numel)
+    grad = torch.from_numpy(grad_np.view(np.int16) if grad_np.dtype == np.uint16 else grad_np).to(dev)
+    if grad_np.dtype == np.uint16:
+        grad = grad.view(torch.bfloat16)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+
+    mfsdp.test_inject_stall(0)                     # the first tile of the next launch
+    t0 = time.monotonic()
+    mfsdp.muon_owner_step(shards, grad, mom, upd, ws, ns_steps=w.ns_steps, coeffs=W.NS_COEFFS, eps=W.NS_EPS)
+    st, detail = mfsdp.muon_device_status(ws)      # synchronises
+    waited = time.monotonic() - t0
+    assert st == mfsdp.ERR_DEVICE_TIMEOUT, (st, detail)
+    # Both waits hang on the stalled tile; the readers of its pair start
+    # waiting first, so either may be the first to run out.
+    assert detail & 0xFF in (ROLE_DEPENDENCY, ROLE_TILE_FULL), detail
+    # the first wait to run out records its product: the stalled tile's (0),
+    # or a later product of the same matrix whose wait started a little earlier
+    assert 0 <= detail >> 8 < 3 * w.ns_steps, detail
+    assert 1.5 < waited < 30.0, waited
+
+    # The context is still usable and the hook has cleared itself.
+    upd_np, mom_np, _ = run_step(mfsdp, shards, grad_np, np.zeros(numel, np.float32), update_dtype=torch.float32)
+    for s in shards:
+        check_matrix(s, upd_np, mom_np, grad_np, np.zeros(numel, np.float32), ns_steps=w.ns_steps)
