@@ -51,7 +51,7 @@ NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_ra
                    ("0.7.0", "llama3_8b_rank"): 50.17e9, ("0.8.1", "llama3_8b_rank"): 50.02e9,
                    ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
                    ("0.8.4", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.5", "llama3_8b_rank"): 50.58e9}
+                   ("0.8.5", "llama3_8b_rank"): 50.58e9, ("0.8.6", "llama3_8b_rank"): 50.08e9}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -495,6 +495,85 @@ def run_ours(args):
     return 0
 
 
+def run_kernel_case(args):
+    """One memory-bound kernel alone, on a case small enough for a full ncu
+    capture (a few GB on the device) but larger than L2: K timed launches after
+    W warm-up ones, CUDA events on the launching stream.  Prints one JSON line
+    with the kernel's algorithmic GB/s against the measured HBM peak.
+
+    adamw:          the fused AdamW kernel over a 50M-element fp32 tail (the
+                    skewed MoE owner set's tail), 28 bytes per element.
+    segment_reduce: the owner-segment reduce of a three-layer Llama-1.3B-shaped
+                    stack (d = 2048, ffn = 5504) planned over 8 simulated ranks:
+                    the heaviest owner's matrix segments summed in rank order
+                    from the 8 ranks' bf16 model-layout buffers, 2 bytes per
+                    element per source plus 2 written.
+    """
+    from matrix_optimizers_under_gb300 import _build
+    _build.ensure_built()
+    from matrix_optimizers_under_gb300 import binding as mfsdp
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    if args.kernel == "adamw":
+        n = 50_000_000
+        bp = torch.randn(n, device=dev, generator=gen) * 1e-3
+        bg = torch.randn(n, device=dev, generator=gen) * 1e-3
+        bm, bv = torch.zeros_like(bp), torch.zeros_like(bp)
+        count = [0]
+
+        def launch():
+            count[0] += 1
+            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=count[0])
+        moved = 28 * n
+        case = {"kernel": "adamw_kernel", "elements": n, "dtype": "f32"}
+    else:
+        world = 8
+        table = W.llama_param_table(3, 2048, 5504, 2048)
+        plan = mfsdp.plan_owners(table, world, 5, 128)
+        owner = heaviest_rank(plan)
+        model = mfsdp.model_placements(table, 128)
+        _, model_total = mfsdp.model_layout(table, 128)
+        mp, _ = mfsdp.placements(plan)
+        segs = mfsdp.placement_segments(model, mp, owner)
+        srcs = [(torch.randn(model_total, device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+                for _ in range(world)]
+        dst = torch.empty(plan.rank_matrix_elems[owner], dtype=torch.bfloat16, device=dev)
+
+        def launch():
+            mfsdp.segment_copy(srcs, segs, mfsdp.SEGMENT_REDUCE, dst)
+        owned = sum(g.numel for g in segs)
+        moved = owned * 2 * (world + 1)
+        case = {"kernel": "segment_kernel", "mode": "reduce", "ranks": world, "segments": len(segs),
+                "elements": owned, "model_elements": model_total, "dtype": "bf16"}
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.4)
+    e0.record(stream)
+    for _ in range(args.steps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks, peak_src = load_peaks()
+    gbs = moved / (ms * 1e-3) / 1e9
+    print(json.dumps({"kernel_case": args.kernel, "metric": "algorithmic HBM GB/s", "value": round(gbs, 1),
+                      "unit": "GB/s", "ms_per_launch": round(ms, 4), "launches": args.steps, "warmup": args.warmup,
+                      "bytes_per_launch": moved, "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                      "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src, "config": case,
+                      "l2": f"no flush: {moved / 1e9:.2f} GB moved per launch > 129 MB L2",
+                      "clocks": clocks, "library": mfsdp.version()}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -506,9 +585,13 @@ def main(argv=None):
     ap.add_argument("--no-supplementary", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=4,
                     help="shard groups the host-buffer step overlaps copies with (1 = no overlap)")
+    ap.add_argument("--kernel", choices=("adamw", "segment_reduce"), default=None,
+                    help="time one memory-bound kernel alone on a small case instead of the owner step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.kernel:
+        return run_kernel_case(args)
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 

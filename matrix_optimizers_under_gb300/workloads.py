@@ -121,6 +121,11 @@ def _llama(layers: int, d: int, ffn: int, kv: int, vocab: Optional[int]) -> List
     return p
 
 
+def llama_param_table(layers: int, d: int, ffn: int, kv: int) -> List[Tuple[int, int, int]]:
+    """(rows, cols, kind) of a Llama-style layer stack without embedding or head."""
+    return [(p.rows, p.cols, p.kind) for p in _llama(layers, d, ffn, kv, None)]
+
+
 def _llama_1p3b() -> Workload:
     # 24 layers, d=2048, ffn=5504, no grouped-query attention stated, vocab 32000
     # untied embedding and head, both kept on AdamW.

@@ -1,0 +1,36 @@
+"""Host-side checks of the bench's single-kernel cases (no GPU).
+
+The owner-segment reduce case that the full ncu capture of `segment_kernel`
+runs on is a three-layer Llama-1.3B-shaped stack planned over 8 simulated
+ranks.  Its layout is fixed here so that the sizes the profile quotes (model
+elements per rank buffer, segments and elements of the heaviest owner) stay
+true, and so that the case covers exactly that owner's matrices (MatrixFSDP --
+Abstract: each owner holds whole matrices, described by offset, rows, cols).
+"""
+import pytest
+
+import bench
+from matrix_optimizers_under_gb300 import workloads as W
+
+
+def test_segment_case_layout(mfsdp):
+    table = W.llama_param_table(3, 2048, 5504, 2048)
+    assert len(table) == 3 * 9 + 1
+    plan = mfsdp.plan_owners(table, 8, 5, 128)
+    owner = bench.heaviest_rank(plan)
+    model = mfsdp.model_placements(table, 128)
+    _, model_total = mfsdp.model_layout(table, 128)
+    mp, _ = mfsdp.placements(plan)
+    segs = mfsdp.placement_segments(model, mp, owner)
+    owned = sum(s.numel for s in segs)
+    # Every matrix of the owner, and nothing else, lands in its flat buffer.
+    mine = [s for s in plan.matrix_shards if s.owner == owner]
+    assert owned == sum(s.rows * s.cols for s in mine) == plan.rank_matrix_elems[owner]
+    assert (model_total, len(segs), owned) == (151_795_712, 2, 22_544_384)
+    # 8 bf16 sources read and one bf16 destination written per element.
+    assert owned * 2 * 9 == 405_798_912
+
+
+def test_kernel_case_flag_choices():
+    with pytest.raises(SystemExit):
+        bench.main(["--kernel", "momentum"])
