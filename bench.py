@@ -51,7 +51,9 @@ NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_ra
                    ("0.7.0", "llama3_8b_rank"): 50.17e9, ("0.8.1", "llama3_8b_rank"): 50.02e9,
                    ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
                    ("0.8.4", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.5", "llama3_8b_rank"): 50.58e9, ("0.8.6", "llama3_8b_rank"): 50.08e9}
+                   ("0.8.5", "llama3_8b_rank"): 50.58e9, ("0.8.6", "llama3_8b_rank"): 50.08e9,
+                   # 0.8.7 changed only the host-buffer entry's grouping: ns_kernel is 0.8.6's
+                   ("0.8.7", "llama3_8b_rank"): 50.08e9}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -345,6 +347,7 @@ def run_ours(args):
     # overlapped with the compute of the neighbouring groups; the AdamW tail's
     # gradient comes in and its parameters go back out too.
     e2e_steps = max(1, min(args.steps, 5))
+    e2e_groups = mfsdp.host_step_groups(shards, grad.dtype, upd.dtype, args.e2e_groups)[0]
     h2d = grad_host.numel() * grad_host.element_size() + (tg_host.numel() * 4 if tail_numel else 0)
     d2h = upd_host.numel() * 2 + (tp_host.numel() * 4 if tail_numel else 0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -482,7 +485,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
-                "pipeline_groups": args.e2e_groups, "steps_ms": e2e_steps_ms},
+                "pipeline_groups": e2e_groups, "steps_ms": e2e_steps_ms},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,
@@ -583,8 +586,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b_rank", choices=W.ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-supplementary", action="store_true")
-    ap.add_argument("--e2e-groups", type=int, default=4,
-                    help="shard groups the host-buffer step overlaps copies with (1 = no overlap)")
+    ap.add_argument("--e2e-groups", type=int, default=0,
+                    help="shard groups the host-buffer step overlaps copies with (1 = no overlap, "
+                         "0 = the library's choice for the owner set)")
     ap.add_argument("--kernel", choices=("adamw", "segment_reduce"), default=None,
                     help="time one memory-bound kernel alone on a small case instead of the owner step")
     args = ap.parse_args(argv)

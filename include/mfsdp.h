@@ -213,24 +213,24 @@ int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int32_t n_shar
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* The owner step with the gradient coming from, and the update going to,
- * pinned host memory.  The shards are cut, in offset order, into `groups`
- * groups of roughly equal Newton-Schulz cost; group g's gradient range is
- * copied host->device on an internal stream while group g-1 computes on
- * `stream`, and its update range is copied device->host on another internal
- * stream while group g+1 computes.  Each group runs the same kernels as
+ * pinned host memory.  The shards are cut into groups (mfsdp_host_step_groups);
+ * group g's gradient ranges are copied host->device on an internal stream
+ * while the groups before it compute on `stream`, and its update ranges are
+ * copied device->host on another internal stream while later groups compute.  Each group runs the same kernels as
  * mfsdp_muon_owner_step on its own shards (results are bit-identical).
  *   grad_host / update_host  pinned host buffers (cudaHostAlloc / registered),
  *                            numel elements of grad_dtype / update_dtype.
  *   grad_dev / update_dev    device staging buffers of numel elements; every
  *                            other argument as for mfsdp_muon_owner_step.
- *   groups >= 1 (1 = no overlap).
+ *   groups >= 1 (1 = no overlap), or 0: the library's choice; both as
+ *                            mfsdp_host_step_groups describes.
  * The call returns once everything is queued; work queued on `stream` later
  * runs after the last copy.  The two copy streams and their events belong to
  * the library: created on a device's first call and kept until the process
  * exits.  Calls on one device enqueue one at a time (a lock held while
  * queuing, not while the GPU works) and their copies run in call order.
  * Errors: as mfsdp_muon_owner_step, plus INVALID_ARG for a NULL host buffer
- * or groups < 1, and CUDA when the current device's index is 64 or more. */
+ * or groups < 0, and CUDA when the current device's index is 64 or more. */
 int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards,
                                const void* grad_host, void* grad_dev, int32_t grad_dtype,
                                float* momentum,
@@ -239,6 +239,29 @@ int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shard
                                double beta, int32_t nesterov, int32_t ns_steps,
                                double a, double b, double c, double eps,
                                void* workspace, size_t workspace_bytes, int32_t groups, void* stream);
+
+/* The shard groups of the host-buffer step (no counterpart in the paper: a
+ * property of this library's copy pipeline).  Returns the number of groups
+ * mfsdp_muon_owner_step_host runs for these arguments and, when group_of is
+ * not NULL, writes each shard's group (0 = first to run) to group_of[0..n).
+ *   groups >= 1  shards in offset order, cut into min(groups, n) ranges of
+ *                balanced Newton-Schulz cost (empty ranges dropped).
+ *   groups == 0  chosen from the copy volume B = sum of rows * cols * (grad +
+ *                update element size).  Copies stay exposed only at the two
+ *                ends; each group past the first costs some compute (up to
+ *                one latency-bound Newton-Schulz chain, ~0.25 ms, when a group
+ *                is too small to fill the GPU).  With g = round(sqrt(B / 50 MB)):
+ *                g <= 1 one group; g == 2, g >= 6 or fewer than 5 shards:
+ *                min(g, 16, n) balanced ranges; 3 <= g <= 5: a ramp -- shards
+ *                ordered small -> large -> small by size and cut at 4 %, 28 %,
+ *                72 % and 96 % of B (a shard goes where the midpoint of its
+ *                bytes falls), so the first copy in and the last copy out are
+ *                small while the groups stay few.
+ * A group's copies are the runs of its shards that neighbour each other in
+ * offset order.  Host only: no device is touched.  Returns 0 for NULL shards,
+ * n_shards <= 0, groups < 0 or a dtype other than F32 / BF16. */
+int32_t mfsdp_host_step_groups(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t grad_dtype,
+                               int32_t update_dtype, int32_t groups, int32_t* group_of);
 
 /* mfsdp_muon_owner_step for callers that cannot allocate device memory (no
  * counterpart in the paper: an addition of this library).  Some callers have

@@ -40,7 +40,8 @@ EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner
             "mfsdp_muon_device_status", "mfsdp_muon_workspace_layout", "mfsdp_adamw_tail_step",
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
             "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
-            "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall")
+            "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall",
+            "mfsdp_host_step_groups")
 
 SEGMENT_REDUCE = 0
 SEGMENT_GATHER = 1
@@ -94,6 +95,9 @@ _lib.mfsdp_muon_owner_step_phases.restype = ctypes.c_int
 _lib.mfsdp_muon_owner_step_host.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _vp, _i32, _vp, _vp, _vp, _i32,
                                             _i64, _d, _i32, _i32, _d, _d, _d, _d, _vp, _sz, _i32, _vp]
 _lib.mfsdp_muon_owner_step_host.restype = ctypes.c_int
+_lib.mfsdp_host_step_groups.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, _i32, _i32,
+                                        ctypes.POINTER(_i32)]
+_lib.mfsdp_host_step_groups.restype = _i32
 _lib.mfsdp_muon_owner_step_apply.argtypes = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _vp, _i32,
                                              _i64, _d, _i32, _i32, _d, _d, _d, _d, _d, _d, _i32, _vp, _sz, _vp]
 _lib.mfsdp_muon_owner_step_apply.restype = ctypes.c_int
@@ -333,13 +337,13 @@ def muon_owner_step_apply(shards: Sequence[MatrixShard], grad, momentum, update,
 
 
 def muon_owner_step_host(shards: Sequence[MatrixShard], grad_host, grad_dev, momentum, update_dev, update_host,
-                         workspace, *, groups: int = 4, beta: float = 0.95, nesterov: bool = False,
+                         workspace, *, groups: int = 0, beta: float = 0.95, nesterov: bool = False,
                          ns_steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315), eps: float = 1e-7,
                          numel: Optional[int] = None, stream=None) -> None:
     """The owner step with the gradient read from and the update written to pinned
     host tensors, the copies of each shard group overlapped with the compute of
     its neighbours (see include/mfsdp.h).  grad_dev/update_dev are device staging
-    tensors of the same length."""
+    tensors of the same length.  groups = 0: the count host_step_groups gives."""
     arr = _shard_array(shards)
     n = int(numel if numel is not None else grad_dev.numel())
     a, b, c = coeffs
@@ -350,6 +354,21 @@ def muon_owner_step_host(shards: Sequence[MatrixShard], grad_host, grad_dev, mom
                                            int(workspace.numel() if workspace is not None else 0), int(groups),
                                            _stream(stream)),
            "muon_owner_step_host")
+
+
+def host_step_groups(shards: Sequence[MatrixShard], grad_dtype=None, update_dtype=None,
+                     groups: int = 0) -> Tuple[int, List[int]]:
+    """(number of groups, each shard's group) of the host-buffer step for
+    `groups` (0 = the library's choice); host only.  The dtypes are torch
+    dtypes, bf16 gradient and update by default."""
+    import torch
+    g = torch.bfloat16 if grad_dtype is None else grad_dtype
+    u = torch.bfloat16 if update_dtype is None else update_dtype
+    code = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
+    out = (_i32 * max(len(shards), 1))()
+    ng = int(_lib.mfsdp_host_step_groups(_shard_array(shards), len(shards), code.get(g, 99), code.get(u, 99),
+                                         int(groups), out))
+    return ng, [int(out[i]) for i in range(len(shards))] if ng else []
 
 
 def muon_owner_step_static_scratch(shards: Sequence[MatrixShard], grad, momentum, update, *, beta: float = 0.95,

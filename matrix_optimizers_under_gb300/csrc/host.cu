@@ -229,7 +229,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.6"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.7"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -368,13 +368,110 @@ extern "C" int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int
                          &ap);
 }
 
+namespace {
+
+// Shard groups of the host-buffer step, in execution order; group_of[i] is
+// shard i's group.  groups >= 1: shards in offset order, cut where the
+// running Newton-Schulz cost crosses k/groups of the total (one contiguous
+// range of the flat buffers per group, compute balanced).  groups == 0: the
+// copy volume decides (mfsdp_host_step_groups).  Only the first copy in and
+// the last copy out are exposed; every group past the first costs a little
+// compute.  Large sets (g >= 6) split into g balanced groups: each still fills
+// the GPU, so more groups only shorten the exposed ends.  Mid-sized sets
+// (3 <= g <= 5) take a ramp -- shards ordered small -> large -> small by size
+// and cut at 4 %, 28 %, 72 % and 96 % of the bytes -- which makes the two
+// exposed copies small with five groups, where balanced groups of a few
+// matrices would leave most of the GPU idle.
+int plan_host_groups(const mfsdp_matrix_shard* shards, int n, int groups, size_t elem_bytes,
+                     std::vector<int>& group_of) {
+  group_of.assign(n, 0);
+  if (n <= 0) return 1;
+  if (groups == 0) {
+    double bytes = 0.0;
+    for (int i = 0; i < n; ++i) bytes += (double)shards[i].rows * (double)shards[i].cols * (double)elem_bytes;
+    const long g = std::lround(std::sqrt(bytes / 50e6));
+    if (g <= 1) return 1;
+    if (g <= 2 || g >= 6 || n < 5) {
+      groups = (int)std::min<long>(std::min<long>(g, 16), n);
+    } else {
+      std::vector<int> by(n);
+      for (int i = 0; i < n; ++i) by[i] = i;
+      std::sort(by.begin(), by.end(), [&](int x, int y) {
+        const int64_t nx = shards[x].rows * shards[x].cols, ny = shards[y].rows * shards[y].cols;
+        return nx != ny ? nx < ny : shards[x].offset < shards[y].offset;
+      });
+      // small -> large: the even positions; large -> small: the odd ones reversed
+      std::vector<int> seq;
+      for (int k = 0; k < n; k += 2) seq.push_back(by[k]);
+      for (int k = (n % 2 == 0) ? n - 1 : n - 2; k >= 1; k -= 2) seq.push_back(by[k]);
+      const double cuts[4] = {0.04, 0.28, 0.72, 0.96};
+      std::vector<int> slot(n);
+      bool used[5] = {false, false, false, false, false};
+      double run = 0.0;
+      for (int i : seq) {
+        const double b = (double)shards[i].rows * (double)shards[i].cols * (double)elem_bytes;
+        const double mid = (run + 0.5 * b) / bytes;     // a shard goes where its midpoint falls
+        int k = 0;
+        while (k < 4 && cuts[k] <= mid) ++k;
+        slot[i] = k;
+        used[k] = true;
+        run += b;
+      }
+      int remap[5], ng = 0;                               // a large shard can leave a slot empty
+      for (int k = 0; k < 5; ++k) remap[k] = used[k] ? ng++ : -1;
+      for (int i = 0; i < n; ++i) group_of[i] = remap[slot[i]];
+      return ng;
+    }
+  }
+  std::vector<int> ord(n);
+  for (int i = 0; i < n; ++i) ord[i] = i;
+  std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
+  std::vector<double> cost(n);
+  double total = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const double sm = (double)std::min(shards[i].rows, shards[i].cols);
+    const double l = (double)std::max(shards[i].rows, shards[i].cols);
+    cost[i] = 4.0 * sm * sm * l + 2.0 * sm * sm * sm + sm * l;   // + s*l: the momentum pass
+    total += cost[i];
+  }
+  const int ng = std::min(groups, n);
+  std::vector<int> used(ng, 0);
+  double run = 0.0;
+  for (int k = 0; k < n; ++k) {
+    const int i = ord[k];
+    int g = total > 0.0 ? (int)(run / total * ng) : 0;
+    g = std::min(std::max(g, 0), ng - 1);
+    group_of[i] = g;
+    used[g] = 1;
+    run += cost[i];
+  }
+  std::vector<int> remap(ng);
+  int nz = 0;
+  for (int g = 0; g < ng; ++g) remap[g] = used[g] ? nz++ : -1;
+  for (int i = 0; i < n; ++i) group_of[i] = remap[group_of[i]];
+  return nz;
+}
+
+}  // namespace
+
+extern "C" int32_t mfsdp_host_step_groups(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t grad_dtype,
+                                          int32_t update_dtype, int32_t groups, int32_t* group_of) {
+  const auto known = [](int32_t dt) { return dt == MFSDP_DTYPE_F32 || dt == MFSDP_DTYPE_BF16; };
+  if (!shards || n_shards <= 0 || groups < 0 || !known(grad_dtype) || !known(update_dtype)) return 0;
+  std::vector<int> gof;
+  const int ng = plan_host_groups(shards, n_shards, groups, dtype_size(grad_dtype) + dtype_size(update_dtype), gof);
+  if (group_of)
+    for (int i = 0; i < n_shards; ++i) group_of[i] = gof[i];
+  return ng;
+}
+
 extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad_host,
                                           void* grad_dev, int32_t grad_dtype, float* momentum, void* update_dev,
                                           void* update_host, int32_t update_dtype, int64_t numel, double beta_d,
                                           int32_t nesterov, int32_t ns_steps, double a_d, double b_d, double c_d,
                                           double eps_d, void* workspace, size_t workspace_bytes, int32_t groups,
                                           void* stream_ptr) {
-  if (groups < 1) return MFSDP_ERR_INVALID_ARG;
+  if (groups < 0) return MFSDP_ERR_INVALID_ARG;
   Layout L;
   int st = validate_step(shards, n_shards, grad_dev, grad_dtype, momentum, update_dev, update_dtype, numel, beta_d,
                          nesterov, ns_steps, a_d, b_d, c_d, eps_d, workspace, workspace_bytes, &L);
@@ -383,28 +480,22 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
   const float beta = (float)beta_d, a = (float)a_d, b = (float)b_d, c = (float)c_d, eps = (float)eps_d;
   const size_t gsz = dtype_size(grad_dtype), usz = dtype_size(update_dtype);
 
-  // Groups: shards in offset order, cut where the running Newton-Schulz cost
-  // crosses k/groups of the total, so the groups' compute is balanced and each
-  // group's segments form one contiguous range of the flat buffers.
+  // Groups (in execution order) and, per group, the element ranges to copy:
+  // runs of its shards that are neighbours in offset order, so a group whose
+  // shards are contiguous in the flat buffers costs one copy each way.
+  std::vector<int> gof;
+  const int ng = plan_host_groups(shards, n_shards, groups, gsz + usz, gof);
+  std::vector<std::vector<mfsdp_matrix_shard>> grp(ng);
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> runs(ng);
   std::vector<int> ord(n_shards);
   for (int i = 0; i < n_shards; ++i) ord[i] = i;
   std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
-  std::vector<double> cost(n_shards);
-  double total = 0.0;
-  for (int i = 0; i < n_shards; ++i) {
-    const double s = (double)std::min(shards[i].rows, shards[i].cols), l = (double)std::max(shards[i].rows, shards[i].cols);
-    cost[i] = 4.0 * s * s * l + 2.0 * s * s * s + s * l;   // + s*l: the momentum pass
-    total += cost[i];
-  }
-  const int ng = std::min<int>(groups, n_shards);
-  std::vector<std::vector<mfsdp_matrix_shard>> grp(ng);
-  double run = 0.0;
   for (int k = 0; k < n_shards; ++k) {
-    const int i = ord[k];
-    int g = (int)(run / total * ng);
-    g = std::min(std::max(g, 0), ng - 1);
+    const int i = ord[k], g = gof[i];
+    const int64_t lo = shards[i].offset, hi = lo + shards[i].rows * shards[i].cols;
     grp[g].push_back(shards[i]);
-    run += cost[i];
+    if (k > 0 && gof[ord[k - 1]] == g) runs[g].back().second = std::max(runs[g].back().second, hi);
+    else runs[g].push_back({lo, hi});
   }
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -437,15 +528,13 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
     const std::vector<mfsdp_matrix_shard>& sh = grp[g];
     if (sh.empty()) continue;
     const PhaseRange range("mfsdp host-buffer group");
-    int64_t lo = sh.front().offset, hi = 0;
-    for (const auto& x : sh) {
-      lo = std::min(lo, x.offset);
-      hi = std::max(hi, x.offset + x.rows * x.cols);
-    }
     cudaEvent_t e_in = ev[1 + 3 * g], e_done = ev[2 + 3 * g], e_out = ev[3 + 3 * g];
-    ce = cudaMemcpyAsync(static_cast<uint8_t*>(grad_dev) + (size_t)lo * gsz,
-                         static_cast<const uint8_t*>(grad_host) + (size_t)lo * gsz, (size_t)(hi - lo) * gsz,
-                         cudaMemcpyHostToDevice, s_in);
+    for (size_t r = 0; r < runs[g].size() && ce == cudaSuccess; ++r) {
+      const int64_t lo = runs[g][r].first, hi = runs[g][r].second;
+      ce = cudaMemcpyAsync(static_cast<uint8_t*>(grad_dev) + (size_t)lo * gsz,
+                           static_cast<const uint8_t*>(grad_host) + (size_t)lo * gsz, (size_t)(hi - lo) * gsz,
+                           cudaMemcpyHostToDevice, s_in);
+    }
     if (ce == cudaSuccess) ce = cudaEventRecord(e_in, s_in);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, e_in, 0);
     if (ce != cudaSuccess) break;
@@ -459,10 +548,12 @@ extern "C" int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int3
     if (st != MFSDP_OK) break;
     ce = cudaEventRecord(e_done, stream);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s_out, e_done, 0);
-    if (ce == cudaSuccess)
+    for (size_t r = 0; r < runs[g].size() && ce == cudaSuccess; ++r) {
+      const int64_t lo = runs[g][r].first, hi = runs[g][r].second;
       ce = cudaMemcpyAsync(static_cast<uint8_t*>(update_host) + (size_t)lo * usz,
                            static_cast<const uint8_t*>(update_dev) + (size_t)lo * usz, (size_t)(hi - lo) * usz,
                            cudaMemcpyDeviceToHost, s_out);
+    }
     if (ce == cudaSuccess) ce = cudaEventRecord(e_out, s_out);
   }
   // `stream` ends after every copy out.  The waits come after the loop: inside

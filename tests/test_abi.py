@@ -162,7 +162,7 @@ def test_host_entry_error_paths(mfsdp):
     def call(gh=H1, uh=H2, groups=4, grad=G, ws=WS):
         return lib.mfsdp_muon_owner_step_host(arr, 1, gh, grad, BF, M, U, uh, BF, 1 << 20, 0.95, 0, 5, 3.4445,
                                               -4.775, 2.0315, 1e-7, ws, wsb, groups, None)
-    assert call(groups=0) == mfsdp.ERR_INVALID_ARG
+    assert call(groups=-1) == mfsdp.ERR_INVALID_ARG
     assert call(gh=None) == mfsdp.ERR_INVALID_ARG
     assert call(uh=None) == mfsdp.ERR_INVALID_ARG
     assert call(grad=G + 2) == mfsdp.ERR_MISALIGNED
@@ -239,3 +239,48 @@ def test_newton_schulz_index_limits(mfsdp):
 
 def test_inject_stall_rejects_negative_tile(mfsdp):
     assert mfsdp.raw_lib().mfsdp_test_inject_stall(-1) == mfsdp.ERR_INVALID_ARG
+
+
+def test_host_step_groups(mfsdp):
+    """groups = 0: g = round(sqrt(copy bytes / 50 MB)); one group for g <= 1,
+    cost-balanced offset ranges for g == 2, g >= 6 or fewer than 5 shards,
+    else the ramp (small -> large -> small by size, cut at 4/28/72/96 % of the
+    bytes, a shard placed by the midpoint of its bytes).  groups >= 1: offset
+    ranges of balanced cost 4 s^2 l + 2 s^3 + s l.  Expected values worked by
+    hand."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+
+    def layout(dims):
+        out, off = [], 0
+        for i, (r, c) in enumerate(dims):
+            out.append(mfsdp.make_shard(off, r, c, param_id=i))
+            off += r * c
+        return out
+
+    assert mfsdp.host_step_groups(layout([(5000, 5000)]), bf, bf) == (1, [0])          # 100 MB: g = 1
+    four = layout([(8192, 8192)] * 4)                                  # 1.07 GB: g = 5, but 4 shards
+    assert mfsdp.host_step_groups(four, bf, bf) == (4, [0, 1, 2, 3])
+    three = layout([(4096, 4096)] * 3)                                 # 201 MB: g = 2
+    assert mfsdp.host_step_groups(three, bf, bf) == (2, [0, 0, 1])
+    # 499 MB, g = 3: the ramp.  By size s0 < s5 < s1 < s2 < s3 < s4, so the
+    # sequence is s0 s1 s3 | s4 s2 s5; byte midpoints at 0.4, 2.5, 17.6, 58.0,
+    # 91.6 and 99.2 % of the total.
+    six = layout([(1024, 1024), (2048, 2048), (4096, 4096), (4096, 8192), (8192, 8192), (1024, 2048)])
+    assert mfsdp.host_step_groups(six, bf, bf) == (5, [0, 0, 3, 1, 2, 4])
+    eight = layout([(8192, 8192)] * 8)                                 # 2.15 GB: g = 7, balanced
+    assert mfsdp.host_step_groups(eight, bf, bf) == (7, [0, 0, 1, 2, 3, 4, 5, 6])
+    many = layout([(8192, 8192)] * 40)                                 # 10.7 GB: g = 15
+    assert mfsdp.host_step_groups(many, bf, bf)[0] == 15
+    assert mfsdp.host_step_groups(many, f32, f32)[0] == 16            # 21.5 GB: g = 21, capped
+    # explicit groups: s4 holds 74 % of the cost, so the cut falls after it
+    assert mfsdp.host_step_groups(six, bf, bf, groups=2) == (2, [0, 0, 0, 0, 0, 1])
+    assert mfsdp.host_step_groups(six, bf, bf, groups=1) == (1, [0] * 6)
+    assert mfsdp.host_step_groups(three, f32, f32, groups=16) == (3, [0, 1, 2])
+    # fp32 gradients: 6 bytes per element -> 749 MB, g = 4: still the ramp
+    assert mfsdp.host_step_groups(six, f32, bf)[0] == 5
+    for bad in (dict(groups=-1), dict(grad_dtype=torch.float16), dict(update_dtype=torch.int32)):
+        kw = dict(grad_dtype=bf, update_dtype=bf, groups=0)
+        kw.update(bad)
+        assert mfsdp.host_step_groups(six, **kw) == (0, [])
+    assert mfsdp.host_step_groups([], bf, bf) == (0, [])

@@ -268,7 +268,43 @@ def test_phase_split_matches_full_step(mfsdp):
     assert np.array_equal(mom.cpu().numpy(), m1)
 
 
-@pytest.mark.parametrize("groups", [1, 2, 3, 8])
+def test_host_buffer_ramp_matches_resident_step(mfsdp):
+    """The library's own group choice on a set large enough for the
+    small -> large -> small ramp (the 1.3B rank: 5 groups, shards out of offset
+    order, several copy runs per group): update and momentum bit-identical to
+    the resident step, and the staging buffers hold exactly the copied
+    gradient."""
+    dev = _dev()
+    w = W.get("llama_1p3b_rank")
+    plan, r, shards, numel = owner_set(mfsdp, w)
+    ng, gof = mfsdp.host_step_groups(shards)
+    assert ng == 5 and sorted(set(gof)) == list(range(5))
+    order = sorted(range(len(shards)), key=lambda i: shards[i].offset)
+    assert any(gof[order[k]] > gof[order[k + 1]] for k in range(len(order) - 1))   # not offset order
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(13)
+    g_dev = (torch.randn(numel, device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+    m0 = torch.randn(numel, device=dev, generator=gen) * 1e-3
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mom_ref, upd_ref = m0.clone(), torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    mfsdp.muon_owner_step(shards, g_dev, mom_ref, upd_ref, ws)
+    gh = g_dev.cpu().pin_memory()
+    uh = torch.full((numel,), float("nan"), dtype=torch.bfloat16).pin_memory()
+    gd = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
+    ud = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    mom = m0.clone()
+    mfsdp.muon_owner_step_host(shards, gh, gd, mom, ud, uh, ws, groups=0)
+    torch.cuda.synchronize()
+    assert mfsdp.muon_device_status(ws)[0] == mfsdp.OK
+    assert torch.equal(mom, mom_ref)
+    ref = upd_ref.cpu()
+    for s in shards:
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        assert torch.equal(uh[seg].view(torch.int16), ref[seg].view(torch.int16)), s.param_id
+        assert torch.equal(gd[seg], g_dev[seg]), s.param_id
+
+
+@pytest.mark.parametrize("groups", [0, 1, 2, 3, 8])
 def test_host_buffer_pipeline_matches_resident_step(mfsdp, groups):
     """Gradient from pinned host memory, update back to it, copies overlapped with
     compute group by group: bit-identical to the resident step."""
