@@ -22,6 +22,7 @@ ranks bracket the timed region).
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -324,11 +325,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    gc.collect()
+    gc.disable()            # no collector pause while the host enqueues the timed steps
     t_start.record(stream)
     for k in range(args.steps):
         one_step(evs[k])
     t_end.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -370,6 +374,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    gc.collect()
+    gc.disable()
     e0.record(stream)
     step_ev[0].record(stream)
     for k in range(e2e_steps):
@@ -377,6 +383,7 @@ def run_ours(args):
         step_ev[k + 1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
+    gc.enable()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_steps_ms = [round(step_ev[k].elapsed_time(step_ev[k + 1]), 3) for k in range(e2e_steps)]
 
