@@ -245,18 +245,23 @@ int mfsdp_muon_owner_step_host(const mfsdp_matrix_shard* shards, int32_t n_shard
  * mfsdp_muon_owner_step_host runs for these arguments and, when group_of is
  * not NULL, writes each shard's group (0 = first to run) to group_of[0..n).
  *   groups >= 1  shards in offset order, cut into min(groups, n) ranges of
- *                balanced Newton-Schulz cost (empty ranges dropped).
+ *                balanced Newton-Schulz cost 4 s^2 l + 2 s^3 + s l (empty
+ *                ranges dropped).
  *   groups == 0  chosen from the copy volume B = sum of rows * cols * (grad +
  *                update element size).  Copies stay exposed only at the two
  *                ends; each group past the first costs some compute (up to
  *                one latency-bound Newton-Schulz chain, ~0.25 ms, when a group
  *                is too small to fill the GPU).  With g = round(sqrt(B / 50 MB)):
- *                g <= 1 one group; g == 2, g >= 6 or fewer than 5 shards:
- *                min(g, 16, n) balanced ranges; 3 <= g <= 5: a ramp -- shards
- *                ordered small -> large -> small by size and cut at 4 %, 28 %,
- *                72 % and 96 % of B (a shard goes where the midpoint of its
- *                bytes falls), so the first copy in and the last copy out are
- *                small while the groups stay few.
+ *                g <= 1 one group; g == 2 or fewer than 5 shards: min(g, n)
+ *                balanced ranges; g >= 6: min(g, 16) balanced ranges between a
+ *                head and a tail group, each up to two of the smallest shards
+ *                with the largest short side (most work per byte) holding at
+ *                most 1 / (2 min(g, 16)) of the elements -- without such
+ *                shards for both ends, only the balanced ranges;
+ *                3 <= g <= 5: a ramp -- shards ordered small -> large -> small
+ *                by size and cut at 4 %, 28 %, 72 % and 96 % of B (a shard
+ *                goes where the midpoint of its bytes falls).  Both make the
+ *                first copy in and the last copy out small.
  * A group's copies are the runs of its shards that neighbour each other in
  * offset order.  Host only: no device is touched.  Returns 0 for NULL shards,
  * n_shards <= 0, groups < 0 or a dtype other than F32 / BF16. */

@@ -229,7 +229,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.7"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.8"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -370,86 +370,126 @@ extern "C" int mfsdp_muon_owner_step_apply(const mfsdp_matrix_shard* shards, int
 
 namespace {
 
-// Shard groups of the host-buffer step, in execution order; group_of[i] is
-// shard i's group.  groups >= 1: shards in offset order, cut where the
-// running Newton-Schulz cost crosses k/groups of the total (one contiguous
-// range of the flat buffers per group, compute balanced).  groups == 0: the
-// copy volume decides (mfsdp_host_step_groups).  Only the first copy in and
-// the last copy out are exposed; every group past the first costs a little
-// compute.  Large sets (g >= 6) split into g balanced groups: each still fills
-// the GPU, so more groups only shorten the exposed ends.  Mid-sized sets
-// (3 <= g <= 5) take a ramp -- shards ordered small -> large -> small by size
-// and cut at 4 %, 28 %, 72 % and 96 % of the bytes -- which makes the two
-// exposed copies small with five groups, where balanced groups of a few
-// matrices would leave most of the GPU idle.
-int plan_host_groups(const mfsdp_matrix_shard* shards, int n, int groups, size_t elem_bytes,
-                     std::vector<int>& group_of) {
-  group_of.assign(n, 0);
-  if (n <= 0) return 1;
-  if (groups == 0) {
-    double bytes = 0.0;
-    for (int i = 0; i < n; ++i) bytes += (double)shards[i].rows * (double)shards[i].cols * (double)elem_bytes;
-    const long g = std::lround(std::sqrt(bytes / 50e6));
-    if (g <= 1) return 1;
-    if (g <= 2 || g >= 6 || n < 5) {
-      groups = (int)std::min<long>(std::min<long>(g, 16), n);
-    } else {
-      std::vector<int> by(n);
-      for (int i = 0; i < n; ++i) by[i] = i;
-      std::sort(by.begin(), by.end(), [&](int x, int y) {
-        const int64_t nx = shards[x].rows * shards[x].cols, ny = shards[y].rows * shards[y].cols;
-        return nx != ny ? nx < ny : shards[x].offset < shards[y].offset;
-      });
-      // small -> large: the even positions; large -> small: the odd ones reversed
-      std::vector<int> seq;
-      for (int k = 0; k < n; k += 2) seq.push_back(by[k]);
-      for (int k = (n % 2 == 0) ? n - 1 : n - 2; k >= 1; k -= 2) seq.push_back(by[k]);
-      const double cuts[4] = {0.04, 0.28, 0.72, 0.96};
-      std::vector<int> slot(n);
-      bool used[5] = {false, false, false, false, false};
-      double run = 0.0;
-      for (int i : seq) {
-        const double b = (double)shards[i].rows * (double)shards[i].cols * (double)elem_bytes;
-        const double mid = (run + 0.5 * b) / bytes;     // a shard goes where its midpoint falls
-        int k = 0;
-        while (k < 4 && cuts[k] <= mid) ++k;
-        slot[i] = k;
-        used[k] = true;
-        run += b;
-      }
-      int remap[5], ng = 0;                               // a large shard can leave a slot empty
-      for (int k = 0; k < 5; ++k) remap[k] = used[k] ? ng++ : -1;
-      for (int i = 0; i < n; ++i) group_of[i] = remap[slot[i]];
-      return ng;
-    }
-  }
-  std::vector<int> ord(n);
-  for (int i = 0; i < n; ++i) ord[i] = i;
+// Balanced groups over the shards marked in `member`: offset order, cut where
+// the running Newton-Schulz cost crosses k/ng of their total, so each group
+// is one contiguous range of the flat buffers (apart from shards placed in
+// other groups) and the groups' compute is balanced.  Group ids start at
+// `first`; returns the number of non-empty groups.
+int balanced_groups(const mfsdp_matrix_shard* shards, int n, const std::vector<char>& member, int ng, int first,
+                    std::vector<int>& group_of) {
+  std::vector<int> ord;
+  for (int i = 0; i < n; ++i)
+    if (member[i]) ord.push_back(i);
+  if (ord.empty()) return 0;
   std::sort(ord.begin(), ord.end(), [&](int x, int y) { return shards[x].offset < shards[y].offset; });
-  std::vector<double> cost(n);
+  std::vector<double> cost(ord.size());
   double total = 0.0;
-  for (int i = 0; i < n; ++i) {
-    const double sm = (double)std::min(shards[i].rows, shards[i].cols);
-    const double l = (double)std::max(shards[i].rows, shards[i].cols);
-    cost[i] = 4.0 * sm * sm * l + 2.0 * sm * sm * sm + sm * l;   // + s*l: the momentum pass
-    total += cost[i];
+  for (size_t k = 0; k < ord.size(); ++k) {
+    const mfsdp_matrix_shard& sh = shards[ord[k]];
+    const double sm = (double)std::min(sh.rows, sh.cols), l = (double)std::max(sh.rows, sh.cols);
+    cost[k] = 4.0 * sm * sm * l + 2.0 * sm * sm * sm + sm * l;   // + s*l: the momentum pass
+    total += cost[k];
   }
-  const int ng = std::min(groups, n);
-  std::vector<int> used(ng, 0);
+  ng = std::min<int>(ng, (int)ord.size());
+  std::vector<int> slot(ord.size()), used(ng, 0);
   double run = 0.0;
-  for (int k = 0; k < n; ++k) {
-    const int i = ord[k];
+  for (size_t k = 0; k < ord.size(); ++k) {
     int g = total > 0.0 ? (int)(run / total * ng) : 0;
     g = std::min(std::max(g, 0), ng - 1);
-    group_of[i] = g;
+    slot[k] = g;
     used[g] = 1;
-    run += cost[i];
+    run += cost[k];
   }
   std::vector<int> remap(ng);
   int nz = 0;
   for (int g = 0; g < ng; ++g) remap[g] = used[g] ? nz++ : -1;
-  for (int i = 0; i < n; ++i) group_of[i] = remap[group_of[i]];
+  for (size_t k = 0; k < ord.size(); ++k) group_of[ord[k]] = first + remap[slot[k]];
   return nz;
+}
+
+// Shard groups of the host-buffer step, in execution order; group_of[i] is
+// shard i's group.  groups >= 1: balanced groups over all shards.
+// groups == 0: the copy volume decides (mfsdp_host_step_groups).  Only the
+// first copy in and the last copy out are exposed; every group past the first
+// costs a little compute.
+//  - Large sets (g >= 6): g balanced groups, each of which still fills the
+//    GPU, between a small head and a small tail group: up to two of the
+//    smallest shards with the largest short side (the most Newton-Schulz work
+//    per byte) at each end, at most 1/(2g) of the elements each.  The head's
+//    compute hides the next group's copy in, the tail's the copy out before it.
+//  - Mid-sized sets (3 <= g <= 5): a ramp -- shards ordered small -> large ->
+//    small by size and cut at 4 %, 28 %, 72 % and 96 % of the bytes -- which
+//    makes the two exposed copies small with five groups, where balanced
+//    groups of a few matrices would leave most of the GPU idle.
+int plan_host_groups(const mfsdp_matrix_shard* shards, int n, int groups, size_t elem_bytes,
+                     std::vector<int>& group_of) {
+  group_of.assign(n, 0);
+  if (n <= 0) return 1;
+  std::vector<char> all(n, 1);
+  if (groups >= 1) return balanced_groups(shards, n, all, groups, 0, group_of);
+  double elems = 0.0;
+  for (int i = 0; i < n; ++i) elems += (double)shards[i].rows * (double)shards[i].cols;
+  const long g = std::lround(std::sqrt(elems * (double)elem_bytes / 50e6));
+  if (g <= 1) return 1;
+  if (g == 2 || n < 5) return balanced_groups(shards, n, all, (int)g, 0, group_of);
+  if (g >= 6) {
+    const int gm = (int)std::min<long>(g, 16);
+    int64_t smax = 0;
+    for (int i = 0; i < n; ++i) smax = std::max(smax, std::min(shards[i].rows, shards[i].cols));
+    std::vector<int> cand;
+    for (int i = 0; i < n; ++i)
+      if (std::min(shards[i].rows, shards[i].cols) == smax) cand.push_back(i);
+    std::sort(cand.begin(), cand.end(), [&](int x, int y) {
+      const int64_t nx = shards[x].rows * shards[x].cols, ny = shards[y].rows * shards[y].cols;
+      return nx != ny ? nx < ny : shards[x].offset < shards[y].offset;
+    });
+    const double limit = elems / (2.0 * gm);
+    std::vector<int> head, tail;
+    size_t k = 0;
+    for (std::vector<int>* end : {&head, &tail}) {
+      double e = 0.0;
+      while (k < cand.size() && end->size() < 2) {
+        const double ne = (double)shards[cand[k]].rows * (double)shards[cand[k]].cols;
+        if (e + ne > limit) break;
+        end->push_back(cand[k++]);
+        e += ne;
+      }
+    }
+    if (head.empty() || tail.empty()) return balanced_groups(shards, n, all, gm, 0, group_of);
+    std::vector<char> mid(n, 1);
+    for (int i : head) { mid[i] = 0; group_of[i] = 0; }
+    for (int i : tail) mid[i] = 0;
+    const int nm = balanced_groups(shards, n, mid, gm, 1, group_of);
+    for (int i : tail) group_of[i] = 1 + nm;
+    return 2 + nm;
+  }
+  std::vector<int> by(n);
+  for (int i = 0; i < n; ++i) by[i] = i;
+  std::sort(by.begin(), by.end(), [&](int x, int y) {
+    const int64_t nx = shards[x].rows * shards[x].cols, ny = shards[y].rows * shards[y].cols;
+    return nx != ny ? nx < ny : shards[x].offset < shards[y].offset;
+  });
+  // small -> large: the even positions; large -> small: the odd ones reversed
+  std::vector<int> seq;
+  for (int k = 0; k < n; k += 2) seq.push_back(by[k]);
+  for (int k = (n % 2 == 0) ? n - 1 : n - 2; k >= 1; k -= 2) seq.push_back(by[k]);
+  const double cuts[4] = {0.04, 0.28, 0.72, 0.96};
+  std::vector<int> slot(n);
+  bool used[5] = {false, false, false, false, false};
+  double run = 0.0;
+  for (int i : seq) {
+    const double e = (double)shards[i].rows * (double)shards[i].cols;
+    const double mid = (run + 0.5 * e) / elems;          // a shard goes where its midpoint falls
+    int k = 0;
+    while (k < 4 && cuts[k] <= mid) ++k;
+    slot[i] = k;
+    used[k] = true;
+    run += e;
+  }
+  int remap[5], ng = 0;                                    // a large shard can leave a slot empty
+  for (int k = 0; k < 5; ++k) remap[k] = used[k] ? ng++ : -1;
+  for (int i = 0; i < n; ++i) group_of[i] = remap[slot[i]];
+  return ng;
 }
 
 }  // namespace

@@ -242,12 +242,14 @@ def test_inject_stall_rejects_negative_tile(mfsdp):
 
 
 def test_host_step_groups(mfsdp):
-    """groups = 0: g = round(sqrt(copy bytes / 50 MB)); one group for g <= 1,
-    cost-balanced offset ranges for g == 2, g >= 6 or fewer than 5 shards,
-    else the ramp (small -> large -> small by size, cut at 4/28/72/96 % of the
-    bytes, a shard placed by the midpoint of its bytes).  groups >= 1: offset
-    ranges of balanced cost 4 s^2 l + 2 s^3 + s l.  Expected values worked by
-    hand."""
+    """groups = 0: g = round(sqrt(copy bytes / 50 MB)); one group for g <= 1;
+    cost-balanced offset ranges for g == 2 or fewer than 5 shards; for g >= 6
+    min(g, 16) balanced ranges between a head and a tail of up to two of the
+    smallest shards with the largest short side (at most 1/(2 min(g, 16)) of
+    the elements per end); for 3 <= g <= 5 the ramp (small -> large -> small by
+    size, cut at 4/28/72/96 % of the bytes, a shard placed by the midpoint of
+    its bytes).  groups >= 1: offset ranges of balanced cost 4 s^2 l + 2 s^3 +
+    s l.  Expected values worked by hand."""
     import torch
     bf, f32 = torch.bfloat16, torch.float32
 
@@ -270,9 +272,21 @@ def test_host_step_groups(mfsdp):
     assert mfsdp.host_step_groups(six, bf, bf) == (5, [0, 0, 3, 1, 2, 4])
     eight = layout([(8192, 8192)] * 8)                                 # 2.15 GB: g = 7, balanced
     assert mfsdp.host_step_groups(eight, bf, bf) == (7, [0, 0, 1, 2, 3, 4, 5, 6])
-    many = layout([(8192, 8192)] * 40)                                 # 10.7 GB: g = 15
-    assert mfsdp.host_step_groups(many, bf, bf)[0] == 15
-    assert mfsdp.host_step_groups(many, f32, f32)[0] == 16            # 21.5 GB: g = 21, capped
+    # 40 equal shards, 10.7 GB: g = 15; one shard (67M elements) fits the
+    # 1/30 limit (89M) at each end: head, 15 balanced groups, tail
+    many = layout([(8192, 8192)] * 40)
+    ng, gof = mfsdp.host_step_groups(many, bf, bf)
+    assert ng == 17 and gof[0] == 0 and gof[1] == 16 and gof[2:] == sorted(gof[2:]) and set(gof[2:]) == set(range(1, 16))
+    assert mfsdp.host_step_groups(many, f32, f32)[0] == 18            # 21.5 GB: g = 21, capped at 16 + 2
+    # layers of 5 wide 4096x14336, one 4096^2 and one 1024x4096: 5.03 GB, g = 10,
+    # limit 62.9M elements per end; the largest short side is 4096 and the
+    # smallest such shards are the 4096^2 ones: two at each end, in offset order
+    layers = layout(([(4096, 14336)] * 5 + [(4096, 4096), (1024, 4096)]) * 4)
+    ng, gof = mfsdp.host_step_groups(layers, bf, bf)
+    sq = [i for i in range(28) if i % 7 == 5]
+    assert ng == 12 and [gof[i] for i in sq] == [0, 0, 11, 11]
+    rest = [gof[i] for i in range(28) if i % 7 != 5]
+    assert rest == sorted(rest) and set(rest) == set(range(1, 11))
     # explicit groups: s4 holds 74 % of the cost, so the cut falls after it
     assert mfsdp.host_step_groups(six, bf, bf, groups=2) == (2, [0, 0, 0, 0, 0, 1])
     assert mfsdp.host_step_groups(six, bf, bf, groups=1) == (1, [0] * 6)
