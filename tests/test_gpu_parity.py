@@ -268,17 +268,18 @@ def test_phase_split_matches_full_step(mfsdp):
     assert np.array_equal(mom.cpu().numpy(), m1)
 
 
-def test_host_buffer_ramp_matches_resident_step(mfsdp):
-    """The library's own group choice on a set large enough for the
-    small -> large -> small ramp (the 1.3B rank: 5 groups, shards out of offset
-    order, several copy runs per group): update and momentum bit-identical to
-    the resident step, and the staging buffers hold exactly the copied
-    gradient."""
+@pytest.mark.parametrize("name,n_groups", [("llama_1p3b_rank", 5), ("llama3_8b_rank", 10)])
+def test_host_buffer_library_groups_match_resident_step(mfsdp, name, n_groups):
+    """The library's own group choice on sets large enough to leave offset
+    order -- the 1.3B rank's small -> large -> small ramp (5 groups) and the 8B
+    rank's balanced groups between a head and a tail (10 groups): update and
+    momentum bit-identical to the resident step, and the staging buffer holds
+    exactly the copied gradient."""
     dev = _dev()
-    w = W.get("llama_1p3b_rank")
+    w = W.get(name)
     plan, r, shards, numel = owner_set(mfsdp, w)
     ng, gof = mfsdp.host_step_groups(shards)
-    assert ng == 5 and sorted(set(gof)) == list(range(5))
+    assert ng == n_groups and sorted(set(gof)) == list(range(ng))
     order = sorted(range(len(shards)), key=lambda i: shards[i].offset)
     assert any(gof[order[k]] > gof[order[k + 1]] for k in range(len(order) - 1))   # not offset order
     gen = torch.Generator(device=dev)
