@@ -758,8 +758,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// The driver's tensor-map encoder, looked up once through the runtime (the
-// library links no driver library).
+// The CUDA driver API's tensor-map encoder, looked up once through the
+// runtime (the library links no driver library).
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = [] {
     void* f = nullptr;
