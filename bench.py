@@ -340,6 +340,7 @@ def run_ours(args):
     mom_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     ns_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     adam_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    steps_ms = sorted(e[0].elapsed_time(e[3]) for e in evs)
     step_ms = max_over_ranks(total_ms / args.steps, dev)
     st, detail = mfsdp.muon_device_status(ws)
     if st != mfsdp.OK:
@@ -482,7 +483,9 @@ def run_ours(args):
                    "newton_schulz_tflops_dense_equivalent": round(ns_tflops, 1),
                    "newton_schulz_frac_bf16_dense_equivalent": round(ns_tflops / peak_tf, 4),
                    "flops_dense": flops, "flops_executed": flops_exec,
-                   "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1)},
+                   "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1),
+                   "step_ms_median": round(statistics.median(steps_ms), 4),
+                   "step_ms_min": round(steps_ms[0], 4), "step_ms_max": round(steps_ms[-1], 4)},
         "roofline": {"kernel": "ns_kernel", "bound": "tensor", "achieved": round(ns_tflops_exec, 1),
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4),
                      "traffic": NS_GEMM_TRAFFIC.get((mfsdp.version(), w.name)),
