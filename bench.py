@@ -409,6 +409,24 @@ def run_ours(args):
         sup["adamw_50M"] = {"ms": round(a_ms, 4), "gbs": round(28 * n_big / a_ms / 1e6, 1)}
         del bp, bg, bm, bv
 
+    # ---------------------------------------------------------- supplementary: momentum phase alone
+    # The momentum phase of this owner set back to back, with no Newton-Schulz launch
+    # before it: inside the step it runs at the SM clock the power cap leaves after
+    # the GEMMs, here at the clock the memory-bound kernel itself allows.
+    if rank == 0 and not args.no_supplementary and shards:
+        for _ in range(2):
+            mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        s0.record(stream)
+        for _ in range(reps):
+            mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sup["momentum_back_to_back"] = {"ms": round(s0.elapsed_time(s1) / reps, 4)}
+
     # ---------------------------------------------------------- supplementary: owner-segment reduce
     # The reduce that lands every owned matrix on this owner before the step:
     # w.world simulated ranks' local gradients (bf16, unsharded model layout)
@@ -452,6 +470,10 @@ def run_ours(args):
     ns_launches = batches
     if "adamw_50M" in sup:
         sup["adamw_50M"]["frac_hbm"] = round(sup["adamw_50M"]["gbs"] / hbm, 4)
+    if "momentum_back_to_back" in sup:
+        mb = sup["momentum_back_to_back"]
+        mb["gbs"] = round(mom_bytes / (mb["ms"] * 1e-3) / 1e9, 1)
+        mb["frac_hbm"] = round(mb["gbs"] / hbm, 4)
     if "owner_segment_reduce" in sup:
         sup["owner_segment_reduce"]["frac_hbm"] = round(sup["owner_segment_reduce"]["gbs"] / hbm, 4)
 
