@@ -305,6 +305,44 @@ def test_host_buffer_library_groups_match_resident_step(mfsdp, name, n_groups):
         assert torch.equal(gd[seg], g_dev[seg]), s.param_id
 
 
+@pytest.mark.parametrize("groups", [1, 3])
+@pytest.mark.parametrize("gdt,udt", [("f32", "f32"), ("f32", "bf16"), ("bf16", "f32"), ("bf16", "bf16")])
+def test_host_buffer_dtypes_ragged(mfsdp, gdt, udt, groups):
+    """Every gradient / update dtype pair through the host-buffer step, on a
+    ragged owner set (dimensions that fill no tile; 128-element aligned
+    offsets with gaps): the copies move grad- and update-sized ranges, so the
+    result must be bit-identical to the resident step with the same inputs."""
+    dev = _dev()
+    params = [p for p in W.ragged_params(41, 24) if p[2] == W.KIND_MATRIX][:9]
+    plan = mfsdp.plan_owners(params, 1, 5, 128)
+    shards = plan.rank_matrices(0)
+    numel = plan.rank_matrix_elems[0]
+    tg = torch.float32 if gdt == "f32" else torch.bfloat16
+    tu = torch.float32 if udt == "f32" else torch.bfloat16
+    rng = np.random.default_rng(4242)
+    g_cpu = torch.from_numpy((rng.standard_normal(numel) * 1e-2).astype(np.float32)).to(tg)
+    m_cpu = torch.from_numpy((rng.standard_normal(numel) * 1e-3).astype(np.float32))
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    g_dev, mom_ref = g_cpu.to(dev), m_cpu.to(dev)
+    upd_ref = torch.full((numel,), float("nan"), dtype=tu, device=dev)
+    mfsdp.muon_owner_step(shards, g_dev, mom_ref, upd_ref, ws)
+    gh = g_cpu.pin_memory()
+    uh = torch.full((numel,), float("nan"), dtype=tu).pin_memory()
+    gd = torch.zeros(numel, dtype=tg, device=dev)
+    ud = torch.full((numel,), float("nan"), dtype=tu, device=dev)
+    mom = m_cpu.to(dev)
+    mfsdp.muon_owner_step_host(shards, gh, gd, mom, ud, uh, ws, groups=groups)
+    torch.cuda.synchronize()
+    assert mfsdp.muon_device_status(ws)[0] == mfsdp.OK
+    assert mfsdp.host_step_groups(shards, tg, tu, groups)[0] == min(groups, len(shards))
+    assert torch.equal(mom, mom_ref)
+    ref = upd_ref.cpu()
+    view = torch.int32 if tu == torch.float32 else torch.int16
+    for s in shards:
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        assert torch.equal(uh[seg].view(view), ref[seg].view(view)), (s.param_id, s.rows, s.cols)
+
+
 @pytest.mark.parametrize("groups", [0, 1, 2, 3, 8])
 def test_host_buffer_pipeline_matches_resident_step(mfsdp, groups):
     """Gradient from pinned host memory, update back to it, copies overlapped with
