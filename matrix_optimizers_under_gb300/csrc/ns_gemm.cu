@@ -20,11 +20,12 @@
 // atoms of one 64-column block contiguous.  So a CTA's share of a pipeline
 // stage is one 16 KB run of rows per column block for each operand (for the
 // MN-major X of the update, one 16 KB run of 128 K rows per 64-column block),
-// and a tensor copy of one map that views the whole
+// and a tensor copy through a map that views the whole
 // workspace as 128-byte rows lands it in shared memory byte for byte, ready
-// for tcgen05.mma: one map for any mix of shapes in one launch, and the same
-// stored X serves as the K-major operand of the Gram product and the MN-major
-// operand of the update.
+// for tcgen05.mma.  Two maps of that one view (boxes of 128 and 64 rows: 16 KB
+// runs, and the 8 KB B halves of 128-column tiles) serve any mix of shapes in
+// one launch, and the same stored X serves as the K-major operand of the Gram
+// product and the MN-major operand of the update.
 //
 // One launch runs every product of every iteration for up to kMaxBatch
 // matrices.  Its tiles form one product-major list (all Gram tiles of
