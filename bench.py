@@ -369,6 +369,8 @@ def run_ours(args):
     # As many untimed warm-up steps as the device-resident measurement: with a
     # single one, the first timed step sometimes took ~200 ms more (a one-off
     # on the host-memory side) and dominated the mean.
+    e2e_sampler = ClockSampler(local_rank)      # clocks and throttle reasons of the e2e region too
+    e2e_sampler.start()
     for _ in range(max(args.warmup, 1)):
         one_step_host()
     torch.cuda.synchronize()
@@ -385,6 +387,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     gc.enable()
+    e2e_clocks = e2e_sampler.stop()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_steps_ms = [round(step_ev[k].elapsed_time(step_ev[k + 1]), 3) for k in range(e2e_steps)]
 
@@ -518,7 +521,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
                 "pipeline_groups": e2e_groups, "steps_ms": e2e_steps_ms,
-                "median_ms": round(statistics.median(e2e_steps_ms), 3)},
+                "median_ms": round(statistics.median(e2e_steps_ms), 3), "clocks": e2e_clocks},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,
