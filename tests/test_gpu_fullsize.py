@@ -102,3 +102,47 @@ def test_full_size_adamw_tail(mfsdp):
     assert H.adam_err(tp.cpu().numpy(), rp) <= H.ADAM_REL
     assert H.adam_err(tm.cpu().numpy(), rm) <= H.ADAM_REL
     assert H.adam_err(tv.cpu().numpy(), rv) <= H.ADAM_REL
+
+
+def test_full_owner_set_second_step_fp32_update(mfsdp):
+    """The 1.3B rank at full size for two steps with different gradients and an
+    fp32 update: the second step starts from momentum G1, so M = beta G1 + G2
+    and the Newton-Schulz input is that sum (MatrixFSDP -- Abstract:
+    momentum-smoothed updates), and the last epilogue writes fp32 in the stored
+    orientation.  One matrix of every shape is checked against the fp64 oracle."""
+    w = W.get("llama_1p3b_rank")
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan)
+    shards = plan.rank_matrices(r)
+    numel = plan.rank_matrix_elems[r]
+    g1_np = W.owner_grad_buffer(w, shards, numel)
+    rng = np.random.default_rng([w.seed, 2])
+    g2_np = W.f32_to_bf16_bits((rng.standard_normal(numel) * w.grad_scale).astype(np.float32))
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    kw = dict(beta=w.beta, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.full((numel,), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    for g_np in (g1_np, g2_np):
+        grad = torch.from_numpy(g_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        mfsdp.muon_owner_step(shards, grad, mom, upd, ws, **kw)
+        st, detail = mfsdp.muon_device_status(ws)
+        assert st == mfsdp.OK, (st, detail)
+    torch.cuda.synchronize()
+    del ws
+    errs = {}
+    for s in _sample(shards, w):
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        G1 = bf16_bits_to_f64(g1_np[seg]).reshape(s.rows, s.cols)
+        G2 = bf16_bits_to_f64(g2_np[seg]).reshape(s.rows, s.cols)
+        M_ref, O_ref = muon_matrix_ref(G2, G1, w.beta, False, w.ns_steps, A, B, C, w.ns_eps)
+        M = mom[seg].cpu().numpy().astype(np.float64).reshape(s.rows, s.cols)
+        bound = H.MOM_REL * (np.abs(w.beta * G1) + np.abs(G2)) + 1e-30
+        assert np.all(np.abs(M - M_ref) <= bound), s.param_id
+        O = upd[seg].cpu().numpy().astype(np.float64).reshape(s.rows, s.cols)
+        assert np.all(np.isfinite(O)), s.param_id
+        errs[(s.rows, s.cols)] = H.rel_fro(O, O_ref)
+        assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
+    print({k: round(v, 5) for k, v in errs.items()})
