@@ -146,3 +146,52 @@ def test_full_owner_set_second_step_fp32_update(mfsdp):
         errs[(s.rows, s.cols)] = H.rel_fro(O, O_ref)
         assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
     print({k: round(v, 5) for k, v in errs.items()})
+
+
+def test_full_owner_set_apply(mfsdp):
+    """The fused weight update at full size (1.3B rank, fp32 weights, the Muon
+    shape scale): every element of the sampled matrices is W (1 - lr wd) -
+    lr scale O for the update O the same call wrote (one fp32 rounding), and
+    the weight change matches the fp64 oracle's within the Newton-Schulz
+    tolerance."""
+    from oracle import muon_apply_ref, muon_scale_ref
+    w = W.get("llama_1p3b_rank")
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan)
+    shards = plan.rank_matrices(r)
+    numel = plan.rank_matrix_elems[r]
+    grad_np = W.owner_grad_buffer(w, shards, numel)
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    lr, wd, mode = 0.02, 0.1, mfsdp.SCALE_MUON
+    W0 = (np.random.default_rng([w.seed, 3]).standard_normal(numel) * 0.02).astype(np.float32)
+    Wt = torch.from_numpy(W0).to(dev)
+    grad = torch.from_numpy(grad_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.full((numel,), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+    mfsdp.muon_owner_step_apply(shards, grad, mom, upd, Wt, ws, lr=lr, weight_decay=wd, scale_mode=mode,
+                                beta=w.beta, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
+    st, detail = mfsdp.muon_device_status(ws)
+    assert st == mfsdp.OK, (st, detail)
+    torch.cuda.synchronize()
+    del ws
+    decay = np.float64(np.float32(1.0 - lr * wd))
+    errs = {}
+    for s in _sample(shards, w):
+        seg = slice(s.offset, s.offset + s.rows * s.cols)
+        O = upd[seg].cpu().numpy().astype(np.float64)
+        Wn = Wt[seg].cpu().numpy().astype(np.float64)
+        W0s = W0[seg].astype(np.float64)
+        scale = muon_scale_ref(s.rows, s.cols, mode)
+        expect = W0s * decay - lr * scale * O
+        tol = 2.0 ** -23 * 4 * (np.abs(W0s) + lr * scale * np.abs(O))
+        assert np.all(np.abs(Wn - expect) <= tol + 1e-30), s.param_id
+        G = bf16_bits_to_f64(grad_np[seg]).reshape(s.rows, s.cols)
+        _, O_ref = muon_matrix_ref(G, np.zeros_like(G), w.beta, False, w.ns_steps, A, B, C, w.ns_eps)
+        W_ref = muon_apply_ref(W0s.reshape(s.rows, s.cols), O_ref, lr, wd, scale)
+        base = W0s.reshape(s.rows, s.cols) * decay
+        errs[(s.rows, s.cols)] = H.rel_fro(Wn.reshape(s.rows, s.cols) - base, W_ref - base)
+        assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
+    print({k: round(v, 5) for k, v in errs.items()})
