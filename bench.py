@@ -53,8 +53,10 @@ NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_ra
                    ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
                    ("0.8.4", "llama3_8b_rank"): 50.02e9,
                    ("0.8.5", "llama3_8b_rank"): 50.58e9, ("0.8.6", "llama3_8b_rank"): 50.08e9,
-                   # 0.8.7 and 0.8.8 changed only the host-buffer entry's grouping: ns_kernel is 0.8.6's
-                   ("0.8.7", "llama3_8b_rank"): 50.08e9, ("0.8.8", "llama3_8b_rank"): 50.08e9}
+                   # 0.8.7-0.8.9 changed only host code (the host-buffer entry's grouping, argument
+                   # checks): ns_kernel is 0.8.6's
+                   ("0.8.7", "llama3_8b_rank"): 50.08e9, ("0.8.8", "llama3_8b_rank"): 50.08e9,
+                   ("0.8.9", "llama3_8b_rank"): 50.08e9}
 
 
 # --------------------------------------------------------------------------- helpers

@@ -229,7 +229,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.8"; }
+extern "C" const char* mfsdp_version(void) { return "0.8.9"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -254,11 +254,11 @@ extern "C" int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int
 namespace mfsdp {
 namespace {
 
-// Every check of the owner-step arguments (host only, nothing queued).
-int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
-                  const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
-                  int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps,
-                  const void* workspace, size_t workspace_bytes, Layout* L) {
+// Every check of an owner step's arguments that needs no workspace (host only,
+// nothing queued).
+int validate_step_args(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
+                       const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
+                       int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps, Layout* L) {
   if (n_shards < 0 || (n_shards > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
   if (!std::isfinite(beta) || !std::isfinite(a) || !std::isfinite(b) || !std::isfinite(c) || !std::isfinite(eps) ||
       eps < 0.0)
@@ -267,9 +267,8 @@ int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void
   if (update_dtype != MFSDP_DTYPE_F32 && update_dtype != MFSDP_DTYPE_BF16) return MFSDP_ERR_UNSUPPORTED_DTYPE;
   if (numel < 0 || ns_steps < 0 || ns_steps > 64 || (nesterov != 0 && nesterov != 1)) return MFSDP_ERR_INVALID_ARG;
   if (n_shards == 0) return MFSDP_OK;
-  if (!grad || !momentum || !update || !workspace) return MFSDP_ERR_INVALID_ARG;
-  if (!aligned(grad, 16) || !aligned(momentum, 16) || !aligned(update, 16) || !aligned(workspace, 256))
-    return MFSDP_ERR_MISALIGNED;
+  if (!grad || !momentum || !update) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(grad, 16) || !aligned(momentum, 16) || !aligned(update, 16)) return MFSDP_ERR_MISALIGNED;
   const int st = make_layout(shards, n_shards, L);
   if (st != MFSDP_OK) return st;
   if (!ns_counts_fit(*L, ns_steps)) return MFSDP_ERR_UNSUPPORTED_SHAPE;
@@ -293,7 +292,23 @@ int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void
   if (ranges_overlap(momentum, mbytes, grad, gbytes) || ranges_overlap(momentum, mbytes, update, ubytes) ||
       (!in_place && ranges_overlap(grad, gbytes, update, ubytes)))
     return MFSDP_ERR_OVERLAP;
+  return MFSDP_OK;
+}
+
+// validate_step_args, then the workspace: present, aligned, large enough and
+// apart from the other buffers.
+int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
+                  const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
+                  int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps,
+                  const void* workspace, size_t workspace_bytes, Layout* L) {
+  const int st = validate_step_args(shards, n_shards, grad, grad_dtype, momentum, update, update_dtype, numel, beta,
+                                    nesterov, ns_steps, a, b, c, eps, L);
+  if (st != MFSDP_OK || n_shards == 0) return st;
+  if (!workspace) return MFSDP_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MFSDP_ERR_MISALIGNED;
   if (workspace_bytes < L->bytes) return MFSDP_ERR_WORKSPACE_TOO_SMALL;
+  const size_t gbytes = (size_t)numel * dtype_size(grad_dtype), mbytes = (size_t)numel * 4,
+               ubytes = (size_t)numel * dtype_size(update_dtype);
   if (ranges_overlap(workspace, L->bytes, grad, gbytes) || ranges_overlap(workspace, L->bytes, momentum, mbytes) ||
       ranges_overlap(workspace, L->bytes, update, ubytes))
     return MFSDP_ERR_OVERLAP;
@@ -301,6 +316,18 @@ int validate_step(const mfsdp_matrix_shard* shards, int32_t n_shards, const void
 }
 
 }  // namespace
+
+int check_step_args(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
+                    const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
+                    int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps,
+                    size_t* workspace_bytes) {
+  Layout L;
+  const int st = validate_step_args(shards, n_shards, grad, grad_dtype, momentum, update, update_dtype, numel, beta,
+                                    nesterov, ns_steps, a, b, c, eps, &L);
+  if (workspace_bytes) *workspace_bytes = (st == MFSDP_OK && n_shards > 0) ? L.bytes : 0;
+  return st;
+}
+
 }  // namespace mfsdp
 
 extern "C" int mfsdp_muon_owner_step_phases(const mfsdp_matrix_shard* shards, int32_t n_shards,

@@ -9,6 +9,8 @@
 
 #include <cuda_runtime.h>
 
+#include "mfsdp.h"
+
 namespace mfsdp {
 
 constexpr int kMaxBatch = 128;     // matrices per launch
@@ -186,6 +188,14 @@ enum WaitRole : int32_t {
 };
 
 cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s);
+
+// Every host-side check of an owner step's arguments except those of the
+// workspace, without touching a device; *workspace_bytes (may be null)
+// receives the scratch the step needs (0 for an empty owner set or an error).
+int check_step_args(const mfsdp_matrix_shard* shards, int32_t n_shards, const void* grad, int32_t grad_dtype,
+                    const float* momentum, const void* update, int32_t update_dtype, int64_t numel, double beta,
+                    int32_t nesterov, int32_t ns_steps, double a, double b, double c, double eps,
+                    size_t* workspace_bytes);
 cudaError_t launch_norm_finalize(const NormBatch& b, cudaStream_t s);
 cudaError_t launch_emit(const EmitBatch& b, int total_tiles, cudaStream_t s);
 cudaError_t launch_ns(const NsBatch& b, size_t ws_bytes, cudaStream_t s);

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "mfsdp.h"
+#include "mfsdp_internal.h"
 
 namespace {
 
@@ -48,9 +49,12 @@ extern "C" int mfsdp_muon_owner_step_static_scratch(const mfsdp_matrix_shard* sh
                                                     void* update, int32_t update_dtype, int64_t numel, double beta,
                                                     int32_t nesterov, int32_t ns_steps, double a, double b, double c,
                                                     double eps, void* stream) {
-  if (n_shards < 0 || (n_shards > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
-  if (n_shards == 0) return MFSDP_OK;
-  const size_t need = mfsdp_muon_workspace_bytes(shards, n_shards);
+  // The arguments are checked on the host before the scratch array's address
+  // is looked up, so they fail with the regular entry point's statuses.
+  size_t need = 0;
+  const int checked = mfsdp::check_step_args(shards, n_shards, grad, grad_dtype, momentum, update, update_dtype,
+                                             numel, beta, nesterov, ns_steps, a, b, c, eps, &need);
+  if (checked != MFSDP_OK || n_shards == 0) return checked;
   if (need > (size_t)MFSDP_STATIC_SCRATCH_BYTES) return MFSDP_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const int st = scratch_address(&scratch);

@@ -298,3 +298,34 @@ def test_host_step_groups(mfsdp):
         kw.update(bad)
         assert mfsdp.host_step_groups(six, **kw) == (0, [])
     assert mfsdp.host_step_groups([], bf, bf) == (0, [])
+
+
+def test_static_scratch_error_paths(mfsdp):
+    """The no-workspace entry point checks its arguments on the host, with the
+    regular entry point's statuses, before it looks up its scratch array."""
+    lib = mfsdp.raw_lib()
+    ok = [mfsdp.make_shard(0, 256, 512)]
+    arr = (mfsdp.MatrixShard * 1)(*ok)
+    big = (mfsdp.MatrixShard * 1)(mfsdp.make_shard(0, 4096, 4096))
+
+    def call(shards=arr, n=1, grad=G, gdt=BF, upd=U, udt=BF, numel=1 << 20, ns=5, beta=0.95):
+        return lib.mfsdp_muon_owner_step_static_scratch(shards, n, grad, gdt, M, upd, udt, numel, beta, 0, ns,
+                                                        3.4445, -4.775, 2.0315, 1e-7, None)
+    assert call(grad=None) == mfsdp.ERR_INVALID_ARG
+    assert call(gdt=7) == mfsdp.ERR_UNSUPPORTED_DTYPE
+    assert call(udt=7) == mfsdp.ERR_UNSUPPORTED_DTYPE
+    assert call(grad=G + 2) == mfsdp.ERR_MISALIGNED
+    assert call(ns=-1) == mfsdp.ERR_INVALID_ARG
+    assert call(beta=float("nan")) == mfsdp.ERR_INVALID_ARG
+    assert call(numel=100) == mfsdp.ERR_OUT_OF_BOUNDS
+    assert call(upd=G, udt=F32) == mfsdp.ERR_OVERLAP         # the same buffer in another dtype (in place needs both equal)
+    assert call(shards=big, numel=4096 * 4096) == mfsdp.ERR_WORKSPACE_TOO_SMALL
+    assert call(shards=None, n=0, grad=None, upd=None) == mfsdp.OK
+    assert call(shards=None, n=-1) == mfsdp.ERR_INVALID_ARG
+
+
+def test_device_status_error_paths(mfsdp):
+    import ctypes
+    lib = mfsdp.raw_lib()
+    detail = ctypes.c_int32(7)
+    assert lib.mfsdp_muon_device_status(None, None, ctypes.byref(detail)) == mfsdp.ERR_INVALID_ARG
