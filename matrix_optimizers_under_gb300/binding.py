@@ -418,6 +418,11 @@ _lib.mfsdp_segment_copy.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POIN
 _lib.mfsdp_segment_copy.restype = ctypes.c_int
 
 
+def library_path() -> str:
+    """Path of the loaded libmfsdp.so."""
+    return _LIB_PATH
+
+
 def raw_lib() -> ctypes.CDLL:
     """The loaded library, for callers that marshal raw pointers themselves."""
     return _lib
