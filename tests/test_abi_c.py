@@ -24,3 +24,27 @@ def test_abi_from_plain_c(mfsdp, tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, run.stdout + run.stderr
     assert run.stdout.startswith("ok " + mfsdp.version())
+
+
+@pytest.mark.gpu
+def test_owner_step_from_plain_c(mfsdp, tmp_path):
+    """tests/c/step_from_c.c: an owner step with device memory from cudaMalloc
+    and no framework, through the workspace and the no-workspace entry points."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if not cc or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    lib_dir = os.path.dirname(mfsdp.library_path())
+    exe = str(tmp_path / "step_from_c")
+    cuda_lib = next((d for d in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib"))
+                     if os.path.exists(os.path.join(d, "libcudart.so"))), os.path.join(cuda, "lib64"))
+    build = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                            "-I", os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c", "step_from_c.c"),
+                            "-o", exe, "-L", lib_dir, "-lmfsdp", "-L", cuda_lib, "-lcudart", "-lm",
+                            "-Wl,-rpath," + lib_dir, "-Wl,-rpath," + cuda_lib], capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    if run.returncode == 2:
+        pytest.skip("no CUDA device")
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert run.stdout.strip().endswith("ok"), run.stdout
