@@ -12,8 +12,13 @@ gradient elements with Student-t(3) entries, 32,768-element RMSNorm tail).
 Prints one JSON line.  `value` is the device-timed owner-step latency in ms
 (inputs resident in HBM; every input is larger than L2, so no flush is needed),
 `e2e` the same latency through the same API with the gradient copied in from
-pinned host memory and the update copied back every step.  `--impl reference`
-times the fp64 CPU oracle on a bounded sample of the same workload instead.
+pinned host memory and the update copied back every step.  The supplementary
+block times, in the same process, the momentum phase alone, the owner-segment
+reduce, AdamW over a 50M-element tail and the other four workloads' owner sets
+(owner-step ms, Newton-Schulz TFLOP/s, momentum and AdamW GB/s, each against
+its measured peak).  `cpu_baseline` is the fp64 oracle on the host cores: one
+matrix of every shape of the owner set timed, times its count, plus the whole
+tail.  `--impl reference` times that oracle instead, one shape per step.
 
 Under torchrun (N > 1) each GPU runs the owner set of a different simulated
 rank (weak scaling: no collective on the data path; a barrier and a max over
@@ -43,20 +48,14 @@ from matrix_optimizers_under_gb300 import workloads as W  # noqa: E402
 METRIC = "owner-step ms; Newton–Schulz TFLOP/s (% BF16 peak); AdamW-tail GB/s (% HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per Newton-Schulz kernel launch on the llama3_8b_rank owner set
-# (0.5/0.6: the mean over one owner step's 15 per-product launches; 0.7: the one launch that
-# runs all of a step's products), from the ncu capture summarised in
-# profiles/launches_llama3_8b_rank.md; keyed by the library version it was taken on, so
-# that a changed kernel reports null until it is captured again.
-NS_GEMM_TRAFFIC = {("0.5.0", "llama3_8b_rank"): 3.359e9, ("0.6.0", "llama3_8b_rank"): 3.401e9,
-                   ("0.7.0", "llama3_8b_rank"): 50.17e9, ("0.8.1", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.2", "llama3_8b_rank"): 50.02e9, ("0.8.3", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.4", "llama3_8b_rank"): 50.02e9,
-                   ("0.8.5", "llama3_8b_rank"): 50.58e9, ("0.8.6", "llama3_8b_rank"): 50.08e9,
-                   # 0.8.7-0.8.9 changed only host code (the host-buffer entry's grouping, argument
-                   # checks): ns_kernel is 0.8.6's
-                   ("0.8.7", "llama3_8b_rank"): 50.08e9, ("0.8.8", "llama3_8b_rank"): 50.08e9,
-                   ("0.8.9", "llama3_8b_rank"): 50.08e9}
+# DRAM bytes (read + write) of one Newton-Schulz kernel launch per owner set,
+# from an ncu capture of dram__bytes_read.sum + dram__bytes_write.sum, keyed
+# by a digest of the kernel's sources (ns_source_digest): a kernel changed
+# since its capture reports null traffic until it is captured again.
+NS_GEMM_TRAFFIC = {}
+
+# The sources that make up the Newton-Schulz kernel.
+NS_SOURCES = ("ns_gemm.cu", "ptx.cuh", "mfsdp_internal.h")
 
 
 # --------------------------------------------------------------------------- helpers
@@ -66,6 +65,17 @@ def load_peaks():
         with open(path) as f:
             return json.load(f), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ns_source_digest() -> str:
+    """First 16 hex digits of the SHA-256 of the Newton-Schulz kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "matrix_optimizers_under_gb300", "csrc")
+    for name in NS_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ns_flops(rows: int, cols: int, steps: int) -> int:
@@ -155,28 +165,65 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, shards, tail_n, sample_ids, threads_note=""):
-    """Times the fp64 oracle on the sample matrices (momentum + Newton-Schulz)
-    and on the AdamW tail; returns (seconds, sample NS FLOPs, sample elements)."""
-    from oracle import adamw_ref, muon_matrix_ref
-    a, b, c = w.ns_coeffs
-    t0 = time.perf_counter()
-    flops = 0
-    elems = 0
+def shape_groups(shards):
+    """The owner set's distinct (rows, cols), each with its count and the
+    lowest param id of that shape (the one timed), largest work first."""
+    groups = {}
     for s in shards:
-        if s.param_id not in sample_ids:
-            continue
-        g = W.grad_storage(w, s.param_id)
-        G = ((g.astype(np.uint32) << 16).view(np.float32) if g.dtype == np.uint16 else g).astype(np.float64)
-        muon_matrix_ref(G, np.zeros_like(G), w.beta, w.nesterov, w.ns_steps, a, b, c, w.ns_eps)
-        flops += ns_flops(s.rows, s.cols, w.ns_steps)
-        elems += s.rows * s.cols
-    if tail_n:
-        rng = np.random.default_rng(0)
-        p = rng.standard_normal(tail_n)
-        adamw_ref(p, p, np.zeros(tail_n), np.zeros(tail_n), w.lr, w.betas[0], w.betas[1], w.adam_eps,
-                  w.weight_decay, w.step)
-    return time.perf_counter() - t0, flops, elems
+        g = groups.setdefault((s.rows, s.cols), [0, s.param_id])
+        g[0] += 1
+        g[1] = min(g[1], s.param_id)
+    return sorted(((rc, c, pid) for rc, (c, pid) in groups.items()),
+                  key=lambda x: (-ns_flops(x[0][0], x[0][1], 5), x[0]))
+
+
+def oracle_matrix_seconds(w, rows, cols, param_id):
+    """Wall-clock of the fp64 oracle's owner step (momentum, Frobenius
+    normalisation, Newton-Schulz) on one matrix held in a flat buffer as
+    stored (bf16 bits or fp32), from zero momentum."""
+    from oracle.muon import muon_owner_step_ref
+    a, b, c = w.ns_coeffs
+    flat = W.grad_storage(w, param_id).reshape(-1)
+    shard = [dict(param_id=param_id, offset=0, rows=rows, cols=cols)]
+    t0 = time.perf_counter()
+    muon_owner_step_ref(shard, flat, w.grad_dtype, np.zeros(rows * cols), w.beta, w.nesterov, w.ns_steps,
+                        a, b, c, w.ns_eps)
+    return time.perf_counter() - t0
+
+
+def oracle_tail_seconds(w, tail_n):
+    """Wall-clock of the fp64 oracle's AdamW over a whole tail of tail_n elements."""
+    from oracle import adamw_ref
+    if not tail_n:
+        return 0.0
+    rng = np.random.default_rng(0)
+    p = rng.standard_normal(tail_n) * w.tail_scale
+    g = rng.standard_normal(tail_n) * w.tail_scale
+    t0 = time.perf_counter()
+    adamw_ref(p, g, np.zeros(tail_n), np.zeros(tail_n), w.lr, w.betas[0], w.betas[1], w.adam_eps,
+              w.weight_decay, w.step)
+    return time.perf_counter() - t0
+
+
+def oracle_owner_step_estimate(w, shards, tail_n):
+    """The fp64 oracle's owner step on the host cores, per shape: one matrix of
+    every distinct shape timed once, each time multiplied by that shape's count
+    (the oracle's work and time per matrix depend on the shape alone), plus
+    AdamW over the whole tail, timed.  Returns (ms, description, seconds spent)."""
+    t_all = time.perf_counter()
+    groups = shape_groups(shards)
+    per = []
+    ms = 0.0
+    for (rows, cols), count, pid in groups:
+        sec = oracle_matrix_seconds(w, rows, cols, pid)
+        per.append(f"{rows}x{cols}: {sec * 1e3:.0f} ms x {count}")
+        ms += sec * 1e3 * count
+    tail_sec = oracle_tail_seconds(w, tail_n)
+    ms += tail_sec * 1e3
+    desc = (f"fp64 NumPy oracle: one matrix of each of the {len(groups)} shapes of the {len(shards)}-matrix owner "
+            f"set timed once (momentum + normalisation + Newton-Schulz from a flat buffer) and multiplied by the "
+            f"shape's count [{'; '.join(per)}], plus AdamW over the whole {tail_n}-element tail ({tail_sec * 1e3:.0f} ms)")
+    return ms, desc, time.perf_counter() - t_all
 
 
 def cpu_threads():
@@ -190,15 +237,16 @@ def cpu_threads():
     return os.cpu_count() or 1
 
 
-def pick_sample(shards):
-    """A bounded sample of the owner set: its smallest matrix plus one square one
-    (about 10-30 s of fp64 CPU work for the transformer owner sets)."""
-    by_size = sorted(shards, key=lambda s: (s.rows * s.cols, s.param_id))
-    ids = [by_size[0].param_id]
-    sq = [s for s in shards if s.rows == s.cols]
-    if sq and sq[0].param_id not in ids:
-        ids.append(sq[0].param_id)
-    return ids
+def blas_info():
+    """BLAS library and thread count NumPy uses (for the CPU-baseline record)."""
+    try:
+        from threadpoolctl import threadpool_info
+        info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if info:
+            return {"blas": info[0].get("internal_api"), "threads": info[0].get("num_threads")}
+    except Exception:
+        pass
+    return {"blas": None, "threads": None}
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -217,31 +265,169 @@ def run_reference(args):
             self.__dict__.update(d)
     shards = [S(d) for d in plan["matrix_shards"] if d["owner"] == r]
     tail_n = plan["rank_tail_numel"][r]
-    total_flops = sum(ns_flops(s.rows, s.cols, w.ns_steps) for s in shards)
-    sample = [min(shards, key=lambda s: (s.rows * s.cols, s.param_id)).param_id]
-    ms = []
+    groups = shape_groups(shards)
+    # Step i times one shape (in rotation) and the tail; the owner-step figure is
+    # every shape's mean time times its count, plus the tail's.
+    times = {g[0]: [] for g in groups}
+    tails = []
+    t_total = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        sec, fl, el = oracle_sample(w, shards, tail_n, sample)
+        (rows, cols), count, pid = groups[i % len(groups)]
+        sec = oracle_matrix_seconds(w, rows, cols, pid)
+        tsec = oracle_tail_seconds(w, tail_n)
         if i >= args.warmup:
-            ms.append(sec * 1e3 * total_flops / fl)
-    value = statistics.mean(ms)
+            times[(rows, cols)].append(sec)
+            tails.append(tsec)
+    for (rows, cols), count, pid in groups:         # fewer timed steps than shapes
+        if not times[(rows, cols)]:
+            times[(rows, cols)].append(oracle_matrix_seconds(w, rows, cols, pid))
+    value = sum(statistics.mean(times[rc]) * 1e3 * count for rc, count, _ in groups) + \
+        (statistics.mean(tails) * 1e3 if tails else 0.0)
     cores = cpu_threads()
-    desc = (f"fp64 NumPy oracle on param {sample[0]} "
-            f"({[(s.rows, s.cols) for s in shards if s.param_id == sample[0]][0]}) + the {tail_n}-element tail "
-            f"per step, scaled by dense Newton-Schulz FLOPs to the {len(shards)}-matrix owner set")
+    desc = (f"fp64 NumPy oracle, one shape of the {len(shards)}-matrix owner set per step in rotation "
+            f"({', '.join(f'{rc[0]}x{rc[1]} x {c}' for rc, c, _ in groups)}) plus AdamW over the whole "
+            f"{tail_n}-element tail; the owner-step figure is each shape's mean time times its count plus "
+            f"the tail's")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "ms", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "matrices": len(shards),
                        "elements": sum(s.rows * s.cols for s in shards), "ns_steps": w.ns_steps},
             "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "estimated": True, "method": "per shape: measured time x count",
+                             "sample": desc, "seconds": round(time.perf_counter() - t_total, 1),
+                             **blas_info()},
             "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # --------------------------------------------------------------------------- our arm
+class OwnerStep:
+    """Device buffers of one owner set and its step through the C ABI: the
+    momentum phase, the Newton-Schulz phase and AdamW over the packed tail, on
+    the current stream (events between the phases when asked)."""
+
+    def __init__(self, mfsdp, w, shards, numel, tail_numel, grad_np, dev, pin=False):
+        import torch
+        self.mfsdp, self.w, self.shards, self.tail_numel = mfsdp, w, shards, tail_numel
+        self.stream = torch.cuda.current_stream()
+        bf16 = w.grad_dtype == "bf16"
+        host = torch.from_numpy(grad_np.view(np.int16) if bf16 else grad_np)
+        self.grad_host = host.pin_memory() if pin else host
+        if bf16:
+            self.grad_host = self.grad_host.view(torch.bfloat16)
+        self.grad = self.grad_host.to(dev)
+        self.mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+        self.upd = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(max(mfsdp.muon_workspace_bytes(shards), 1), dtype=torch.uint8, device=dev)
+        rng = np.random.default_rng(w.seed)
+        n = max(tail_numel, 1)
+        self.tp = torch.from_numpy((rng.standard_normal(n) * w.tail_scale).astype(np.float32)).to(dev)
+        tg = torch.from_numpy((rng.standard_normal(n) * w.tail_scale).astype(np.float32))
+        self.tg_host = tg.pin_memory() if pin else tg
+        self.tg = self.tg_host.to(dev)
+        self.tm, self.tv = torch.zeros_like(self.tp), torch.zeros_like(self.tp)
+        self.kw = dict(beta=w.beta, nesterov=w.nesterov, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
+        self.count = 0
+        batches = math.ceil(len(shards) / 128) if shards else 0
+        self.batches = batches
+        # per batch of 128 matrices: momentum, norm finalise, one Newton-Schulz launch
+        self.launches = 3 * batches + (1 if tail_numel else 0)
+
+    def adamw(self):
+        w = self.w
+        self.mfsdp.adamw_tail_step(self.tp, self.tg, self.tm, self.tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1],
+                                   eps=w.adam_eps, wd=w.weight_decay, step=self.count)
+
+    def step(self, ev=None):
+        m = self.mfsdp
+        self.count += 1
+        if ev:
+            ev[0].record(self.stream)
+        if self.shards:
+            m.muon_owner_step(self.shards, self.grad, self.mom, self.upd, self.ws, phases=m.PHASE_MOMENTUM,
+                              **self.kw)
+        if ev:
+            ev[1].record(self.stream)
+        if self.shards:
+            m.muon_owner_step(self.shards, self.grad, self.mom, self.upd, self.ws, phases=m.PHASE_NEWTON_SCHULZ,
+                              **self.kw)
+        if ev:
+            ev[2].record(self.stream)
+        if self.tail_numel:
+            self.adamw()
+        if ev:
+            ev[3].record(self.stream)
+
+    def check_status(self, when):
+        if not self.shards:
+            return
+        st, detail = self.mfsdp.muon_device_status(self.ws)
+        if st != self.mfsdp.OK:
+            raise RuntimeError(f"device status {when}: {self.mfsdp.status_string(st)} ({detail})")
+
+
+def figures(mfsdp, step, ms, peaks):
+    """Algorithmic rates of one owner set's phases (ms: mean phase times)."""
+    w, shards = step.w, step.shards
+    flops, flops_exec = mfsdp.muon_step_flops(shards, w.ns_steps) if shards else (0, 0)
+    elems = sum(s.rows * s.cols for s in shards)
+    gsz = 2 if w.grad_dtype == "bf16" else 4
+    mom_bytes = elems * (gsz + 4 + 4 + 2)
+    peak_tf, hbm = peaks["bf16_tflops_sustained"], peaks["hbm_gbs"]
+    ns_tf = flops / (ms["ns"] * 1e-3) / 1e12 if ms["ns"] > 0 else 0.0
+    ns_tf_exec = flops_exec / (ms["ns"] * 1e-3) / 1e12 if ms["ns"] > 0 else 0.0
+    mom_gbs = mom_bytes / (ms["momentum"] * 1e-3) / 1e9 if ms["momentum"] > 0 else 0.0
+    adam_gbs = 28 * step.tail_numel / (ms["adamw"] * 1e-3) / 1e9 if ms["adamw"] > 0 and step.tail_numel else 0.0
+    return {"momentum_ms": round(ms["momentum"], 4), "momentum_gbs": round(mom_gbs, 1),
+            "momentum_frac_hbm": round(mom_gbs / hbm, 4), "momentum_bytes": mom_bytes,
+            "newton_schulz_ms": round(ms["ns"], 4),
+            "newton_schulz_tflops_executed": round(ns_tf_exec, 1),
+            "newton_schulz_frac_bf16_executed": round(ns_tf_exec / peak_tf, 4),
+            "newton_schulz_tflops_dense_equivalent": round(ns_tf, 1),
+            "newton_schulz_frac_bf16_dense_equivalent": round(ns_tf / peak_tf, 4),
+            "flops_dense": flops, "flops_executed": flops_exec,
+            "adamw_ms": round(ms["adamw"], 4), "adamw_gbs": round(adam_gbs, 1),
+            "adamw_frac_hbm": round(adam_gbs / hbm, 4)}
+
+
+def time_resident(step, steps, warmup, sampler=None, barrier=None):
+    """W untimed steps, then K steps timed with CUDA events on the launching
+    stream (a synchronize on both sides); returns the total ms, per-phase mean
+    ms and the per-step times."""
+    import torch
+    for _ in range(warmup):
+        step.step()
+    torch.cuda.synchronize()
+    step.check_status("after warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.4)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    gc.collect()
+    gc.disable()            # no collector pause while the host enqueues the timed steps
+    t0.record(step.stream)
+    for k in range(steps):
+        step.step(evs[k])
+    t1.record(step.stream)
+    torch.cuda.synchronize()
+    gc.enable()
+    if barrier:
+        barrier()
+    clocks = sampler.stop() if sampler else None
+    step.check_status("after the timed region")
+    ms = {"momentum": sum(e[0].elapsed_time(e[1]) for e in evs) / steps,
+          "ns": sum(e[1].elapsed_time(e[2]) for e in evs) / steps,
+          "adamw": sum(e[2].elapsed_time(e[3]) for e in evs) / steps}
+    per_step = sorted(e[0].elapsed_time(e[3]) for e in evs)
+    return t0.elapsed_time(t1), ms, per_step, clocks
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -252,16 +438,23 @@ def run_ours(args):
     _build.ensure_built()
     from matrix_optimizers_under_gb300 import binding as mfsdp
 
-    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
-    heavy = heaviest_rank(plan)
-    sim_rank = simulated_rank(heavy, rank, w.world)
-    shards = plan.rank_matrices(sim_rank)
-    tails = plan.rank_tails(sim_rank)
-    numel = plan.rank_matrix_elems[sim_rank]
-    tail_numel = plan.rank_tail_elems[sim_rank]
+    def owner_set(wl, r_offset):
+        plan = mfsdp.plan_owners(wl.param_table(), wl.world, wl.ns_steps, wl.align_elems)
+        heavy = heaviest_rank(plan)
+        sim = simulated_rank(heavy, r_offset, wl.world)
+        return plan, sim, plan.rank_matrices(sim), plan.rank_matrix_elems[sim], plan.rank_tail_elems[sim]
 
+    plan, sim_rank, shards, numel, tail_numel = owner_set(w, rank)
+    supp_names = [] if (rank != 0 or args.no_supplementary) else [n for n in W.ORDER if n != w.name]
+
+    # Every gradient buffer is generated before the first CUDA call (a spawn pool).
     t_gen = time.time()
-    grad_np = W.owner_grad_buffer(w, shards, numel)   # before any CUDA call (spawn pool)
+    grad_np = W.owner_grad_buffer(w, shards, numel)
+    supp_inputs = {}
+    for name in supp_names:
+        ws_ = W.get(name)
+        _, _, sh, nm, tn = owner_set(ws_, 0)
+        supp_inputs[name] = (ws_, sh, nm, tn, W.owner_grad_buffer(ws_, sh, nm))
     t_gen = time.time() - t_gen
 
     import torch
@@ -270,103 +463,39 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    stream = torch.cuda.current_stream()
-
-    bf16 = w.grad_dtype == "bf16"
-    grad_host = torch.from_numpy(grad_np.view(np.int16) if bf16 else grad_np).pin_memory()
-    grad_host = grad_host.view(torch.bfloat16) if bf16 else grad_host
-    grad = grad_host.to(dev)
-    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
-    upd = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
-    rng = np.random.default_rng(w.seed)
-    tp = torch.from_numpy((rng.standard_normal(max(tail_numel, 1)) * w.tail_scale).astype(np.float32)).to(dev)
-    tg_host = torch.from_numpy((rng.standard_normal(max(tail_numel, 1)) * w.tail_scale)
-                               .astype(np.float32)).pin_memory()
-    tg = tg_host.to(dev)
-    tm, tv = torch.zeros_like(tp), torch.zeros_like(tp)
-    upd_host = torch.empty(numel, dtype=torch.bfloat16).pin_memory()
-    tp_host = torch.empty_like(tg_host).pin_memory()
-    a, b, c = w.ns_coeffs
-    kw = dict(beta=w.beta, nesterov=w.nesterov, ns_steps=w.ns_steps, coeffs=w.ns_coeffs, eps=w.ns_eps)
-    batches = math.ceil(len(shards) / 128) if shards else 0
-    # per batch of 128 matrices: momentum, norm finalise, one Newton-Schulz launch (or the T = 0 emit)
-    launches_per_step = 3 * batches + (1 if tail_numel else 0)
-
-    step_counter = [0]
-
-    def one_step(ev=None):
-        step_counter[0] += 1
-        if ev:
-            ev[0].record(stream)
-        mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
-        if ev:
-            ev[1].record(stream)
-        mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_NEWTON_SCHULZ, **kw)
-        if ev:
-            ev[2].record(stream)
-        if tail_numel:
-            mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
-                                  wd=w.weight_decay, step=step_counter[0])
-        if ev:
-            ev[3].record(stream)
-
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    st, detail = mfsdp.muon_device_status(ws)
-    if st != mfsdp.OK:
-        raise RuntimeError(f"device status after warm-up: {mfsdp.status_string(st)} ({detail})")
+    peaks, peak_src = load_peaks()
+    barrier = dist.barrier if world > 1 else None
 
     # ---------------------------------------------------------- timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.4)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    gc.collect()
-    gc.disable()            # no collector pause while the host enqueues the timed steps
-    t_start.record(stream)
-    for k in range(args.steps):
-        one_step(evs[k])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    gc.enable()
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    mom_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    ns_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    adam_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
-    steps_ms = sorted(e[0].elapsed_time(e[3]) for e in evs)
+    step = OwnerStep(mfsdp, w, shards, numel, tail_numel, grad_np, dev, pin=True)
+    total_ms, phase_ms, steps_ms, clocks = time_resident(step, args.steps, args.warmup, ClockSampler(local_rank),
+                                                         barrier)
     step_ms = max_over_ranks(total_ms / args.steps, dev)
-    st, detail = mfsdp.muon_device_status(ws)
-    if st != mfsdp.OK:
-        raise RuntimeError(f"device status after timed region: {mfsdp.status_string(st)} ({detail})")
+    phases = figures(mfsdp, step, phase_ms, peaks)
+    phases.update({"step_ms_median": round(statistics.median(steps_ms), 4), "step_ms_min": round(steps_ms[0], 4),
+                   "step_ms_max": round(steps_ms[-1], 4)})
 
     # ---------------------------------------------------------- end to end
     # Through the host-buffer entry point: each step copies the gradient in from
     # pinned host memory and the update back out, shard group by shard group,
     # overlapped with the compute of the neighbouring groups; the AdamW tail's
     # gradient comes in and its parameters go back out too.
+    stream = step.stream
     e2e_steps = max(1, min(args.steps, 10))
-    e2e_groups = mfsdp.host_step_groups(shards, grad.dtype, upd.dtype, args.e2e_groups)[0]
-    h2d = grad_host.numel() * grad_host.element_size() + (tg_host.numel() * 4 if tail_numel else 0)
+    e2e_groups = mfsdp.host_step_groups(shards, step.grad.dtype, step.upd.dtype, args.e2e_groups)[0]
+    upd_host = torch.empty(numel, dtype=torch.bfloat16).pin_memory()
+    tp_host = torch.empty_like(step.tg_host).pin_memory()
+    h2d = step.grad_host.numel() * step.grad_host.element_size() + (step.tg_host.numel() * 4 if tail_numel else 0)
     d2h = upd_host.numel() * 2 + (tp_host.numel() * 4 if tail_numel else 0)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def one_step_host():
-        step_counter[0] += 1
-        mfsdp.muon_owner_step_host(shards, grad_host, grad, mom, upd, upd_host, ws, groups=args.e2e_groups, **kw)
+        step.count += 1
+        mfsdp.muon_owner_step_host(shards, step.grad_host, step.grad, step.mom, step.upd, upd_host, step.ws,
+                                   groups=args.e2e_groups, **step.kw)
         if tail_numel:
-            tg.copy_(tg_host, non_blocking=True)
-            mfsdp.adamw_tail_step(tp, tg, tm, tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1], eps=w.adam_eps,
-                                  wd=w.weight_decay, step=step_counter[0])
-            tp_host.copy_(tp, non_blocking=True)
+            step.tg.copy_(step.tg_host, non_blocking=True)
+            step.adamw()
+            tp_host.copy_(step.tp, non_blocking=True)
 
     # As many untimed warm-up steps as the device-resident measurement: with a
     # single one, the first timed step sometimes took ~200 ms more (a one-off
@@ -379,6 +508,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gc.collect()
     gc.disable()
     e0.record(stream)
@@ -390,47 +520,33 @@ def run_ours(args):
     torch.cuda.synchronize()
     gc.enable()
     e2e_clocks = e2e_sampler.stop()
+    step.check_status("after the end-to-end region")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_steps_ms = [round(step_ev[k].elapsed_time(step_ev[k + 1]), 3) for k in range(e2e_steps)]
 
-    # ---------------------------------------------------------- supplementary: a large AdamW tail
     sup = {}
-    if rank == 0 and not args.no_supplementary:
-        n_big = 50_000_000
-        bp = torch.randn(n_big, device=dev) * 1e-3
-        bg = torch.randn(n_big, device=dev) * 1e-3
-        bm, bv = torch.zeros_like(bp), torch.zeros_like(bp)
-        for i in range(3):
-            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=i + 1)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 10
-        torch.cuda.synchronize()
-        s0.record(stream)
-        for i in range(reps):
-            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=4 + i)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        a_ms = s0.elapsed_time(s1) / reps
-        sup["adamw_50M"] = {"ms": round(a_ms, 4), "gbs": round(28 * n_big / a_ms / 1e6, 1)}
-        del bp, bg, bm, bv
-
     # ---------------------------------------------------------- supplementary: momentum phase alone
     # The momentum phase of this owner set back to back, with no Newton-Schulz launch
     # before it: inside the step it runs at the SM clock the power cap leaves after
     # the GEMMs, here at the clock the memory-bound kernel itself allows.
     if rank == 0 and not args.no_supplementary and shards:
         for _ in range(2):
-            mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
+            mfsdp.muon_owner_step(shards, step.grad, step.mom, step.upd, step.ws, phases=mfsdp.PHASE_MOMENTUM,
+                                  **step.kw)
         torch.cuda.synchronize()
         time.sleep(0.2)
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 5
         s0.record(stream)
         for _ in range(reps):
-            mfsdp.muon_owner_step(shards, grad, mom, upd, ws, phases=mfsdp.PHASE_MOMENTUM, **kw)
+            mfsdp.muon_owner_step(shards, step.grad, step.mom, step.upd, step.ws, phases=mfsdp.PHASE_MOMENTUM,
+                                  **step.kw)
         s1.record(stream)
         torch.cuda.synchronize()
-        sup["momentum_back_to_back"] = {"ms": round(s0.elapsed_time(s1) / reps, 4)}
+        mb_ms = s0.elapsed_time(s1) / reps
+        gbs = phases["momentum_bytes"] / (mb_ms * 1e-3) / 1e9
+        sup["momentum_back_to_back"] = {"ms": round(mb_ms, 4), "gbs": round(gbs, 1),
+                                        "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
 
     # ---------------------------------------------------------- supplementary: owner-segment reduce
     # The reduce that lands every owned matrix on this owner before the step:
@@ -457,41 +573,71 @@ def run_ours(args):
         r_ms = s0.elapsed_time(s1) / reps
         moved = sum(g.numel for g in segs) * 2 * (w.world + 1)
         sup["owner_segment_reduce"] = {"ranks": w.world, "ms": round(r_ms, 4),
-                                       "gbs": round(moved / r_ms / 1e6, 1), "bytes": moved}
+                                       "gbs": round(moved / r_ms / 1e6, 1), "bytes": moved,
+                                       "frac_hbm": round(moved / r_ms / 1e6 / peaks["hbm_gbs"], 4)}
         del srcs, red_dst
 
+    # ---------------------------------------------------------- supplementary: a large AdamW tail
+    if rank == 0 and not args.no_supplementary:
+        n_big = 50_000_000
+        bp = torch.randn(n_big, device=dev) * 1e-3
+        bg = torch.randn(n_big, device=dev) * 1e-3
+        bm, bv = torch.zeros_like(bp), torch.zeros_like(bp)
+        for i in range(3):
+            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=i + 1)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for i in range(reps):
+            mfsdp.adamw_tail_step(bp, bg, bm, bv, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=4 + i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        a_ms = s0.elapsed_time(s1) / reps
+        gbs = 28 * n_big / a_ms / 1e6
+        sup["adamw_50M"] = {"ms": round(a_ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del bp, bg, bm, bv
+
+    # ---------------------------------------------------------- supplementary: the other owner sets
+    # Each of the other workloads' owner sets (the heaviest planner rank),
+    # device-resident, timed the same way as the headline (fewer steps).
+    if supp_names:
+        del step
+        torch.cuda.empty_cache()
+        sup["workloads"] = {}
+        for name in supp_names:
+            ws_, sh, nm, tn, g_np = supp_inputs.pop(name)
+            st_ = OwnerStep(mfsdp, ws_, sh, nm, tn, g_np, dev)
+            k = args.supp_steps
+            tot, pms, sms, clk = time_resident(st_, k, max(args.warmup, 3), ClockSampler(local_rank))
+            fig = figures(mfsdp, st_, pms, peaks)
+            fig.pop("momentum_bytes")
+            sup["workloads"][name] = {"owner_step_ms": round(tot / k, 4),
+                                      "owner_step_ms_median": round(statistics.median(sms), 4),
+                                      "steps": k, "matrices": len(sh), "elements": sum(s.rows * s.cols for s in sh),
+                                      "tail_elems": tn, **fig,
+                                      "sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons")}
+            del st_, g_np
+            torch.cuda.empty_cache()
+
     # ---------------------------------------------------------- figures
-    peaks, peak_src = load_peaks()
-    flops, flops_exec = mfsdp.muon_step_flops(shards, w.ns_steps)
-    elems = sum(s.rows * s.cols for s in shards)
-    gsz = 2 if bf16 else 4
-    mom_bytes = elems * (gsz + 4 + 4 + 2)
-    ns_tflops = flops / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0           # dense-equivalent
-    ns_tflops_exec = flops_exec / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0  # executed MMA work
-    mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
-    adam_gbs = 28 * tail_numel / (adam_ms * 1e-3) / 1e9 if adam_ms > 0 and tail_numel else 0.0
+    ns_launches = math.ceil(len(shards) / 128) if shards else 0
+    flops_exec = phases["flops_executed"]
+    ns_ms = phases["newton_schulz_ms"]
+    ns_tflops_exec = phases["newton_schulz_tflops_executed"]
     peak_tf = peaks["bf16_tflops_sustained"]
-    hbm = peaks["hbm_gbs"]
-    ns_launches = batches
-    if "adamw_50M" in sup:
-        sup["adamw_50M"]["frac_hbm"] = round(sup["adamw_50M"]["gbs"] / hbm, 4)
-    if "momentum_back_to_back" in sup:
-        mb = sup["momentum_back_to_back"]
-        mb["gbs"] = round(mom_bytes / (mb["ms"] * 1e-3) / 1e9, 1)
-        mb["frac_hbm"] = round(mb["gbs"] / hbm, 4)
-    if "owner_segment_reduce" in sup:
-        sup["owner_segment_reduce"]["frac_hbm"] = round(sup["owner_segment_reduce"]["gbs"] / hbm, 4)
+    digest = ns_source_digest()
+    traffic = NS_GEMM_TRAFFIC.get((digest, w.name))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        sample = pick_sample(shards)
-        sec, fl, el = oracle_sample(w, shards, 0, sample)
-        est_ms = sec * 1e3 * flops / fl
-        desc = (f"fp64 NumPy oracle (momentum + Newton-Schulz) on params {sample} "
-                f"{[(s.rows, s.cols) for s in shards if s.param_id in sample]} of the benched owner set, "
-                f"{sec:.1f} s, scaled by dense Newton-Schulz FLOPs to all {len(shards)} matrices")
-        cpu = {"value": round(est_ms, 1), "unit": "ms", "cores": cpu_threads(), "kind": "oracle", "sample": desc}
+        est_ms, desc, sec = oracle_owner_step_estimate(w, shards, tail_numel)
+        cpu = {"value": round(est_ms, 1), "unit": "ms", "cores": cpu_threads(), "kind": "oracle",
+               "estimated": True, "method": "per shape: measured time x count", "sample": desc,
+               "seconds": round(sec, 1), **blas_info()}
 
+    elems = sum(s.rows * s.cols for s in shards)
+    phases.pop("momentum_bytes")
     line = {
         "metric": METRIC, "value": round(step_ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False, "scaling": "weak",
@@ -500,40 +646,39 @@ def run_ours(args):
                    "matrices": len(shards), "elements": elems, "ns_steps": w.ns_steps,
                    "grad_dtype": w.grad_dtype, "update_dtype": "bf16", "tail_elems": tail_numel,
                    "grad_dist": w.grad_dist,
-                   "l2": f"no flush: inputs {(grad_np.nbytes + 4 * numel + ws.numel()) / 1e9:.1f} GB > 129 MB L2",
+                   "l2": f"no flush: inputs {(grad_np.nbytes + 4 * numel) / 1e9:.1f} GB > 129 MB L2",
                    "parallelism": f"owner sets x{world}"},
-        "phases": {"momentum_ms": round(mom_ms, 4), "momentum_gbs": round(mom_gbs, 1),
-                   "momentum_frac_hbm": round(mom_gbs / hbm, 4),
-                   "newton_schulz_ms": round(ns_ms, 4),
-                   "newton_schulz_tflops_executed": round(ns_tflops_exec, 1),
-                   "newton_schulz_frac_bf16_executed": round(ns_tflops_exec / peak_tf, 4),
-                   "newton_schulz_tflops_dense_equivalent": round(ns_tflops, 1),
-                   "newton_schulz_frac_bf16_dense_equivalent": round(ns_tflops / peak_tf, 4),
-                   "flops_dense": flops, "flops_executed": flops_exec,
-                   "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1),
-                   "step_ms_median": round(statistics.median(steps_ms), 4),
-                   "step_ms_min": round(steps_ms[0], 4), "step_ms_max": round(steps_ms[-1], 4)},
-        "roofline": {"kernel": "ns_kernel", "bound": "tensor", "achieved": round(ns_tflops_exec, 1),
+        "phases": phases,
+        "roofline": {"kernel": "ns_kernel", "bound": "tensor", "achieved": ns_tflops_exec,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4),
-                     "traffic": NS_GEMM_TRAFFIC.get((mfsdp.version(), w.name)),
+                     "traffic": traffic, "kernel_digest": digest,
                      "peak_source": f"{peak_src} bf16_tflops_sustained",
                      "flops": "executed tensor-core FLOPs (symmetric Gram/polynomial: upper-triangle blocks only)",
-                     "flops_per_launch": round(flops_exec / max(ns_launches, 1)), "launches_per_step": ns_launches},
+                     "flops_per_launch": round(flops_exec / max(ns_launches, 1)), "launches_per_step": ns_launches,
+                     "ms_per_launch": round(ns_ms / max(ns_launches, 1), 4)},
         "clocks": clocks,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
                 "pipeline_groups": e2e_groups, "steps_ms": e2e_steps_ms,
                 "median_ms": round(statistics.median(e2e_steps_ms), 3), "clocks": e2e_clocks},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": step_launches(shards, tail_numel) * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,
         "input_generation_s": round(t_gen, 1),
+        "library": mfsdp.version(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def step_launches(shards, tail_numel):
+    """Kernels one owner step launches: per batch of 128 matrices the momentum
+    kernel, the norm finalise and one Newton-Schulz launch; one AdamW launch."""
+    batches = math.ceil(len(shards) / 128) if shards else 0
+    return 3 * batches + (1 if tail_numel else 0)
 
 
 def run_kernel_case(args):
@@ -624,6 +769,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b_rank", choices=W.ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-supplementary", action="store_true")
+    ap.add_argument("--supp-steps", type=int, default=10,
+                    help="timed steps of each other workload's owner set in the supplementary lines")
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="shard groups the host-buffer step overlaps copies with (1 = no overlap, "
                          "0 = the library's choice for the owner set)")

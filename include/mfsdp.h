@@ -282,14 +282,18 @@ int32_t mfsdp_host_step_groups(const mfsdp_matrix_shard* shards, int32_t n_shard
  *     mfsdp_muon_workspace_bytes() exceeds MFSDP_STATIC_SCRATCH_BYTES is
  *     rejected with MFSDP_ERR_WORKSPACE_TOO_SMALL before anything runs.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     device's current CUDA context; a call in another context of the device
+ *     (a new primary context after cudaDeviceReset, or a context the caller
+ *     made current) looks it up again.  Make the first call on a device, in
+ *     each context, before any stream capture on it.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents (the step clears what must start at zero itself).  Calls whose
  *     work overlaps on the GPU (different streams, or different host threads
  *     without ordering) race on it: serialise them.
- *   - The device status word of these calls is not readable through
- *     mfsdp_muon_device_status (the caller holds no workspace pointer). */
+ *   - Its device status word (a bounded wait that gave up, see
+ *     mfsdp_muon_device_status) sits at the start of the array, out of the
+ *     caller's reach: read it with mfsdp_muon_static_scratch_status. */
 #define MFSDP_STATIC_SCRATCH_BYTES (64u << 20)
 int mfsdp_muon_owner_step_static_scratch(const mfsdp_matrix_shard* shards, int32_t n_shards,
                                          const void* grad, int32_t grad_dtype,
@@ -299,6 +303,15 @@ int mfsdp_muon_owner_step_static_scratch(const mfsdp_matrix_shard* shards, int32
                                          double beta, int32_t nesterov, int32_t ns_steps,
                                          double a, double b, double c, double eps,
                                          void* stream);
+
+/* The device status word of the last mfsdp_muon_owner_step_static_scratch
+ * call on the current device (no counterpart in the paper).  Like
+ * mfsdp_muon_device_status -- same return values and *detail encoding, and it
+ * synchronises `stream` -- but it reads the library's scratch array, so queue
+ * it on the stream of the call it reports on, after that call.  Returns
+ * MFSDP_OK when no static-scratch call ran yet on the device (the array starts
+ * zeroed), and CUDA when the array's address cannot be looked up. */
+int mfsdp_muon_static_scratch_status(void* stream, int32_t* detail);
 
 /* FLOP counts of mfsdp_muon_owner_step for these shards, host only:
  * *dense = sum over matrices of ns_steps * (4 s^2 l + 2 s^3) (the algorithmic
@@ -313,8 +326,12 @@ int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, in
 /* Reads the device status word a previous mfsdp_muon_owner_step left in
  * `workspace` (synchronising `stream`): MFSDP_OK, or MFSDP_ERR_DEVICE_TIMEOUT
  * if one of its kernels gave up on a bounded wait (its outputs are then
- * undefined).  Every wait of the Newton-Schulz kernel gives up after 2 s; the
- * first one to do so records the word and every other CTA then stops too.
+ * undefined).  Every wait of a Newton-Schulz launch gives up after its limit:
+ * 2 s, or, for launches whose largest product (Gram, polynomial or update,
+ * summed over the launch's matrices) would take longer than 2 s / 8 with
+ * every CTA pair at a quarter of its bf16 tensor peak at 1 GHz, 8x that time
+ * (at most an hour).  The first wait to give up records the word and every
+ * other CTA then stops too.
  * *detail (may be NULL) receives the raw word: bits 0-7 the waiting role
  * (1 producer: a free pipeline stage; 2 MMA issuer: a stage's operands;
  * 3 MMA issuer: a drained accumulator; 4 epilogue: a finished accumulator;

@@ -41,7 +41,7 @@ EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
             "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
             "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall",
-            "mfsdp_host_step_groups")
+            "mfsdp_host_step_groups", "mfsdp_muon_static_scratch_status")
 
 SEGMENT_REDUCE = 0
 SEGMENT_GATHER = 1
@@ -108,6 +108,8 @@ _lib.mfsdp_muon_step_flops.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, 
 _lib.mfsdp_muon_step_flops.restype = ctypes.c_int
 _lib.mfsdp_muon_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
 _lib.mfsdp_muon_device_status.restype = ctypes.c_int
+_lib.mfsdp_muon_static_scratch_status.argtypes = [_vp, ctypes.POINTER(_i32)]
+_lib.mfsdp_muon_static_scratch_status.restype = ctypes.c_int
 _lib.mfsdp_test_inject_stall.argtypes = [_i32]
 _lib.mfsdp_test_inject_stall.restype = ctypes.c_int
 _lib.mfsdp_adamw_tail_step.argtypes = [_vp, _vp, _vp, _vp, _i64, _d, _d, _d, _d, _d, _i64, _vp]
@@ -397,6 +399,14 @@ def test_inject_stall(tile: int) -> None:
 def muon_device_status(workspace, stream=None) -> Tuple[int, int]:
     detail = _i32(0)
     st = _lib.mfsdp_muon_device_status(_ptr(workspace), _stream(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def muon_static_scratch_status(stream=None) -> Tuple[int, int]:
+    """(status, raw word) of the last static-scratch step on the current device
+    (synchronises the stream; see include/mfsdp.h)."""
+    detail = _i32(0)
+    st = _lib.mfsdp_muon_static_scratch_status(_stream(stream), ctypes.byref(detail))
     return st, detail.value
 
 

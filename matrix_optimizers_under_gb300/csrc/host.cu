@@ -763,6 +763,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
     nb.norm = norm;
     nb.ws = ws;
     nb.status = status;
+    nb.wait_limit_ns = 0;   // set by launch_ns from the launch's products and the device's CTA pairs
     nb.next_tile = counters;
     nb.done = counters + 1 + base;
     if (apply) {

@@ -128,6 +128,7 @@ struct NsBatch {
   const float2* norm;
   const uint8_t* ws;     // workspace base: tensor-copy row y is byte 128 y of it
   int32_t* status;       // device status word (first wait that gave up)
+  uint64_t wait_limit_ns;  // every wait of the launch gives up after this long (ns_wait_limit_ns)
   int32_t* next_tile;    // tiles handed out so far (dynamic schedule), zeroed before the launch
   int32_t* done;         // per matrix of the launch, zeroed before it
   int32_t tile_start[3][kMaxBatch + 1];

@@ -89,7 +89,7 @@
 namespace mfsdp {
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: the floor of every wait's limit, and the drains' limit
 constexpr uint32_t kAccCols = 256;     // one fp32 accumulator of 128 lanes x 256 columns
 constexpr uint32_t kTmemCols = 512;    // two accumulators: epilogue of tile i overlaps the MMAs of tile i+1
 constexpr int32_t kArrivalsPerTile = 2 * kEpilogueWarps;   // completion-counter adds per pair tile
@@ -303,40 +303,47 @@ __device__ __forceinline__ int32_t ws_row(const NsBatch& p, const uint8_t* src) 
 
 __device__ __forceinline__ int32_t wait_code(int phase, int role) { return (phase << 8) | role; }
 
+// What a bounded wait needs: the CTA's abort flag (another role of this CTA
+// gave up), the launch's status word (another CTA recorded a failure) and the
+// launch's wait limit (NsBatch::wait_limit_ns).
+struct Abort {
+  volatile int* flag;
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
 // Called between polls of a wait: true when the wait must be abandoned --
 // another role of this CTA gave up, another CTA recorded a failure, or this
-// wait has run for kWaitLimitNs (then it records `code`).
-__device__ __forceinline__ bool give_up(volatile int* abort_flag, int32_t* status, uint64_t t0, int32_t code) {
-  if (*abort_flag) return true;
-  if (*reinterpret_cast<volatile int32_t*>(status) != 0) {
-    *abort_flag = 1;
+// wait has run for the launch's limit (then it records `code`).
+__device__ __forceinline__ bool give_up(const Abort& ab, uint64_t t0, int32_t code) {
+  if (*ab.flag) return true;
+  if (*reinterpret_cast<volatile int32_t*>(ab.status) != 0) {
+    *ab.flag = 1;
     return true;
   }
-  if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-    *abort_flag = 1;
-    atomicCAS(status, 0, code);
+  if (ptx::globaltimer_ns() - t0 > ab.limit_ns) {
+    *ab.flag = 1;
+    atomicCAS(ab.status, 0, code);
     return true;
   }
   return false;
 }
 
 // Bounded mbarrier wait.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
-                                              int32_t code) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const Abort& ab, int32_t code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (give_up(abort_flag, status, t0, code)) return false;
+    if (give_up(ab, t0, code)) return false;
   }
 }
 
 // Bounded wait until a matrix's completion counter reaches `need` (acquire:
 // the stores it counts are visible to this thread afterwards).
-__device__ __forceinline__ bool wait_done(const int32_t* ctr, int32_t need, volatile int* abort_flag, int32_t* status,
-                                          int32_t code) {
+__device__ __forceinline__ bool wait_done(const int32_t* ctr, int32_t need, const Abort& ab, int32_t code) {
   if (ptx::ld_acquire_gpu(ctr) >= need) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
@@ -345,21 +352,20 @@ __device__ __forceinline__ bool wait_done(const int32_t* ctr, int32_t need, vola
       __nanosleep(64);
       if (ptx::ld_acquire_gpu(ctr) >= need) return true;
     }
-    if (give_up(abort_flag, status, t0, code)) return false;
+    if (give_up(ab, t0, code)) return false;
   }
 }
 
 // Bounded wait on an mbarrier that another CTA of the pair arrives on
 // (acquire at cluster scope).
-__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                      int32_t* status, int32_t code) {
+__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, const Abort& ab, int32_t code) {
   if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
-    if (give_up(abort_flag, status, t0, code)) return false;
+    if (give_up(ab, t0, code)) return false;
   }
 }
 
@@ -376,30 +382,27 @@ struct Ring {
 };
 
 // CTA-local ring: the scheduler stores tile t into slot seq for this CTA's roles.
-__device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32_t t, volatile int* abort_flag,
-                                             int32_t* status) {
+__device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab) {
   const uint32_t k = seq % kTileRing, use = seq / kTileRing;
-  if (!wait_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, abort_flag, status, wait_code(0, kRoleTileFree))) return false;
+  if (!wait_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, ab, wait_code(0, kRoleTileFree))) return false;
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(r.slot0 + 4u * k), "r"(t) : "memory");
   ptx::mbar_arrive(r.full0 + 8u * k);   // releases the store (CTA scope)
   return true;
 }
 
 // A role takes the tile of sequence number seq from its CTA's ring.
-__device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t& t, volatile int* abort_flag,
-                                          int32_t* status) {
+__device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab) {
   const uint32_t k = seq % kTileRing, use = seq / kTileRing;
-  if (!wait_or_abort(r.full0 + 8u * k, use & 1, abort_flag, status, wait_code(0, kRoleTileFull))) return false;
+  if (!wait_or_abort(r.full0 + 8u * k, use & 1, ab, wait_code(0, kRoleTileFull))) return false;
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
   ptx::mbar_arrive(r.empty0 + 8u * k);
   return true;
 }
 
 // Pair ring, even CTA's scheduler side: stores tile t into the odd CTA's slot seq.
-__device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_t t, volatile int* abort_flag,
-                                            int32_t* status) {
+__device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab) {
   const uint32_t k = seq % kPairRing, use = seq / kPairRing;
-  if (!wait_cluster_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, abort_flag, status, wait_code(0, kRoleTileFree)))
+  if (!wait_cluster_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, ab, wait_code(0, kRoleTileFree)))
     return false;
   ptx::st_shared_cluster_s32(ptx::mapa_shared(r.slot0 + 4u * k, 1), t);
   ptx::mbar_arrive_cluster(ptx::mapa_shared(r.full0 + 8u * k, 1));   // releases the store (cluster scope)
@@ -407,10 +410,9 @@ __device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_
 }
 
 // Pair ring, odd CTA's scheduler side.
-__device__ __forceinline__ bool pair_take(const Ring& r, uint32_t seq, int32_t& t, volatile int* abort_flag,
-                                         int32_t* status) {
+__device__ __forceinline__ bool pair_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab) {
   const uint32_t k = seq % kPairRing, use = seq / kPairRing;
-  if (!wait_cluster_or_abort(r.full0 + 8u * k, use & 1, abort_flag, status, wait_code(0, kRoleTileFull))) return false;
+  if (!wait_cluster_or_abort(r.full0 + 8u * k, use & 1, ab, wait_code(0, kRoleTileFull))) return false;
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
   ptx::mbar_arrive_cluster(ptx::mapa_shared(r.empty0 + 8u * k, 0));
   return true;
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   ptx::cluster_sync();    // both CTAs' barriers exist before any multicast or remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
-  volatile int* abort_v = &abort_flag;
+  const Abort ab{&abort_flag, p.status, p.wait_limit_ns};
 
   if (warp == 0) {
     if (lane == 0) {
@@ -488,7 +490,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       bool ok = true;
       while (ok) {
         int32_t t;
-        ok = local_take(ring, seq++, t, abort_v, p.status);
+        ok = local_take(ring, seq++, t, ab);
         if (!ok || t >= p.tile_end) break;
         const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           const int s = it % kStages;
           const uint32_t use = it / kStages;
           // stage s is free: the pair MMA has read both CTAs' halves of its last use
-          ok = wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, abort_v, p.status,
+          ok = wait_or_abort(ptx::smem_u32(&empty_bar[s]), (use & 1) ^ 1, ab,
                              wait_code(tl.phase, kRoleStageFree));
           if (!ok) break;
           const uint32_t fb_local = ptx::smem_u32(&full_bar[s]);
@@ -547,14 +549,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       bool ok = true;
       while (ok) {
         int32_t t;
-        ok = local_take(ring, seq++, t, abort_v, p.status);
+        ok = local_take(ring, seq++, t, ab);
         if (!ok || t >= p.tile_end) break;
         if (rank != 0) continue;
         const Tile tl = decode_tile(p, t, rank);
         if (tl.zero) continue;
         const uint32_t a = acc_it & 1, ause = acc_it >> 1;
         // both CTAs' epilogues have drained accumulator a
-        ok = wait_cluster_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, abort_v, p.status,
+        ok = wait_cluster_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, ab,
                                    wait_code(tl.phase, kRoleAccFree));
         if (!ok) break;
         ptx::tc_fence_after();
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         for (int kb = 0; kb < tl.k_blocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t use = it / kStages;
-          ok = wait_or_abort(ptx::smem_u32(&full_bar[s]), use & 1, abort_v, p.status,
+          ok = wait_or_abort(ptx::smem_u32(&full_bar[s]), use & 1, ab,
                              wait_code(tl.phase, kRoleStageFull));
           if (!ok) break;
           ptx::tc_fence_after();
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
     while (true) {
       int32_t t = 0;
       int got_tile = 1;
-      if (lane == 0) got_tile = local_take(ring, seq, t, abort_v, p.status);
+      if (lane == 0) got_tile = local_take(ring, seq, t, ab);
       ++seq;
       t = __shfl_sync(0xffffffffu, t, 0);
       if (!__shfl_sync(0xffffffffu, got_tile, 0) || t >= p.tile_end) break;
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       uint4 xin[4];
       if (has_c) load_chunk(tl.c_in, stride, row_off, m, tl.n0 + c0, xin);
       const uint32_t a = acc_it & 1, ause = acc_it >> 1;
-      const bool got = wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, abort_v, p.status,
+      const bool got = wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, ab,
                                      wait_code(tl.phase, kRoleAccFull));
       if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
@@ -728,14 +730,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
             const Tile tl = decode_tile(p, t, 0);
             const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
             if (!tl.zero && need > 0 &&
-                !wait_done(p.done + tl.mi, need, abort_v, p.status, wait_code(tl.phase, kRoleDependency)))
+                !wait_done(p.done + tl.mi, need, ab, wait_code(tl.phase, kRoleDependency)))
               break;
           }
-          if (!pair_publish(pair, seq, t, abort_v, p.status)) break;
+          if (!pair_publish(pair, seq, t, ab)) break;
         } else {
-          if (!pair_take(pair, seq, t, abort_v, p.status)) break;
+          if (!pair_take(pair, seq, t, ab)) break;
         }
-        if (!local_publish(ring, seq++, t, abort_v, p.status) || t >= p.tile_end) break;
+        if (!local_publish(ring, seq++, t, ab) || t >= p.tile_end) break;
       }
     }
     __syncwarp();
@@ -809,6 +811,32 @@ cudaError_t resident_pairs(int dev, int* out) {
   return cudaSuccess;
 }
 
+// The wait limit of one launch.  The longest legitimate wait is a tile's
+// wait for the earlier products of its matrix (and its pair's roles waiting
+// behind it for the tile): those products sit before it in the product-major
+// tile list, so it ends once the machine has worked through at most one whole
+// product of every matrix of the launch.  The limit is 8x the largest such
+// product's executed FLOPs at a conservative rate -- every CTA pair at a
+// quarter of its tensor peak (16384 bf16 FLOP per clock) at 1 GHz -- and never
+// below 2 s (nor above an hour).  Only launches whose largest product runs for
+// more than ~0.1 s (short sides in the tens of thousands) get more than 2 s.
+uint64_t wait_limit_ns(const NsBatch& b, int pairs) {
+  double prod[3] = {0.0, 0.0, 0.0};
+  for (int i = 0; i < b.n; ++i) {
+    const NsMat& d = b.mat[i];
+    const double tile = 2.0 * kPairM * kPairM;   // FLOPs of one 256 x 256 output tile per unit of K
+    prod[kGram] += d.tiles_sym * tile * d.l_pad;
+    prod[kPoly] += d.tiles_sym * tile * d.s_pad;
+    prod[kUpdate] += 2.0 * d.s_pad * (double)d.s_pad * d.l_pad;
+  }
+  const double worst = prod[0] > prod[1] ? (prod[0] > prod[2] ? prod[0] : prod[2]) : (prod[1] > prod[2] ? prod[1] : prod[2]);
+  const double rate = (double)(pairs > 0 ? pairs : 1) * 16384.0 * 0.25 * 1e9;   // FLOP/s
+  double ns = 8.0 * worst / rate * 1e9;
+  if (ns < (double)kWaitLimitNs) ns = (double)kWaitLimitNs;
+  if (ns > 3.6e12) ns = 3.6e12;
+  return (uint64_t)ns;
+}
+
 }  // namespace
 
 // The whole workspace as a 2-D tensor of 128-byte rows, with two boxes: 128
@@ -856,7 +884,9 @@ cudaError_t launch_ns(const NsBatch& b, size_t ws_bytes, cudaStream_t s) {
   cfg.numAttrs = 1;
   const int clusters = total_tiles < max_clusters ? total_tiles : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, ns_kernel, b, tmap_8k, tmap_16k);
+  NsBatch lb = b;
+  lb.wait_limit_ns = wait_limit_ns(b, clusters);
+  e = cudaLaunchKernelEx(&cfg, ns_kernel, lb, tmap_8k, tmap_16k);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

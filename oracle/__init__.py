@@ -19,7 +19,7 @@ cases and invariances; momentum against its closed forms at steps 1 and 2;
 AdamW against its closed-form first step and torch.optim.AdamW; the planner
 against brute force, Graham's LPT bound and a hand-worked layout.
 """
-from .planner import plan_owners_ref, lpt_makespan_ref  # noqa: F401
+from .planner import plan_owners_ref, heaviest_rank_ref  # noqa: F401
 from .muon import (bf16_bits_to_f64, momentum_ref, newton_schulz_ref,  # noqa: F401
                    muon_owner_step_ref, muon_matrix_ref, muon_scale_ref, muon_apply_ref)
 from .adamw import adamw_ref  # noqa: F401

@@ -93,15 +93,6 @@ def plan_owners_ref(params: Sequence[Tuple[int, int, int]], world: int, ns_steps
                 rank_tail_elems=text, rank_cost=load, rank_tail_numel=tload)
 
 
-def lpt_makespan_ref(costs: Sequence[int], world: int) -> int:
-    """Makespan of the matrix pass alone (max per-rank cost) for a cost list."""
-    load = [0] * world
-    for i in sorted(range(len(costs)), key=lambda i: (-costs[i], i)):
-        r = min(range(world), key=lambda r: (load[r], r))
-        load[r] += costs[i]
-    return max(load)
-
-
 def heaviest_rank_ref(plan: Dict[str, object]) -> int:
     """The rank a benchmark of one owner set uses: largest matrix cost, then the
     smallest tail, then the lowest rank id (reading; the pages name no rank)."""

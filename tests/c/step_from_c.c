@@ -1,7 +1,7 @@
 /* An owner step from plain C with the CUDA runtime: device buffers from
  * cudaMalloc, one call of mfsdp_muon_owner_step and one of the no-workspace
- * entry point on the default stream, no other framework.  Checks the device
- * status, that every update element is finite and that each matrix's update
+ * entry point on the default stream, no other framework.  Checks both device
+ * status words, that every update element is finite and that each matrix's update
  * has the Frobenius norm Newton-Schulz gives a full-rank input (its singular
  * values lie in [0.68, 1.14], so ||O||_F / sqrt(s) does too), and that the two
  * entry points agree bit for bit.  Prints "ok" and returns 0, or names the
@@ -80,6 +80,7 @@ int main(void) {
   CHECK(mfsdp_muon_device_status(ws, NULL, &detail) == MFSDP_OK);
   CHECK(mfsdp_muon_owner_step_static_scratch(m, n_m, g, MFSDP_DTYPE_BF16, mom2, u2, MFSDP_DTYPE_BF16, n, 0.95, 0, 5,
                                              3.4445, -4.7750, 2.0315, 1e-7, NULL) == MFSDP_OK);
+  CHECK(mfsdp_muon_static_scratch_status(NULL, &detail) == MFSDP_OK);
   CHECK(cudaDeviceSynchronize() == cudaSuccess);
   CHECK(cudaMemcpy(u_host, u, (size_t)n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);
   CHECK(cudaMemcpy(u2_host, u2, (size_t)n * 2, cudaMemcpyDeviceToHost) == cudaSuccess);

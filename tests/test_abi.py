@@ -329,3 +329,14 @@ def test_device_status_error_paths(mfsdp):
     lib = mfsdp.raw_lib()
     detail = ctypes.c_int32(7)
     assert lib.mfsdp_muon_device_status(None, None, ctypes.byref(detail)) == mfsdp.ERR_INVALID_ARG
+
+
+def test_static_scratch_status_without_device(mfsdp):
+    """With no usable GPU the static-scratch status query cannot look up its
+    array and reports a CUDA error (it never reads a host-side stand-in)."""
+    import ctypes
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    detail = ctypes.c_int32(7)
+    assert mfsdp.raw_lib().mfsdp_muon_static_scratch_status(None, ctypes.byref(detail)) == mfsdp.ERR_CUDA

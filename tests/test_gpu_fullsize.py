@@ -1,13 +1,20 @@
 """Full-size parity: the large owner sets run on the GPU exactly as bench.py runs
-them (one call of the owner step over the whole owner set, bf16 update), and a
-sample of their matrices -- one of every shape and orientation, plus all-zero
-experts -- is checked against the fp64 oracle; the sampled matrices are also
-re-run standalone and must match bit for bit (MatrixFSDP -- Abstract: the
-update matches full-matrix Muon).  The AdamW tail is checked element by element
-at its full size.
+them (one call of the owner step over the whole owner set, bf16 update).
 
-These need minutes of oracle time on the host cores; they are marked slow as
-well as gpu.
+  * Against the fp64 oracle: from every launch of the set (128 matrices per
+    launch, in shard order) the first matrix of every shape and up to two
+    all-zero matrices.  Each sampled update is checked as a whole (relative
+    Frobenius error) and block by block: every 128 x 128 block within the
+    block bounds, so that one wrong tile cannot hide in a whole-matrix norm.
+  * Against itself run alone: every matrix of the set is run again as a
+    one-matrix owner set at the same offsets, and the whole update and
+    momentum buffers must match the owner-set run bit for bit (MatrixFSDP --
+    Abstract: the update matches full-matrix Muon).  A batch-offset or
+    scheduling mistake in the second or third launch of the MoE set changes
+    bits even where it stays within the oracle's tolerance.
+
+The AdamW tail is checked element by element at its full size.  These need
+minutes of oracle time on the host cores; they are marked slow as well as gpu.
 """
 import numpy as np
 import pytest
@@ -20,19 +27,38 @@ torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 A, B, C = W.NS_COEFFS
+LAUNCH = 128   # matrices per Newton-Schulz launch (the library's batch)
 
 
 def _sample(shards, w):
-    """One matrix per (rows, cols), the first in the owner set, plus up to two zero matrices."""
-    seen, out = set(), []
-    for s in shards:
-        if s.param_id in w.zero_params:
-            continue
-        if (s.rows, s.cols) not in seen:
-            seen.add((s.rows, s.cols))
-            out.append(s)
-    out += [s for s in shards if s.param_id in w.zero_params][:2]
+    """Per launch (runs of LAUNCH shards in the order given): the first matrix
+    of every (rows, cols) and up to two all-zero matrices."""
+    out = []
+    for base in range(0, len(shards), LAUNCH):
+        seen = set()
+        batch = shards[base:base + LAUNCH]
+        for s in batch:
+            if s.param_id not in w.zero_params and (s.rows, s.cols) not in seen:
+                seen.add((s.rows, s.cols))
+                out.append(s)
+        out += [s for s in batch if s.param_id in w.zero_params][:2]
     return out
+
+
+def _standalone_matches(mfsdp, shards, grad, mom, upd, kw):
+    """Every shard run alone, at its own offset of the same buffers: the whole
+    update and momentum buffers equal the owner-set run's bit for bit."""
+    dev = grad.device
+    mom1 = torch.zeros_like(mom)
+    upd1 = torch.zeros_like(upd)
+    ws1 = torch.empty(max(mfsdp.muon_workspace_bytes([s]) for s in shards), dtype=torch.uint8, device=dev)
+    for s in shards:
+        mfsdp.muon_owner_step([s], grad, mom1, upd1, ws1, **kw)
+    st, detail = mfsdp.muon_device_status(ws1)
+    assert st == mfsdp.OK, (st, detail)
+    torch.cuda.synchronize()
+    assert torch.equal(upd1.view(torch.int16), upd.view(torch.int16)), "update differs from the standalone runs"
+    assert torch.equal(mom1.view(torch.int32), mom.view(torch.int32)), "momentum differs from the standalone runs"
 
 
 @pytest.mark.parametrize("name", ["llama_1p3b_rank", "llama3_8b_rank", "moe_skewed"])
@@ -56,9 +82,15 @@ def test_full_owner_set(mfsdp, name):
     assert st == mfsdp.OK, (st, detail)
     torch.cuda.synchronize()
     del ws
+    _standalone_matches(mfsdp, shards, grad, mom, upd, kw)
 
     errs = {}
-    for s in _sample(shards, w):
+    sample = _sample(shards, w)
+    if len(shards) > LAUNCH:   # the sample reaches every launch
+        index = {s.param_id: i for i, s in enumerate(shards)}
+        launches = {index[s.param_id] // LAUNCH for s in sample if s.param_id not in w.zero_params}
+        assert launches == set(range(-(-len(shards) // LAUNCH))), launches
+    for s in sample:
         n = s.rows * s.cols
         seg = slice(s.offset, s.offset + n)
         O = upd[seg].float().cpu().numpy().astype(np.float64).reshape(s.rows, s.cols)
@@ -69,18 +101,9 @@ def test_full_owner_set(mfsdp, name):
         if s.param_id in w.zero_params:
             assert np.all(O == 0.0)
             continue
-        errs[(s.rows, s.cols)] = H.rel_fro(O, O_ref)
-        assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
-        # standalone run of the same matrix: bitwise the same update
-        alone = [mfsdp.make_shard(0, s.rows, s.cols, param_id=s.param_id)]
-        g1 = grad[seg].clone()
-        m1 = torch.zeros(n, dtype=torch.float32, device=dev)
-        u1 = torch.zeros(n, dtype=torch.bfloat16, device=dev)
-        ws1 = torch.empty(mfsdp.muon_workspace_bytes(alone), dtype=torch.uint8, device=dev)
-        mfsdp.muon_owner_step(alone, g1, m1, u1, ws1, **kw)
-        torch.cuda.synchronize()
-        assert torch.equal(u1.view(torch.int16), upd[seg].view(torch.int16)), s.param_id
-        del g1, m1, u1, ws1
+        errs[s.param_id] = H.rel_fro(O, O_ref)
+        assert errs[s.param_id] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
+        H.check_blocks(O, O_ref, f"param {s.param_id} {s.rows}x{s.cols}")
     print(name, {k: round(v, 5) for k, v in errs.items()})
 
 
@@ -145,6 +168,7 @@ def test_full_owner_set_second_step_fp32_update(mfsdp):
         assert np.all(np.isfinite(O)), s.param_id
         errs[(s.rows, s.cols)] = H.rel_fro(O, O_ref)
         assert errs[(s.rows, s.cols)] <= H.ns_tol(s.rows, s.cols), (s.param_id, errs)
+        H.check_blocks(O, O_ref, f"param {s.param_id} {s.rows}x{s.cols}")
     print({k: round(v, 5) for k, v in errs.items()})
 
 

@@ -59,3 +59,37 @@ def test_bounded_wait_gives_up_and_reports(mfsdp):
     upd_np, mom_np, _ = run_step(mfsdp, shards, grad_np, np.zeros(numel, np.float32), update_dtype=torch.float32)
     for s in shards:
         check_matrix(s, upd_np, mom_np, grad_np, np.zeros(numel, np.float32), ns_steps=w.ns_steps)
+
+
+def test_static_scratch_timeout_is_reported(mfsdp):
+    """The static-scratch entry point keeps its status word in the library's
+    scratch array, out of the caller's reach: a bounded wait that gives up
+    there is read back with mfsdp_muon_static_scratch_status, and the next
+    call on the same array succeeds and clears it."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    w = W.get("tiny")
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    r = H.heaviest_rank(plan)
+    shards, numel = plan.rank_matrices(r), plan.rank_matrix_elems[r]
+    grad_np = H.build_grad_buffer(w, shards, numel)
+    grad = torch.from_numpy(grad_np).to(dev)
+    kw = dict(beta=w.beta, ns_steps=w.ns_steps, coeffs=W.NS_COEFFS, eps=W.NS_EPS)
+
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.float32, device=dev)
+    mfsdp.test_inject_stall(0)
+    mfsdp.muon_owner_step_static_scratch(shards, grad, mom, upd, **kw)
+    st, detail = mfsdp.muon_static_scratch_status()     # synchronises
+    assert st == mfsdp.ERR_DEVICE_TIMEOUT, (st, detail)
+    assert detail & 0xFF in (ROLE_DEPENDENCY, ROLE_TILE_FULL), detail
+
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.float32, device=dev)
+    mfsdp.muon_owner_step_static_scratch(shards, grad, mom, upd, **kw)
+    st, detail = mfsdp.muon_static_scratch_status()
+    assert st == mfsdp.OK, (st, detail)
+    zeros = np.zeros(numel, np.float32)
+    for s in shards:
+        check_matrix(s, upd.cpu().numpy(), mom.cpu().numpy(), grad_np, zeros, ns_steps=w.ns_steps)

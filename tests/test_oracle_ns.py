@@ -173,3 +173,58 @@ def test_apply_special_cases():
     np.testing.assert_allclose(muon_apply_ref(W, np.zeros_like(O), 0.02, 0.5, 7.0), 0.99 * W, rtol=1e-15)
     # one step on W = O with lr*wd = 0 and scale = 1/lr cancels exactly
     np.testing.assert_allclose(muon_apply_ref(O, O, 0.5, 0.0, 2.0), 0 * O, atol=1e-15)
+
+
+def test_bf16_bits_to_f64_ieee_values():
+    """bf16 is the top half of an IEEE binary32: sign, 8 exponent bits, 7
+    fraction bits.  Values fixed by that definition, including the smallest
+    subnormal and the largest finite value."""
+    from oracle import bf16_bits_to_f64
+    bits = np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x4049, 0x3F81, 0x0001, 0x0080, 0x7F7F, 0x7F80, 0xFF80],
+                    np.uint16)
+    want = np.array([0.0, -0.0, 1.0, -1.0, 3.140625, 1 + 2.0 ** -7, 2.0 ** -133, 2.0 ** -126,
+                     (2 - 2.0 ** -7) * 2.0 ** 127, np.inf, -np.inf])
+    got = bf16_bits_to_f64(bits)
+    assert got.dtype == np.float64
+    assert np.array_equal(got, want) and np.signbit(got[1])
+    assert np.isnan(bf16_bits_to_f64(np.array([0x7FC1], np.uint16)))[0]
+
+
+def test_owner_step_over_a_flat_buffer():
+    """The flat-buffer owner step: two matrices (one wide, one tall) at ragged
+    offsets of one buffer, with padding between and after them.  Each matrix's
+    update is the SVD closed form of its own momentum-smoothed slice, its
+    momentum is beta M + G on that slice, and every padding element of the
+    momentum buffer comes back unchanged; `only` restricts the work."""
+    from oracle.muon import muon_owner_step_ref, stored_to_f64
+    rng = np.random.default_rng(21)
+    shapes, offsets = [(6, 10), (12, 5)], [3, 3 + 60 + 4]
+    numel = offsets[1] + 60 + 7
+    G32 = (rng.standard_normal(numel) * 1e-2).astype(np.float32)
+    bits = (G32.view(np.uint32) >> 16).astype(np.uint16)        # truncated to bf16: exact bf16 values
+    M0 = rng.standard_normal(numel)
+    shards = [dict(param_id=i, offset=o, rows=r, cols=c) for i, ((r, c), o) in enumerate(zip(shapes, offsets))]
+    beta = 0.9
+    for dtype, buf in (("f32", G32), ("bf16", bits)):
+        Gall = stored_to_f64(buf, dtype)
+        if dtype == "bf16":
+            assert np.array_equal(Gall, ((bits.astype(np.uint32) << 16).view(np.float32)).astype(np.float64))
+        else:
+            assert np.array_equal(Gall, G32.astype(np.float64))
+        M, out = muon_owner_step_ref(shards, buf, dtype, M0, beta, False, 5, A, B, C, EPS)
+        used = np.zeros(numel, bool)
+        for sh in shards:
+            o, r, c = sh["offset"], sh["rows"], sh["cols"]
+            used[o:o + r * c] = True
+            G = Gall[o:o + r * c].reshape(r, c)
+            Mi = beta * M0[o:o + r * c].reshape(r, c) + G
+            np.testing.assert_allclose(M[o:o + r * c].reshape(r, c), Mi, rtol=1e-15, atol=0)
+            assert out[sh["param_id"]].shape == (r, c)
+            np.testing.assert_allclose(out[sh["param_id"]], svd_closed_form(Mi, 5, EPS), atol=1e-12, rtol=0)
+        assert np.array_equal(M[~used], M0[~used])
+    M, out = muon_owner_step_ref(shards, G32, "f32", M0, beta, False, 5, A, B, C, EPS, only=[1])
+    assert list(out) == [1]
+    o = offsets[0]
+    assert np.array_equal(M[o:o + 60], M0[o:o + 60])
+    with pytest.raises(ValueError):
+        stored_to_f64(G32, "f16")

@@ -59,6 +59,19 @@ def test_static_scratch_matches_workspace_entry_point(mfsdp):
             seg = slice(s.offset, s.offset + s.rows * s.cols)
             assert torch.equal(upd_new[seg].view(torch.int16), upd_ref[seg].view(torch.int16)), (step, s.param_id)
             assert torch.equal(mom_new[seg].view(torch.int32), mom_ref[seg].view(torch.int32)), (step, s.param_id)
+        st, detail = mfsdp.muon_static_scratch_status()
+        assert st == mfsdp.OK, (step, st, detail)
+
+    # A further call allocates nothing: torch's allocator and the device's free
+    # memory are the same before and after it.
+    g = _grads(w, shards, numel, 2)
+    upd_new = torch.zeros(numel, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(dev), torch.cuda.mem_get_info(dev)[0]
+    mfsdp.muon_owner_step_static_scratch(shards, g, mom_new, upd_new, **kw)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert torch.cuda.mem_get_info(dev)[0] == free0
 
     # an owner set whose scratch exceeds the fixed array is refused up front
     big = [mfsdp.make_shard(0, 4096, 4096)]
