@@ -238,7 +238,9 @@ def cpu_threads():
 
 
 def blas_info():
-    """BLAS library and thread count NumPy uses (for the CPU-baseline record)."""
+    """BLAS library and thread count NumPy uses (for the CPU-baseline record):
+    from threadpoolctl where it is installed, else NumPy's build configuration
+    and the usual thread-count variables."""
     try:
         from threadpoolctl import threadpool_info
         info = [i for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -246,7 +248,17 @@ def blas_info():
             return {"blas": info[0].get("internal_api"), "threads": info[0].get("num_threads")}
     except Exception:
         pass
-    return {"blas": None, "threads": None}
+    blas = None
+    try:
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]["name"]
+    except Exception:
+        pass
+    threads = None
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            threads = int(os.environ[var])
+            break
+    return {"blas": blas, "threads": threads if threads is not None else os.cpu_count()}
 
 
 # --------------------------------------------------------------------------- reference arm

@@ -229,7 +229,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.8.9"; }
+extern "C" const char* mfsdp_version(void) { return "0.9.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -679,6 +679,8 @@ int launch_momentum_phase(const mfsdp_matrix_shard* shards, int n_shards, const 
       d.l_pad = m.l_pad;
       d.transposed = m.transposed;
       d.vec_ok = (sh.offset % 8 == 0) && (sh.cols % 8 == 0);
+      d.g32 = aligned(d.g, 32);
+      d.m32 = aligned(d.m, 32);
       d.tiles_j = m.l_pad / kTile;
       d.partial0 = m.partial0;
       mb.tile_start[k] = tiles;

@@ -52,7 +52,8 @@ struct MomMat {
   int64_t rows, cols;  // stored shape
   int32_t s_pad, l_pad;
   int32_t transposed;
-  int32_t vec_ok;      // offset and cols multiples of 8: 16-byte vector access
+  int32_t vec_ok;      // offset and cols multiples of 8: every run of 8 elements of a row is a vector
+  int32_t g32, m32;    // the matrix's first gradient / momentum element is 32-byte aligned (256-bit access)
   int32_t tiles_j;     // l_pad / kTile
   int32_t partial0;    // first tile index of this matrix (its partial slots start at 8x this)
 };

@@ -10,17 +10,22 @@
 // X0 = U / (||U||_F + eps) that Newton-Schulz needs.
 //
 // Each CTA takes one 64 x 64 tile of the Newton-Schulz iterate X0 (s x l, the
-// stored matrix transposed when rows > cols).  Every thread issues all its
-// loads of the matching stored G and M (16-byte vectors when the segment
-// allows) before using any, writes M back, and writes X0 = bf16(U) into the
-// workspace's blocked, pre-swizzled layout: straight from registers when X0
-// has the stored orientation (each warp fills one 1 KB atom).  When X0 is the
+// stored matrix transposed when rows > cols).  A thread holds two runs of 8
+// consecutive elements of one stored row, and the 32 lanes of a warp hold 4
+// whole stored rows of the tile: every access of a warp -- 16-byte gradient
+// loads, 32-byte momentum loads and stores -- covers whole 32-byte sectors
+// (4 x 128 bytes of bf16 G, 4 x 256 bytes of M).  Handing each lane 16
+// elements of a row instead, with its 16-byte accesses 32 or 64 bytes apart,
+// left every sector half used by each access; the L2 then served twice the
+// requests, and the phase reached ~78 % of HBM inside the step (after
+// Newton-Schulz, at the power-capped clock) against ~95 % now.  Every thread
+// issues all its loads before using any, writes M back, and writes
+// X0 = bf16(U) into the workspace's blocked, pre-swizzled layout: a run is
+// one 16-byte chunk of an atom row when X0 has the stored orientation; for the
 // transpose, the tile's X0 block (64 X0 rows = one column block, 8 atoms) is
 // assembled in shared memory -- 2-byte stores in an XOR-swizzled image that
-// keeps them free of bank conflicts -- and, after one block barrier, each warp
-// copies one whole atom out with 16-byte accesses, so every X0 line is written
-// in full by one warp (writing 16-byte pieces of 64 different lines per warp
-// held tall matrices to ~72 % of HBM against ~88 % for wide ones).
+// keeps them free of bank conflicts -- and, after one block barrier, each
+// warp copies one whole atom out with 16-byte accesses.
 // The padding up to multiples of 128 is written as zeros.  Each warp's sum of
 // U^2 (fp32, fixed shuffle order) goes to its own slot; the finalise kernel
 // adds a matrix's slots in a fixed order, so the norm is bitwise
@@ -44,153 +49,227 @@ __device__ __forceinline__ int find_mat(const int32_t* start, int n, int t) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Tiles per CTA of the momentum kernel.  Two (every load of both issued
+// first, 96 registers, two CTAs per SM) measured 4-17 % slower than one (60
+// registers, four CTAs per SM).
+constexpr int kMomTilesPerCta = 1;
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// 16 consecutive elements of one stored row: gradient as fp32, momentum.
-struct Row16 {
-  float g[16];
-  float m[16];
+// Global accesses of the momentum kernel, as volatile asm so that they stay in
+// program order (every load of a CTA's tiles is issued before the first
+// store).  16-byte and 32-byte (sm_100 and later) vectors, streaming.
+__device__ __forceinline__ uint4 ld_cs_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void ld_cs_v8(const void* p, uint32_t (&v)[8]) {
+  asm volatile("ld.global.cs.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st_cs_v4(void* p, const float* v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
+               : "memory");
+}
+__device__ __forceinline__ void st_cs_v8(void* p, const float* v) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+               "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
+// One thread's share of one tile: 8 consecutive stored elements of one
+// stored row (a "run").  Thread t of the CTA holds runs t and t + 256 of the
+// tile's 512: run k is stored row r0 + k / 8, stored columns c0 + 8 (k % 8)
+// .. + 7.  So the 32 lanes of a warp cover 4 whole stored rows of the tile per
+// access: 4 x 128 bytes of a bf16 gradient, 4 x 256 bytes of momentum -- every
+// 32-byte sector an access touches is used in full.
+constexpr int kRunsPerThread = 2;
+
+struct Run {
+  int64_t e;       // stored element index of the run's first element (within the matrix)
+  int kind;        // 0: outside the matrix (zeros), 1: vectors, 2: scalar (ragged edge or offset)
+  uint32_t g[8];   // bf16 gradient: g[0..3] (8 values); fp32 gradient: g[0..7]
+  uint32_t m[8];   // fp32 momentum
 };
 
-__device__ __forceinline__ void load_row16_vec(const MomMat& d, int grad_bf16, int64_t e0, Row16& r) {
-  // All six (bf16) or eight (fp32) 16-byte loads are issued before any use.
-  const float4* mp = reinterpret_cast<const float4*>(d.m + e0);
-  float4 mq[4];
-  if (grad_bf16) {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(d.g) + e0);
-    const uint4 q0 = __ldcs(src), q1 = __ldcs(src + 1);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mq[k] = __ldcs(mp + k);
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      r.g[2 * k] = bf16_bits_to_float(w[k] & 0xFFFFu);
-      r.g[2 * k + 1] = bf16_bits_to_float(w[k] >> 16);
-    }
+template <bool kBf16>
+__device__ __forceinline__ void issue_run(const MomMat& d, Run& r) {
+  if (r.kind != 1) return;
+  if constexpr (kBf16) {
+    const uint4 q = ld_cs_v4(static_cast<const uint16_t*>(d.g) + r.e);
+    r.g[0] = q.x; r.g[1] = q.y; r.g[2] = q.z; r.g[3] = q.w;
   } else {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(d.g) + e0);
-    float4 gq[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) gq[k] = __ldcs(src + k);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mq[k] = __ldcs(mp + k);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      r.g[4 * k] = gq[k].x; r.g[4 * k + 1] = gq[k].y; r.g[4 * k + 2] = gq[k].z; r.g[4 * k + 3] = gq[k].w;
+    const float* gp = static_cast<const float*>(d.g) + r.e;
+    if (d.g32) {
+      ld_cs_v8(gp, r.g);
+    } else {
+      const uint4 a = ld_cs_v4(gp), b = ld_cs_v4(gp + 4);
+      r.g[0] = a.x; r.g[1] = a.y; r.g[2] = a.z; r.g[3] = a.w; r.g[4] = b.x; r.g[5] = b.y; r.g[6] = b.z; r.g[7] = b.w;
     }
   }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    r.m[4 * k] = mq[k].x; r.m[4 * k + 1] = mq[k].y; r.m[4 * k + 2] = mq[k].z; r.m[4 * k + 3] = mq[k].w;
+  const float* mp = d.m + r.e;
+  if (d.m32) {
+    ld_cs_v8(mp, r.m);
+  } else {
+    const uint4 a = ld_cs_v4(mp), b = ld_cs_v4(mp + 4);
+    r.m[0] = a.x; r.m[1] = a.y; r.m[2] = a.z; r.m[3] = a.w; r.m[4] = b.x; r.m[5] = b.y; r.m[6] = b.z; r.m[7] = b.w;
   }
 }
 
-// Position (in 16-byte chunks) of chunk q of X0 row i (both within the tile) in
-// the transpose buffer: the atom swizzle q ^ (i % 8), further XORed with
-// 2 * ((i / 16) % 4) so that the 2-byte stores of one warp instruction -- rows
-// 16a + e for a = 0..3, one chunk, eight row pairs -- fall in 16 distinct banks.
-__device__ __forceinline__ int xpose_slot(int i, int q) { return (q ^ (i & 7) ^ (((i >> 4) & 3) << 1)) & 7; }
+template <bool kBf16>
+__device__ __forceinline__ float run_g(const Run& r, int e) {
+  if constexpr (kBf16) return bf16_bits_to_float((e & 1) ? (r.g[e >> 1] >> 16) : (r.g[e >> 1] & 0xFFFFu));
+  return __uint_as_float(r.g[e]);
+}
 
-// One CTA = one 64 x 64 tile of X0; warp w owns stored rows [r0 + 8w, r0 + 8w + 8),
-// lane l row r0 + 8w + l/4 and stored columns [c0 + 16(l%4), +16).  Every warp
-// writes its own norm partial.
-__global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ MomBatch p) {
-  __shared__ __align__(16) uint8_t xpose[kTile * kTile * 2];   // transposed tiles: the X0 block, 8 atoms
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int mi = find_mat(p.tile_start, p.n, blockIdx.x);
-  const MomMat& d = p.mat[mi];
-  const int local = blockIdx.x - p.tile_start[mi];
-  const int ti = local / d.tiles_j, tj = local - ti * d.tiles_j;
-  const int i0 = ti * kTile, j0 = tj * kTile;       // tile origin in X0 (s x l)
-  const int64_t r0 = d.transposed ? j0 : i0;         // matching stored block
-  const int64_t c0 = d.transposed ? i0 : j0;
-
-  const int lr = warp * 8 + (lane >> 2), lc = (lane & 3) * 16;
-  const int64_t gr = r0 + lr, gc = c0 + lc;
+// Momentum of one run: M <- beta M + G written back, u = the Newton-Schulz
+// input (M, or G + beta M with nesterov).
+template <bool kBf16>
+__device__ __forceinline__ void momentum_run(const MomBatch& p, const MomMat& d, const Run& r, int64_t gc,
+                                             float (&u)[8]) {
   const float beta = p.beta;
-  float u[16];
-  float ss = 0.f;
-  if (gr < d.rows && gc < d.cols) {
-    const int64_t e0 = gr * d.cols + gc;
-    if (d.vec_ok && gc + 16 <= d.cols) {
-      Row16 r;
-      load_row16_vec(d, p.grad_bf16, e0, r);
-      float mn[16];
+  if (r.kind == 1) {
+    float mn[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        mn[e] = fmaf(beta, r.m[e], r.g[e]);
-        u[e] = p.nesterov ? fmaf(beta, mn[e], r.g[e]) : mn[e];
-      }
-      float4* mp = reinterpret_cast<float4*>(d.m + e0);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) __stcs(mp + k, make_float4(mn[4 * k], mn[4 * k + 1], mn[4 * k + 2], mn[4 * k + 3]));
+    for (int e = 0; e < 8; ++e) {
+      const float g = run_g<kBf16>(r, e);
+      mn[e] = fmaf(beta, __uint_as_float(r.m[e]), g);
+      u[e] = p.nesterov ? fmaf(beta, mn[e], g) : mn[e];
+    }
+    float* mp = d.m + r.e;
+    if (d.m32) {
+      st_cs_v8(mp, mn);
     } else {
+      st_cs_v4(mp, mn);
+      st_cs_v4(mp + 4, mn + 4);
+    }
+  } else if (r.kind == 2) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        u[e] = 0.f;
-        if (gc + e < d.cols) {
-          const int64_t idx = e0 + e;
-          const float gv = p.grad_bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(d.g)[idx])
-                                       : static_cast<const float*>(d.g)[idx];
-          const float mnv = fmaf(beta, d.m[idx], gv);
-          d.m[idx] = mnv;
-          u[e] = p.nesterov ? fmaf(beta, mnv, gv) : mnv;
-        }
+    for (int e = 0; e < 8; ++e) {
+      u[e] = 0.f;
+      if (gc + e < d.cols) {
+        const int64_t idx = r.e + e;
+        const float gv = kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(d.g)[idx])
+                               : static_cast<const float*>(d.g)[idx];
+        const float mnv = fmaf(beta, d.m[idx], gv);
+        d.m[idx] = mnv;
+        u[e] = p.nesterov ? fmaf(beta, mnv, gv) : mnv;
       }
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) u[e] = 0.f;
+    for (int e = 0; e < 8; ++e) u[e] = 0.f;
   }
-#pragma unroll
-  for (int e = 0; e < 16; ++e) ss = fmaf(u[e], u[e], ss);
-  uint32_t pk[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(u[2 * k], u[2 * k + 1]);
+}
 
-  if (!d.transposed) {
-    // X0 row = stored row: two 16-byte chunks straight from registers; the warp
-    // writes one whole 1 KB atom (8 rows x 64 columns).
-    const int row = i0 + lr;
+// Position (in 16-byte chunks) of X0 chunk q of row i (tile-relative) in the
+// transpose image: the atom swizzle q ^ (i % 8), further XORed with i / 8.
+// A thread's 2-byte stores of one instruction (one value of its run: rows
+// 8a + e for a = 0..7, columns four apart per 8 lanes) then hit 8 distinct
+// chunk slots of 8 rows, all 32 banks; the copy-out of one atom row group
+// reads 4 whole 128-byte image rows per instruction.
+__device__ __forceinline__ int xpose_slot(int i, int q) { return (q ^ (i & 7) ^ (i >> 3)) & 7; }
+
+// kTilesPerCta consecutive 64 x 64 tiles of X0 per CTA.  Each thread issues
+// every load of its runs in all of them before it uses any, then writes M
+// back and X0 = bf16(U) into the workspace's blocked, pre-swizzled layout:
+// for X0 in the stored orientation a run is one 16-byte chunk of an atom row
+// (the warp writes 512 contiguous bytes of one atom); for the transpose, the
+// tile is assembled in shared memory and each warp copies one whole 1 KB atom
+// out.  One norm partial per warp and tile (fixed shuffle order).
+template <bool kBf16, int kTilesPerCta>
+__global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ MomBatch p, int total_tiles) {
+  __shared__ __align__(16) uint8_t xpose[kTilesPerCta][kTile * kTile * 2];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int first = blockIdx.x * kTilesPerCta;
+  int mi[kTilesPerCta], local[kTilesPerCta];
+  Run run[kTilesPerCta][kRunsPerThread];
+  int m = find_mat(p.tile_start, p.n, first);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = j0 + lc + 8 * h;
-      uint8_t* dst = d.y + blocked_chunk(d.s_pad, row, col);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+  for (int k = 0; k < kTilesPerCta; ++k) {
+    const int tile = first + k;
+    if (tile < total_tiles) {
+      while (m + 1 < p.n && p.tile_start[m + 1] <= tile) ++m;
     }
-  } else {
-    // X0 row i = stored column i, X0 column j = stored row j.  This thread's
-    // 16 values are X0 rows lc .. lc+15 (tile-relative) at X0 column lr:
-    // chunk lr / 8 = warp, element lr % 8 of it.
-    uint16_t* img = reinterpret_cast<uint16_t*>(xpose);
+    mi[k] = m;
+    const MomMat& d = p.mat[m];
+    local[k] = tile - p.tile_start[m];
+    const int ti = local[k] / d.tiles_j, tj = local[k] - ti * d.tiles_j;
+    const int64_t r0 = d.transposed ? tj * kTile : ti * kTile;   // stored block of this X0 tile
+    const int64_t c0 = d.transposed ? ti * kTile : tj * kTile;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int i = lc + e;
-      const uint32_t word = pk[e >> 1];
-      img[i * 64 + xpose_slot(i, warp) * 8 + (lane >> 2)] = (uint16_t)((e & 1) ? (word >> 16) : (word & 0xFFFFu));
-    }
-    __syncthreads();
-    // Warp w writes atom w of the block (X0 rows i0 + 8w .. +7): lane l the
-    // 16-byte chunks at positions l and l + 32 of the atom, in the atom's own
-    // swizzled order.
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int pos = lane + 32 * h;                 // chunk position within the 1 KB atom
-      const int r = pos >> 3, phys = pos & 7;        // atom row, stored chunk position
-      const int i = 8 * warp + r;                    // X0 row within the tile
-      const int q = phys ^ r;                        // logical chunk (X0 columns 8q .. 8q+7)
-      const uint4 v = *reinterpret_cast<const uint4*>(xpose + (i * 64 + xpose_slot(i, q) * 8) * 2);
-      *reinterpret_cast<uint4*>(d.y + blocked_chunk(d.s_pad, i0 + i, j0 + 8 * q)) = v;
+    for (int h = 0; h < kRunsPerThread; ++h) {
+      Run& r = run[k][h];
+      const int64_t gr = r0 + (t >> 3) + 32 * h, gc = c0 + 8 * (t & 7);
+      r.e = gr * d.cols + gc;
+      r.kind = (tile < total_tiles && gr < d.rows && gc < d.cols) ? ((d.vec_ok && gc + 8 <= d.cols) ? 1 : 2) : 0;
+      issue_run<kBf16>(d, r);
     }
   }
-
-  // Fixed-order warp reduction; one partial per warp.
+  bool any_xpose = false;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) p.partials[(size_t)(d.partial0 + local) * 8 + warp] = ss;
+  for (int k = 0; k < kTilesPerCta; ++k) {
+    if (first + k >= total_tiles) break;
+    const MomMat& d = p.mat[mi[k]];
+    const int ti = local[k] / d.tiles_j, tj = local[k] - ti * d.tiles_j;
+    const int i0 = ti * kTile, j0 = tj * kTile;
+    float ss = 0.f;
+#pragma unroll
+    for (int h = 0; h < kRunsPerThread; ++h) {
+      const int row = (t >> 3) + 32 * h, col = 8 * (t & 7);       // tile-relative stored row / column
+      float u[8];
+      momentum_run<kBf16>(p, d, run[k][h], (d.transposed ? i0 : j0) + col, u);
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(u[e], u[e], ss);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pk[q] = pack_bf16x2(u[2 * q], u[2 * q + 1]);
+      if (!d.transposed) {
+        *reinterpret_cast<uint4*>(d.y + blocked_chunk(d.s_pad, i0 + row, j0 + col)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      } else {
+        // X0 rows col .. col+7 (tile-relative) at X0 column row.
+        uint16_t* img = reinterpret_cast<uint16_t*>(xpose[k]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = col + e;
+          img[i * 64 + xpose_slot(i, row >> 3) * 8 + (row & 7)] =
+              (uint16_t)((e & 1) ? (pk[e >> 1] >> 16) : (pk[e >> 1] & 0xFFFFu));
+        }
+        any_xpose = true;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) p.partials[(size_t)(d.partial0 + local[k]) * 8 + warp] = ss;
+  }
+  if (__syncthreads_or(any_xpose)) {
+    // Warp w writes atom w of each transposed tile's block (X0 rows i0 + 8w ..
+    // +7): lane l the 16-byte chunks at positions l and l + 32 of the atom, in
+    // the atom's own swizzled order.
+#pragma unroll
+    for (int k = 0; k < kTilesPerCta; ++k) {
+      if (first + k >= total_tiles) break;
+      const MomMat& d = p.mat[mi[k]];
+      if (!d.transposed) continue;
+      const int ti = local[k] / d.tiles_j, tj = local[k] - ti * d.tiles_j;
+      const int i0 = ti * kTile, j0 = tj * kTile;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pos = lane + 32 * h;                 // chunk position within the 1 KB atom
+        const int rr = pos >> 3, phys = pos & 7;       // atom row, stored chunk position
+        const int i = 8 * warp + rr;                   // X0 row within the tile
+        const int q = phys ^ rr;                       // logical chunk (X0 columns 8q .. 8q+7)
+        const uint4 v = *reinterpret_cast<const uint4*>(xpose[k] + (i * 64 + xpose_slot(i, q) * 8) * 2);
+        *reinterpret_cast<uint4*>(d.y + blocked_chunk(d.s_pad, i0 + i, j0 + 8 * q)) = v;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constant__ NormBatch p) {
@@ -239,7 +318,10 @@ __global__ void __launch_bounds__(256) emit_kernel(const __grid_constant__ EmitB
 
 cudaError_t launch_momentum(const MomBatch& b, int total_tiles, cudaStream_t s) {
   if (total_tiles <= 0) return cudaSuccess;
-  momentum_kernel<<<total_tiles, 256, 0, s>>>(b);
+  constexpr int kT = kMomTilesPerCta;
+  const int blocks = (total_tiles + kT - 1) / kT;
+  if (b.grad_bf16) momentum_kernel<true, kT><<<blocks, 256, 0, s>>>(b, total_tiles);
+  else momentum_kernel<false, kT><<<blocks, 256, 0, s>>>(b, total_tiles);
   return cudaGetLastError();
 }
 
