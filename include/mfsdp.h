@@ -43,7 +43,9 @@ typedef enum {
   MFSDP_ERR_UNSUPPORTED_SHAPE = -6,  /* dimension < 1, s > MFSDP_MAX_SHORT_SIDE, or l > MFSDP_MAX_LONG_SIDE */
   MFSDP_ERR_WORKSPACE_TOO_SMALL = -7,
   MFSDP_ERR_CUDA = -8,               /* a CUDA runtime call failed (no device, launch failure, ...) */
-  MFSDP_ERR_DEVICE_TIMEOUT = -9      /* a kernel's bounded wait expired (reported by mfsdp_muon_device_status) */
+  MFSDP_ERR_DEVICE_TIMEOUT = -9,     /* a kernel's bounded wait expired (reported by mfsdp_muon_device_status) */
+  MFSDP_ERR_IO = -10,                /* a checkpoint file could not be opened, written or read */
+  MFSDP_ERR_FORMAT = -11             /* not a checkpoint of this format, or a damaged or truncated one */
 } mfsdp_status;
 
 typedef enum { MFSDP_DTYPE_F32 = 0, MFSDP_DTYPE_BF16 = 1 } mfsdp_dtype;
@@ -434,6 +436,73 @@ int mfsdp_placement_segments(const mfsdp_placement* src, int32_t n_src, const mf
 int mfsdp_segment_copy(const void* const* srcs, const int64_t* src_numel, int32_t n_src, int32_t src_dtype,
                        const mfsdp_segment* segs, int32_t n_segs, int32_t mode,
                        void* dst, int32_t dst_dtype, int64_t dst_numel, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Owner-shard checkpoints (Abstract: "owner-shard checkpoint resharding";
+ * FAQ: MatrixShard metadata carries the owner plan through optimizer routing
+ * and resharding).  One file holds one rank's optimizer state -- its fp32
+ * momentum buffer and its packed AdamW tail (p, m, v) -- together with the
+ * rank's MatrixShard and tail tables, which say where every parameter sits.
+ * Reloading under another world size: read every old rank's file, plan the
+ * new world with mfsdp_plan_owners, and for each new rank let
+ * mfsdp_placement_segments match every parameter's old (rank, offset) to its
+ * new one; mfsdp_segment_copy (GATHER) then moves the state, one buffer kind
+ * at a time, from the old ranks' buffers into the new rank's.
+ *
+ * The file is little-endian and independent of the host (every field is
+ * written byte by byte): the 8 bytes "MFSDPCK1", a u32 format version (1), the
+ * header fields in the order below (i32 world, rank, ns_steps, n_matrix,
+ * n_tail; i64 align_elems, matrix_elems, tail_elems, adam_step), the matrix
+ * shards (48 bytes each: i32 param_id, i32 owner, i64 offset, rows, cols,
+ * i32 transposed, i32 reserved, u64 cost), the tail shards (24 bytes each:
+ * i32 param_id, i32 owner, i64 offset, numel), matrix_elems binary32 values of
+ * momentum, tail_elems values each of tail p, m and v, and a u64 FNV-1a-64
+ * digest of every byte before it.  Host only: the buffers are host memory
+ * (copy device buffers out and in around these calls).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t world;         /* ranks of the plan the file belongs to (>= 1) */
+  int32_t rank;          /* this file's rank, 0 <= rank < world */
+  int32_t ns_steps;      /* Newton-Schulz steps the plan's costs were computed with */
+  int32_t n_matrix;      /* matrix shards of the rank */
+  int32_t n_tail;        /* tail shards of the rank */
+  int32_t reserved;
+  int64_t align_elems;   /* segment alignment of the plan */
+  int64_t matrix_elems;  /* momentum buffer length (the rank's matrix-buffer extent) */
+  int64_t tail_elems;    /* tail buffer length (the rank's tail-buffer extent) */
+  int64_t adam_step;     /* AdamW steps the tail state has taken */
+} mfsdp_checkpoint_header;
+
+/* Size in bytes of the file mfsdp_checkpoint_write makes for this header (0
+ * for an invalid header). */
+size_t mfsdp_checkpoint_bytes(const mfsdp_checkpoint_header* header);
+
+/* Writes one rank's checkpoint to `path` (created or truncated).
+ * matrix_shards[n_matrix] / tail_shards[n_tail]: the rank's tables (every
+ * shard's owner must be header->rank and lie inside its buffer); momentum
+ * [matrix_elems], tail_p / tail_m / tail_v [tail_elems]: host buffers.
+ * Errors: INVALID_ARG (null pointer, invalid header), OUT_OF_BOUNDS (a shard
+ * outside its buffer or owned by another rank), IO. */
+int mfsdp_checkpoint_write(const char* path, const mfsdp_checkpoint_header* header,
+                           const mfsdp_matrix_shard* matrix_shards, const mfsdp_tail_shard* tail_shards,
+                           const float* momentum, const float* tail_p, const float* tail_m,
+                           const float* tail_v);
+
+/* Reads only the header of a checkpoint file (to size the buffers of
+ * mfsdp_checkpoint_read).  Errors: INVALID_ARG, IO, FORMAT. */
+int mfsdp_checkpoint_read_header(const char* path, mfsdp_checkpoint_header* header);
+
+/* Reads a whole checkpoint into caller-provided host buffers of the given
+ * capacities (shards, momentum elements, tail elements); the digest and the
+ * tables are checked before anything is reported.  *header is written only on
+ * success.  Errors: INVALID_ARG, IO, FORMAT (wrong magic or version, a
+ * damaged, truncated or over-long file, tables outside the buffers),
+ * WORKSPACE_TOO_SMALL (a capacity below the file's counts). */
+int mfsdp_checkpoint_read(const char* path, mfsdp_checkpoint_header* header,
+                          mfsdp_matrix_shard* matrix_shards, int32_t matrix_capacity,
+                          mfsdp_tail_shard* tail_shards, int32_t tail_capacity,
+                          float* momentum, int64_t momentum_capacity,
+                          float* tail_p, float* tail_m, float* tail_v, int64_t tail_capacity_elems);
 
 /* Static description of a status code (never NULL). */
 const char* mfsdp_status_string(int status);

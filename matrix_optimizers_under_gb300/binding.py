@@ -27,6 +27,8 @@ ERR_UNSUPPORTED_SHAPE = -6
 ERR_WORKSPACE_TOO_SMALL = -7
 ERR_CUDA = -8
 ERR_DEVICE_TIMEOUT = -9
+ERR_IO = -10
+ERR_FORMAT = -11
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
@@ -41,7 +43,8 @@ EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner
             "mfsdp_status_string", "mfsdp_version", "mfsdp_muon_owner_step_static_scratch",
             "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
             "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall",
-            "mfsdp_host_step_groups", "mfsdp_muon_static_scratch_status")
+            "mfsdp_host_step_groups", "mfsdp_muon_static_scratch_status", "mfsdp_checkpoint_bytes",
+            "mfsdp_checkpoint_write", "mfsdp_checkpoint_read_header", "mfsdp_checkpoint_read")
 
 SEGMENT_REDUCE = 0
 SEGMENT_GATHER = 1
@@ -426,6 +429,84 @@ _lib.mfsdp_placement_segments.restype = ctypes.c_int
 _lib.mfsdp_segment_copy.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(_i64), _i32, _i32,
                                     ctypes.POINTER(Segment), _i32, _i32, _vp, _i32, _i64, _vp]
 _lib.mfsdp_segment_copy.restype = ctypes.c_int
+
+
+class CheckpointHeader(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int32), ("rank", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
+                ("n_matrix", ctypes.c_int32), ("n_tail", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("align_elems", ctypes.c_int64), ("matrix_elems", ctypes.c_int64), ("tail_elems", ctypes.c_int64),
+                ("adam_step", ctypes.c_int64)]
+
+
+_lib.mfsdp_checkpoint_bytes.argtypes = [ctypes.POINTER(CheckpointHeader)]
+_lib.mfsdp_checkpoint_bytes.restype = _sz
+_lib.mfsdp_checkpoint_write.argtypes = [ctypes.c_char_p, ctypes.POINTER(CheckpointHeader), ctypes.POINTER(MatrixShard),
+                                        ctypes.POINTER(TailShard), _vp, _vp, _vp, _vp]
+_lib.mfsdp_checkpoint_write.restype = ctypes.c_int
+_lib.mfsdp_checkpoint_read_header.argtypes = [ctypes.c_char_p, ctypes.POINTER(CheckpointHeader)]
+_lib.mfsdp_checkpoint_read_header.restype = ctypes.c_int
+_lib.mfsdp_checkpoint_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(CheckpointHeader), ctypes.POINTER(MatrixShard),
+                                       _i32, ctypes.POINTER(TailShard), _i32, _vp, _i64, _vp, _vp, _vp, _i64]
+_lib.mfsdp_checkpoint_read.restype = ctypes.c_int
+
+
+@dataclasses.dataclass
+class Checkpoint:
+    """One rank's owner-shard checkpoint: its header, tables and host buffers
+    (NumPy float32 arrays)."""
+    header: CheckpointHeader
+    matrix_shards: List[MatrixShard]
+    tail_shards: List[TailShard]
+    momentum: "object"
+    tail_p: "object"
+    tail_m: "object"
+    tail_v: "object"
+
+
+def _host_f32(x, n: int):
+    """A C-contiguous float32 NumPy copy of a tensor or array of n elements."""
+    import numpy as np
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if a.size != n:
+        raise ValueError(f"buffer has {a.size} elements, the header says {n}")
+    return a
+
+
+def checkpoint_save(path: str, world: int, rank: int, ns_steps: int, align_elems: int,
+                    matrix_shards: Sequence[MatrixShard], tail_shards: Sequence[TailShard], momentum, tail_p, tail_m,
+                    tail_v, adam_step: int) -> None:
+    """Writes one rank's state (momentum and the AdamW tail's p, m, v, as
+    tensors or arrays; copied to host memory here) with its tables (see
+    include/mfsdp.h)."""
+    h = CheckpointHeader()
+    h.world, h.rank, h.ns_steps = int(world), int(rank), int(ns_steps)
+    h.n_matrix, h.n_tail, h.align_elems = len(matrix_shards), len(tail_shards), int(align_elems)
+    h.matrix_elems = int(momentum.numel() if hasattr(momentum, "numel") and callable(momentum.numel)
+                         else len(momentum))
+    h.tail_elems = int(tail_p.numel() if hasattr(tail_p, "numel") and callable(tail_p.numel) else len(tail_p))
+    h.adam_step = int(adam_step)
+    bufs = [_host_f32(momentum, h.matrix_elems)] + [_host_f32(t, h.tail_elems) for t in (tail_p, tail_m, tail_v)]
+    marr = _shard_array(matrix_shards)
+    tarr = (TailShard * max(len(tail_shards), 1))(*tail_shards)
+    _check(_lib.mfsdp_checkpoint_write(os.fsencode(path), ctypes.byref(h), marr, tarr,
+                                       *[b.ctypes.data for b in bufs]), "checkpoint_write")
+
+
+def checkpoint_load(path: str) -> Checkpoint:
+    """Reads one rank's checkpoint into host memory (see include/mfsdp.h)."""
+    import numpy as np
+    h = CheckpointHeader()
+    _check(_lib.mfsdp_checkpoint_read_header(os.fsencode(path), ctypes.byref(h)), "checkpoint_read_header")
+    marr = (MatrixShard * max(h.n_matrix, 1))()
+    tarr = (TailShard * max(h.n_tail, 1))()
+    mom = np.empty(h.matrix_elems, np.float32)
+    tail = [np.empty(h.tail_elems, np.float32) for _ in range(3)]
+    _check(_lib.mfsdp_checkpoint_read(os.fsencode(path), ctypes.byref(h), marr, h.n_matrix, tarr, h.n_tail,
+                                      mom.ctypes.data, h.matrix_elems, *[t.ctypes.data for t in tail], h.tail_elems),
+           "checkpoint_read")
+    return Checkpoint(h, [marr[i] for i in range(h.n_matrix)], [tarr[i] for i in range(h.n_tail)], mom, *tail)
 
 
 def library_path() -> str:

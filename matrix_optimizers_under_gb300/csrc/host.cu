@@ -225,6 +225,8 @@ extern "C" const char* mfsdp_status_string(int status) {
     case MFSDP_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MFSDP_ERR_CUDA: return "CUDA runtime error";
     case MFSDP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MFSDP_ERR_IO: return "checkpoint file input/output error";
+    case MFSDP_ERR_FORMAT: return "not a valid checkpoint file";
     default: return "unknown status";
   }
 }
