@@ -133,29 +133,58 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFSDP_OK : MFSDP_ERR_
 int clear_status(uint8_t* ws, cudaStream_t stream) { return cuda_status(cudaMemsetAsync(ws, 0, kHeaderBytes, stream)); }
 
 // Output tiling of one product of one matrix, in tiles of the 256 rows a CTA
-// pair computes together.  The Gram and polynomial outputs are symmetric: only
-// the 256 x 256 tiles on or above the diagonal are computed, and mirrored by
-// the epilogue.
+// pair computes together and `width` (256, or 128 for narrow tiles) columns.
+// The Gram and polynomial outputs are symmetric: only the tiles on or above
+// the diagonal of 256 x 256 blocks are computed (for narrow tiles: the two
+// 128-column halves of each), and mirrored by the epilogue.
 struct GemmTiling {
   int tiles, tiles_m, tiles_n, n_last, symmetric;
 };
 
-GemmTiling gemm_tiling(int mode, int s_pad, int l_pad) {
+GemmTiling gemm_tiling(int mode, int s_pad, int l_pad, int width = kBlockN) {
   GemmTiling t;
   t.tiles_m = s_pad / kPairM;
   if (mode == kGram || mode == kPoly) {
     const int nb2 = s_pad / kPairM;
     t.symmetric = 1;
-    t.tiles_n = nb2;
-    t.n_last = kBlockN;
-    t.tiles = nb2 * (nb2 + 1) / 2;
+    t.tiles_n = nb2 * (kBlockN / width);
+    t.n_last = width;
+    t.tiles = nb2 * (nb2 + 1) / 2 * (kBlockN / width);
   } else {
     t.symmetric = 0;
-    t.tiles_n = (l_pad + kBlockN - 1) / kBlockN;
-    t.n_last = l_pad - (t.tiles_n - 1) * kBlockN;
+    t.tiles_n = (l_pad + width - 1) / width;
+    t.n_last = l_pad - (t.tiles_n - 1) * width;
     t.tiles = t.tiles_m * t.tiles_n;
   }
   return t;
+}
+
+// Narrow tiles (256 x 128) for a launch whose tiles per Newton-Schulz
+// iteration at the full width are fewer than twice the SMs: such an owner set
+// is bound by its chain of dependent products, and halving a tile halves its
+// epilogue and main loop, which sit on that chain; larger sets keep the
+// full-width tiles, whose per-stage fixed costs are spread over twice the
+// MMAs.  Every output element sums its products in the same order either way,
+// so the update is bit for bit the same.
+bool use_narrow_tiles(const Layout& L, int base, int cnt) {
+  static std::mutex mu;
+  static int sms[kMaxPipeDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxPipeDevices) return false;
+  int n_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms[dev] = 0;
+    n_sm = sms[dev];
+  }
+  if (n_sm <= 0) return false;
+  int64_t per_iter = 0;
+  for (int i = base; i < base + cnt; ++i) {
+    const MatLayout& m = L.mats[i];
+    per_iter += 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad).tiles + gemm_tiling(kUpdate, m.s_pad, m.l_pad).tiles;
+  }
+  return per_iter < 2 * (int64_t)n_sm;
 }
 
 // Tensor-core FLOPs one product of one matrix executes (padded dimensions;
@@ -177,8 +206,9 @@ bool ns_counts_fit(const Layout& L, int32_t ns_steps) {
     int64_t batch = 0;
     for (int i = base; i < std::min(n, base + kMaxBatch); ++i) {
       const MatLayout& m = L.mats[i];
-      const int64_t per_iter = 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad).tiles +
-                               gemm_tiling(kUpdate, m.s_pad, m.l_pad).tiles;
+      // narrow tiles, the larger count
+      const int64_t per_iter = 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad, kBlockN / 2).tiles +
+                               gemm_tiling(kUpdate, m.s_pad, m.l_pad, kBlockN / 2).tiles;
       if (per_iter * ns_steps * 2 * kEpilogueWarps > INT32_MAX) return false;
       batch += per_iter;
     }
@@ -231,7 +261,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.9.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.9.1"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -774,6 +804,8 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       nb.decay = (float)(1.0 - apply->lr * apply->wd);
       nb.w_bf16 = apply->w_dtype == MFSDP_DTYPE_BF16;
     }
+    nb.narrow = use_narrow_tiles(L, base, cnt) ? 1 : 0;
+    const int width = nb.narrow ? kBlockN / 2 : kBlockN;
     for (int k = 0; k < cnt; ++k) {
       const int i = base + k;
       const MatLayout& m = L.mats[i];
@@ -791,7 +823,8 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       d.l_pad = m.l_pad;
       d.s = m.s;
       d.l = m.l;
-      const GemmTiling ts = gemm_tiling(kGram, m.s_pad, m.l_pad), tu = gemm_tiling(kUpdate, m.s_pad, m.l_pad);
+      const GemmTiling ts = gemm_tiling(kGram, m.s_pad, m.l_pad, width);
+      const GemmTiling tu = gemm_tiling(kUpdate, m.s_pad, m.l_pad, width);
       d.tiles_sym = ts.tiles;
       d.tiles_m = tu.tiles_m;
       d.tiles_n = tu.tiles_n;

@@ -30,7 +30,9 @@ constexpr int kStageBytes = kStageBytesA + kStageBytesB;
 constexpr int kEpilogueWarps = 8;  // warps 2-9 of the GEMM CTA: two per TMEM lane quadrant
 constexpr int kSchedulerWarp = 2 + kEpilogueWarps;        // warp 10: hands out ready tiles
 constexpr int kGemmThreads = 32 * (kSchedulerWarp + 1);   // producer, MMA, epilogue warps, scheduler
-constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kStageOutBytes = kBlockM * kAtomK * 2;   // 16 KB: one 128-row x 64-column block of the epilogue
+// the stages, one epilogue staging block per half of the epilogue warps, alignment slack
+constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 2 * (size_t)kStageOutBytes + 1024;
 
 // Bytes between consecutive 64-column blocks of a blocked matrix with rows_pad rows.
 __host__ __device__ inline size_t colblock_stride(int rows_pad) { return (size_t)rows_pad * 128; }
@@ -96,9 +98,9 @@ struct NsMat {
   void* w;               // apply: the weights at the shard offset, else null
   int32_t s_pad, l_pad;
   int32_t s, l;          // true short / long side
-  int32_t tiles_sym;     // Gram / polynomial: 256 x 256 pair tiles on or above the diagonal
-  int32_t tiles_m, tiles_n;   // update: 256-row x 256-column pair tiles
-  int32_t n_last;        // update: width of the last column tile (128 or 256)
+  int32_t tiles_sym;     // Gram / polynomial: pair tiles on or above the diagonal (256 or 128 wide)
+  int32_t tiles_m, tiles_n;   // update: 256-row pair tiles, 256 (or 128, narrow) columns wide
+  int32_t n_last;        // update: width of the last column tile
   int32_t norm_idx;      // index into the norm table
   int32_t transposed;    // final update: stored matrix is l x s
   int32_t vec_ok;        // final update: row-major stores may use 16-byte vectors
@@ -122,6 +124,7 @@ struct NsBatch {
   int32_t stall_tile;    // test hook: this tile's dependency target is never reached (-1: none)
   int32_t iter_tiles;    // tiles of one iteration (three products, all matrices)
   int32_t mode_start[3];
+  int32_t narrow;        // tiles 256 x 128 instead of 256 x 256 (owner sets with few tiles: twice the tiles, half the epilogue each)
   int32_t out_bf16;      // final update dtype
   int32_t w_bf16;        // apply: weight dtype
   float a, b, c;

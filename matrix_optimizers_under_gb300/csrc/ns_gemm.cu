@@ -113,18 +113,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Byte offset of the q-th 16-byte chunk of columns [n, n + 32) of row m in a
-// blocked matrix (n a multiple of 32).
-__device__ __forceinline__ size_t chunk_off(size_t stride, size_t row_off, int m, int n, int q) {
-  return (size_t)(n >> 6) * stride + row_off + (size_t)(((((n & 63) >> 3) + q) ^ (m & 7)) << 4);
+// The epilogue stages each 128-row x 64-column block of a CTA's tile in
+// shared memory, in the layout the block has in the workspace: there it is one
+// contiguous 16 KB run (16 atoms of one column block).  Its input (A or X) is
+// read from global memory, and its output written back, by the 128 threads of
+// a half of the epilogue warps with 16-byte accesses at consecutive addresses
+// (each warp access covers 512 contiguous bytes); a thread of the tile's row
+// reads and writes its own 16-byte chunks in shared memory, where the atom
+// swizzle spreads a warp's 32 rows over all banks.  (Each thread reading and
+// writing its own row straight from global memory touched 32 lines per warp
+// access, half of each sector, and cost ~6 us per tile in a latency-bound
+// owner set.)
+constexpr int kRunChunks = kStageOutBytes / 16 / 128;   // 16-byte chunks per thread of a 16 KB run (8)
+
+// The input run, read from L2 (ld.global.cg: it was written by other CTAs
+// earlier in this launch, so never from a possibly stale L1 line).
+__device__ __forceinline__ void load_run(const uint8_t* run, int k, uint4 (&w)[kRunChunks]) {
+#pragma unroll
+  for (int i = 0; i < kRunChunks; ++i) w[i] = __ldcg(reinterpret_cast<const uint4*>(run) + k + 128 * i);
+}
+__device__ __forceinline__ void put_run(uint8_t* stage, int k, const uint4 (&w)[kRunChunks]) {
+#pragma unroll
+  for (int i = 0; i < kRunChunks; ++i) reinterpret_cast<uint4*>(stage)[k + 128 * i] = w[i];
+}
+__device__ __forceinline__ void store_run(uint8_t* run, const uint8_t* stage, int k) {
+#pragma unroll
+  for (int i = 0; i < kRunChunks; ++i)
+    reinterpret_cast<uint4*>(run)[k + 128 * i] = reinterpret_cast<const uint4*>(stage)[k + 128 * i];
 }
 
-// The epilogue input was written by other CTAs earlier in the same launch:
-// read it from L2 (ld.global.cg), never from a possibly stale L1 line.
-__device__ __forceinline__ void load_chunk(const uint8_t* base, size_t stride, size_t row_off, int m, int n,
-                                           uint4 (&w)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) w[q] = __ldcg(reinterpret_cast<const uint4*>(base + chunk_off(stride, row_off, m, n, q)));
+// Byte offset in a staged block of the q-th 16-byte chunk of columns
+// [c, c + 32) (c = 0 or 32 within the block) of block row r (0..127).
+__device__ __forceinline__ uint32_t stage_off(int r, int c, int q) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c >> 3) + q) ^ (r & 7)) << 4));
 }
 
 // Unpack 32 bf16 (four 16-byte chunks) into fp32.
@@ -138,8 +159,7 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&x)[3
   }
 }
 
-__device__ __forceinline__ void store_chunk(uint8_t* base, size_t stride, size_t row_off, int m, int n,
-                                            const float (&v)[32]) {
+__device__ __forceinline__ void stage_chunk(uint8_t* stage, int r, int c, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 w;
@@ -147,7 +167,7 @@ __device__ __forceinline__ void store_chunk(uint8_t* base, size_t stride, size_t
     w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
     w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
     w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(base + chunk_off(stride, row_off, m, n, q)) = w;
+    *reinterpret_cast<uint4*>(stage + stage_off(r, c, q)) = w;
   }
 }
 
@@ -258,21 +278,24 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
   }
   r.symmetric = prod != kUpdate;
   r.b_mn = prod == kUpdate;
+  const int width = p.narrow ? kBlockN / 2 : kBlockN;    // tile columns
   if (r.symmetric) {
-    const int nb2 = d.s_pad / kPairM;
+    // Row pair-block I holds the tiles of columns 256 I .. s_pad - 1: nb2 - I
+    // of them, or twice that for narrow tiles.
+    const int nb2 = d.s_pad / kPairM, per = kBlockN / width;
     int rem2 = local, I = 0;
-    while (I < nb2 - 1 && rem2 >= nb2 - I) {
-      rem2 -= nb2 - I;
+    while (I < nb2 - 1 && rem2 >= per * (nb2 - I)) {
+      rem2 -= per * (nb2 - I);
       ++I;
     }
     r.m0 = I * kPairM;
-    r.n0 = (I + rem2) * kPairM;
-    r.N = kBlockN;
+    r.n0 = I * kPairM + rem2 * width;
+    r.N = width;
   } else {
     const int mt = local % d.tiles_m, nt = local / d.tiles_m;
     r.m0 = mt * kPairM;
-    r.n0 = nt * kBlockN;
-    r.N = (nt == d.tiles_n - 1) ? d.n_last : kBlockN;
+    r.n0 = nt * width;
+    r.N = (nt == d.tiles_n - 1) ? d.n_last : width;
   }
   r.mc = r.m0 + (int)rank * kBlockM;
   r.zero = p.norm[d.norm_idx].x == 0.0f;
@@ -369,6 +392,17 @@ __device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t par
   }
 }
 
+// The four warps of one epilogue half meet on their mbarrier (every thread
+// arrives, so each thread's shared-memory writes before it are visible to all
+// of them after it).  Bounded like every other wait; false, warp-uniform, when
+// the kernel is giving up.
+__device__ __forceinline__ bool half_sync(uint32_t bar, uint32_t& phase, const Abort& ab, int32_t code) {
+  ptx::mbar_arrive(bar);
+  const bool ok = wait_or_abort(bar, phase & 1, ab, code);
+  ++phase;
+  return __all_sync(0xffffffffu, ok);
+}
+
 // A ring of tile indices: slot k holds the tiles of sequence numbers
 // k, k + size, ...; full[k] (count 1) completes when the writer has stored
 // it, empty[k] when every reader has taken it.  Each CTA's scheduler feeds
@@ -427,6 +461,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   __shared__ __align__(8) uint64_t tfull_bar[2];    // accumulator ready for the epilogue
   __shared__ __align__(8) uint64_t tempty_bar[2];   // accumulator drained, MMA may reuse it
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t half_bar[2];     // the two halves of the epilogue warps meet
   __shared__ __align__(8) uint64_t ring_full[kTileRing];
   __shared__ __align__(8) uint64_t ring_empty[kTileRing];
   __shared__ int32_t ring_slot[kTileRing];
@@ -458,6 +493,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       ptx::mbar_init(ptx::smem_u32(&tempty_bar[a]), 2 * kEpilogueWarps);   // even CTA: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    for (int h = 0; h < 2; ++h) ptx::mbar_init(ptx::smem_u32(&half_bar[h]), 4 * 32);
     for (int k = 0; k < kTileRing; ++k) {
       ptx::mbar_init(ptx::smem_u32(&ring_full[k]), 1);
       ptx::mbar_init(ptx::smem_u32(&ring_empty[k]), kTileReaders);
@@ -605,8 +641,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
     // warp-uniform before the warp acts on it (tcgen05.ld is warp-wide).
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
+    const int k = (warp - 2 - 4 * half) * 32 + lane;   // this thread within its half (0..127)
+    uint8_t* const stage = smem_raw + ((smem_base + (uint32_t)kStages * kStageBytes) - ptx::smem_u32(smem_raw)) +
+                           (size_t)half * kStageOutBytes;
+    const uint32_t hbar = ptx::smem_u32(&half_bar[half]);
+    uint32_t hphase = 0;
     uint32_t acc_it = 0, seq = 0;
-    while (true) {
+    bool live = true;
+    while (live) {
       int32_t t = 0;
       int got_tile = 1;
       if (lane == 0) got_tile = local_take(ring, seq, t, ab);
@@ -615,8 +657,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       if (!__shfl_sync(0xffffffffu, got_tile, 0) || t >= p.tile_end) break;
       const Tile tl = decode_tile(p, t, rank);
       const NsMat& d = p.mat[tl.mi];
-      const int m = tl.mc + quad * 32 + lane;          // this thread's output row
-      const int cw = tl.N >> 1;                         // columns per warp
+      const int rrow = quad * 32 + lane;                 // this thread's row of the CTA's 128
+      const int m = tl.mc + rrow;                        // its output row
+      const int cw = tl.N >> 1;                          // columns of this half (128, or 64)
       const int c0 = half * cw;
       if (tl.zero) {
         if (tl.mode == kUpdateFinal) {
@@ -628,14 +671,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         continue;
       }
       const size_t stride = colblock_stride(d.s_pad);
-      const size_t row_off = (size_t)(m >> 3) * 1024 + (size_t)(m & 7) * 128;
       const bool has_c = (tl.mode != kGram);
-      const int rblk = tl.mc >> 7;                     // this CTA's 128-row block
+      const bool final_out = (tl.mode == kUpdateFinal);
+      const int rblk = tl.mc >> 7;                       // this CTA's 128-row block
+      const int nblk = cw >> 6;                          // 64-column blocks of this half
+      const size_t run_off = (size_t)(tl.mc >> 3) * 1024;   // the CTA's rows in a column block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
-      // the first chunk before waiting for the MMAs, the next one while the
+      // the first block before waiting for the MMAs, the next while the
       // current one is processed.
-      uint4 xin[4];
-      if (has_c) load_chunk(tl.c_in, stride, row_off, m, tl.n0 + c0, xin);
+      uint4 pre[kRunChunks];
+      if (has_c) load_run(tl.c_in + (size_t)((tl.n0 + c0) >> 6) * stride + run_off, k, pre);
       const uint32_t a = acc_it & 1, ause = acc_it >> 1;
       const bool got = wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, ab,
                                      wait_code(tl.phase, kRoleAccFull));
@@ -645,61 +690,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const float scale_gram = tl.first ? nrm.y * nrm.y : 1.0f;
       const float scale_upd = tl.first ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
-      for (int c = c0; c < c0 + cw; c += 32) {
-        const bool more = c + 32 < c0 + cw;
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c, r);
-        uint4 xnext[4];
-        if (has_c && more) load_chunk(tl.c_in, stride, row_off, m, tl.n0 + c + 32, xnext);
-        ptx::tmem_ld_wait();
-        if (!more) {
-          // last chunk read: hand the accumulator back to the MMA warp
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));   // the even CTA's
-        }
-        const int n = tl.n0 + c;
-        const int cblk = n >> 7;
+      const int32_t code = wait_code(tl.phase, kRoleAccFull);
+      for (int blk = 0; blk < nblk && live; ++blk) {
+        const int nb = tl.n0 + c0 + 64 * blk;            // first column of this 64-column block
         // Symmetric products: a block below the diagonal (only inside a
         // diagonal pair tile) is written by its mirror image; a block above
         // it is written directly and transposed.
+        const int cblk = nb >> 7;
         const bool below = tl.symmetric && cblk < rblk;
         const bool mirror = tl.symmetric && cblk > rblk;
-        float v[32];
-        if (tl.mode == kGram) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
-        } else {
-          float x[32];
-          unpack_bf16x32(xin, x);
-          if (tl.mode == kPoly) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
-          }
+        const bool staged_out = !final_out && !below;
+        if (has_c) {
+          put_run(stage, k, pre);
+          if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the input block is staged
+          if (blk + 1 < nblk) load_run(tl.c_in + (size_t)((nb + 64) >> 6) * stride + run_off, k, pre);
         }
-        if (tl.mode == kUpdateFinal) {
-          store_final(d, p, m, n, v);
-        } else if (!below) {
-          uint8_t* out = static_cast<uint8_t*>(tl.out);
-          store_chunk(out, stride, row_off, m, n, v);
-          if (mirror) {
-            // element (n + j, m)
-            const size_t mcol = (size_t)(m & 7) * 2;
+#pragma unroll 1
+        for (int hc = 0; hc < 2; ++hc) {
+          const int cb = 32 * hc;                        // columns [cb, cb + 32) of the block
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
+          ptx::tmem_ld_wait();
+          if (blk == nblk - 1 && hc == 1) {
+            // last accumulator read: hand it back to the MMA warp
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));   // the even CTA's
+          }
+          float v[32];
+          if (tl.mode == kGram) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
-              *reinterpret_cast<__nv_bfloat16*>(out + blocked_chunk(d.s_pad, n + j, m & ~7) + mcol) = h;
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
+          } else {
+            uint4 xin[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
+            float x[32];
+            unpack_bf16x32(xin, x);
+            if (tl.mode == kPoly) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
+            }
+          }
+          const int n = nb + cb;
+          if (final_out) {
+            store_final(d, p, m, n, v);
+          } else if (!below) {
+            stage_chunk(stage, rrow, cb, v);
+            if (mirror) {
+              // element (n + j, m): for each j the warp writes 64 contiguous bytes of row n + j
+              uint8_t* out = static_cast<uint8_t*>(tl.out);
+              const size_t mcol = (size_t)(m & 7) * 2;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+                *reinterpret_cast<__nv_bfloat16*>(out + blocked_chunk(d.s_pad, n + j, m & ~7) + mcol) = h;
+              }
             }
           }
         }
-        if (more) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) xin[q] = xnext[q];
+        if (staged_out) {
+          if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
+          store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
         }
+        // the stage is free again before anyone writes the next block (or tile) into it
+        if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }
       }
+      if (!live) break;
       ++acc_it;
       if (tl.phase + 1 < p.phase_end) {
         // Publish this warp's share of the tile: its stores are ordered
@@ -824,7 +884,7 @@ uint64_t wait_limit_ns(const NsBatch& b, int pairs) {
   double prod[3] = {0.0, 0.0, 0.0};
   for (int i = 0; i < b.n; ++i) {
     const NsMat& d = b.mat[i];
-    const double tile = 2.0 * kPairM * kPairM;   // FLOPs of one 256 x 256 output tile per unit of K
+    const double tile = 2.0 * kPairM * (b.narrow ? kBlockN / 2 : kBlockN);   // FLOPs of one output tile per unit of K
     prod[kGram] += d.tiles_sym * tile * d.l_pad;
     prod[kPoly] += d.tiles_sym * tile * d.s_pad;
     prod[kUpdate] += 2.0 * d.s_pad * (double)d.s_pad * d.l_pad;

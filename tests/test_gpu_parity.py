@@ -461,3 +461,28 @@ def test_empty_owner_set(mfsdp):
     dev = _dev()
     g = torch.zeros(16, dtype=torch.bfloat16, device=dev)
     mfsdp.muon_owner_step([], g, torch.zeros(16, device=dev), g, None)
+
+
+def test_narrow_and_full_width_tiles_agree(mfsdp):
+    """A launch with few tiles per iteration (fewer than twice the SMs) runs
+    256 x 128 tiles, a larger one 256 x 256 tiles; each output element sums the
+    same products in the same order either way.  The 768 x 2304 matrix run
+    alone (narrow tiles) and inside a launch with twenty 2048 x 2048 matrices
+    (full width) gives the same update and momentum, bit for bit."""
+    dev = _dev()
+    rng = np.random.default_rng(31)
+    shapes = [(768, 2304)] + [(2048, 2048)] * 20
+    shards, off = [], 0
+    for i, (r, c) in enumerate(shapes):
+        shards.append(mfsdp.make_shard(off, r, c, param_id=i))
+        off += r * c
+    numel = off
+    grad = W.f32_to_bf16_bits((rng.standard_normal(numel) * 1e-3).astype(np.float32))
+    mom0 = np.zeros(numel, np.float32)
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.bfloat16)
+    s = shards[0]
+    n = s.rows * s.cols
+    u1, m1, _ = run_step(mfsdp, [s], grad[:n].copy(), np.zeros(n, np.float32), update_dtype=torch.bfloat16)
+    assert np.array_equal(u1.view(np.uint32), upd[:n].view(np.uint32))
+    assert np.array_equal(m1, mom[:n])
+    check_matrix(s, upd, mom, grad, mom0, ns_steps=5)
