@@ -736,25 +736,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
             }
           }
           const int n = nb + cb;
-          if (final_out) {
-            store_final(d, p, m, n, v);
-          } else if (!below) {
-            stage_chunk(stage, rrow, cb, v);
-            if (mirror) {
-              // element (n + j, m): for each j the warp writes 64 contiguous bytes of row n + j
-              uint8_t* out = static_cast<uint8_t*>(tl.out);
-              const size_t mcol = (size_t)(m & 7) * 2;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
-                *reinterpret_cast<__nv_bfloat16*>(out + blocked_chunk(d.s_pad, n + j, m & ~7) + mcol) = h;
-              }
-            }
-          }
+          if (final_out) store_final(d, p, m, n, v);
+          else if (!below) stage_chunk(stage, rrow, cb, v);
         }
         if (staged_out) {
           if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
           store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
+          if (mirror) {
+            // Element (nb + j, m) of the transposed block, from this thread's
+            // own staged row (8 values per 16-byte chunk); for each j the warp
+            // writes 64 contiguous bytes of row nb + j.  Rows nb + j lie in
+            // column block m / 64 of the output, in atom row (nb + j) / 8,
+            // swizzled chunk ((m % 64) / 8) ^ (j % 8).
+            uint8_t* out = static_cast<uint8_t*>(tl.out) + (size_t)(m >> 6) * stride + (size_t)(nb >> 3) * 1024 +
+                           (size_t)(m & 7) * 2;
+            const int c8 = (m & 63) >> 3;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, 0, q));
+              const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int j = 8 * q + e;               // column nb + j of the direct block
+                const uint16_t bits = (uint16_t)((e & 1) ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
+                *reinterpret_cast<uint16_t*>(out + (size_t)(j >> 3) * 1024 + (size_t)(j & 7) * 128 +
+                                             (size_t)((c8 ^ (j & 7)) << 4)) = bits;
+              }
+            }
+          }
         }
         // the stage is free again before anyone writes the next block (or tile) into it
         if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }
