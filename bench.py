@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from an ncu capture of dram__bytes_read.sum + dram__bytes_write.sum, keyed
 # by a digest of the kernel's sources (ns_source_digest): a kernel changed
 # since its capture reports null traffic until it is captured again.
-NS_GEMM_TRAFFIC = {("eb58a2eccb969a98", "llama3_8b_rank"): 50.02e9, ("eb58a2eccb969a98", "llama_1p3b_rank"): 8.36e9}
+NS_GEMM_TRAFFIC = {("9643d0d35937fed1", "llama3_8b_rank"): 50.02e9, ("9643d0d35937fed1", "llama_1p3b_rank"): 8.36e9}
 
 # The sources that make up the Newton-Schulz kernel.
 NS_SOURCES = ("ns_gemm.cu", "ptx.cuh", "mfsdp_internal.h")
@@ -67,14 +67,28 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def ns_source_digest() -> str:
-    """First 16 hex digits of the SHA-256 of the Newton-Schulz kernel's sources."""
+def strip_code(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed, so that
+    editing a comment does not change what the digest says about the code."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def ns_source_digest(sources=None) -> str:
+    """First 16 hex digits of the SHA-256 of the Newton-Schulz kernel's sources
+    (comments and layout ignored).  `sources`: {name: text}, default the files."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "matrix_optimizers_under_gb300", "csrc")
     for name in NS_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        if sources is not None:
+            text = sources[name]
+        else:
+            with open(os.path.join(csrc, name)) as f:
+                text = f.read()
+        h.update(strip_code(text).encode())
     return h.hexdigest()[:16]
 
 

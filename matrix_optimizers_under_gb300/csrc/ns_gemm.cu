@@ -10,10 +10,13 @@
 //     X <- a X + B X         (kUpdate, K = s)
 // with the Frobenius prescale 1/(||U||+eps) folded into the first iteration's
 // epilogues (A scaled by its square, the new X by it).  A and B are symmetric:
-// their products compute only the 256 x 256 tiles on or above the diagonal
-// and the epilogue writes every off-diagonal 128 x 128 block twice, directly
-// and transposed, so the stored A and B are exactly symmetric and the Gram and
-// polynomial products execute ~53 % of the dense FLOPs.
+// their products compute only the tiles on or above the diagonal of 256 x 256
+// blocks and the epilogue writes every off-diagonal 128 x 128 block twice,
+// directly and transposed, so the stored A and B are exactly symmetric and the
+// Gram and polynomial products execute ~53 % of the dense FLOPs.  A pair's
+// tile is 256 x 256, or 256 x 128 ("narrow") in a launch with few tiles per
+// iteration, where the chain of dependent products sets the time; each output
+// element sums the same products in the same order at either width.
 //
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
@@ -55,13 +58,17 @@
 // (cta_group::2 copies), which the even producer arms with both CTAs' bytes.
 // The even CTA's warp 1 (one lane) issues 256 x N x 16 pair UMMAs into one of
 // two 256-column accumulators and frees each stage in both CTAs with one
-// multicast commit.  Warps 2-9 of both CTAs drain the other accumulator
-// (tcgen05.ld; two warps per TMEM lane quadrant, each taking half the columns,
-// the epilogue input prefetched ahead of the data), apply the fused polynomial
-// epilogue in fp32 and store bf16 -- or, on the last iteration, the update in
-// the caller's dtype and layout, transposed back for tall matrices -- and hand
-// the accumulator back to the even CTA's issuer.  So one tile's epilogue runs
-// under the next tile's main loop.  Every wait is
+// multicast commit.  Warps 2-9 of both CTAs drain the other accumulator: two
+// halves of four warps (one per TMEM lane quadrant), each half owning half the
+// tile's columns.  A half moves each 128-row x 64-column block of its input
+// (A or X) and output through a 16 KB stage in shared memory with 16-byte
+// accesses at consecutive addresses (the block is one contiguous 16 KB run in
+// the workspace), while each thread reads its accumulator row (tcgen05.ld),
+// its input row from the stage, applies the fused epilogue in fp32 and writes
+// bf16 back into the stage -- or, on the last iteration, the update in the
+// caller's dtype and layout, transposed back for tall matrices -- and the
+// accumulator goes back to the even CTA's issuer after its last read.  So one
+// tile's epilogue runs under the next tile's main loop.  Every wait is
 // bounded: on expiry the CTA records which wait gave up in the status word,
 // every other CTA sees the word and stops too, and each drains what it issued,
 // frees TMEM and returns.
@@ -886,9 +893,11 @@ cudaError_t resident_pairs(int dev, int* out) {
 // tile list, so it ends once the machine has worked through at most one whole
 // product of every matrix of the launch.  The limit is 8x the largest such
 // product's executed FLOPs at a conservative rate -- every CTA pair at a
-// quarter of its tensor peak (16384 bf16 FLOP per clock) at 1 GHz -- and never
-// below 2 s (nor above an hour).  Only launches whose largest product runs for
-// more than ~0.1 s (short sides in the tens of thousands) get more than 2 s.
+// quarter of its tensor peak of 16384 bf16 FLOP per clock, at 1 GHz -- and
+// never below 2 s (nor above an hour).  Only a launch whose largest product
+// would take more than 0.25 s at that rate (~35 ms at full speed; short sides
+// in the tens of thousands) gets more than 2 s: the 8B owner set's largest
+// product, 6.9 TFLOP, takes 22 ms at that rate.
 uint64_t wait_limit_ns(const NsBatch& b, int pairs) {
   double prod[3] = {0.0, 0.0, 0.0};
   for (int i = 0; i < b.n; ++i) {

@@ -34,3 +34,20 @@ def test_segment_case_layout(mfsdp):
 def test_kernel_case_flag_choices():
     with pytest.raises(SystemExit):
         bench.main(["--kernel", "momentum"])
+
+
+def test_kernel_digest_ignores_comments():
+    """The traffic figure is keyed by the Newton-Schulz kernel's code, not its
+    comments or layout: a comment edit keeps the digest, a code edit changes it."""
+    import os
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "matrix_optimizers_under_gb300",
+                        "csrc")
+    srcs = {n: open(os.path.join(csrc, n)).read() for n in bench.NS_SOURCES}
+    base = bench.ns_source_digest(srcs)
+    assert base == bench.ns_source_digest()
+    commented = dict(srcs)
+    commented["ns_gemm.cu"] = "// a new comment\n/* and a block\n comment */\n" + srcs["ns_gemm.cu"].replace("\n", "\n  ")
+    assert bench.ns_source_digest(commented) == base
+    changed = dict(srcs)
+    changed["ptx.cuh"] = srcs["ptx.cuh"].replace("kSuspendHintNs = 32", "kSuspendHintNs = 64")
+    assert changed["ptx.cuh"] != srcs["ptx.cuh"] and bench.ns_source_digest(changed) != base
