@@ -1,6 +1,7 @@
 /* The C ABI used from plain C99: only include/mfsdp.h and the shared library.
- * Host-only calls (planner, sizes, strings, argument checks), so it runs
- * without a GPU.  Prints "ok" and returns 0, or names the first failed check. */
+ * Host-only calls (planner, sizes, strings, argument checks, an owner-shard
+ * checkpoint written to argv[1] and read back), so it runs without a GPU.
+ * Prints "ok" and returns 0, or names the first failed check. */
 #include <stdio.h>
 #include <string.h>
 
@@ -14,7 +15,7 @@
     }                                                        \
   } while (0)
 
-int main(void) {
+int main(int argc, char** argv) {
   /* a 4096-wide block: two square matrices, a tall and a wide one, two vectors */
   const mfsdp_param params[6] = {
       {4096, 1, MFSDP_KIND_TAIL, 0},    {4096, 4096, MFSDP_KIND_MATRIX, 0}, {14336, 4096, MFSDP_KIND_MATRIX, 0},
@@ -54,6 +55,42 @@ int main(void) {
         MFSDP_ERR_INVALID_ARG);
   CHECK(mfsdp_adamw_tail_step(NULL, NULL, NULL, NULL, 16, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1, NULL) ==
         MFSDP_ERR_INVALID_ARG);
+
+  /* an owner-shard checkpoint of a small plan's rank 1: its shards, momentum and tail */
+  if (argc > 1) {
+    const mfsdp_param small[4] = {{64, 96, MFSDP_KIND_MATRIX, 0}, {40, 1, MFSDP_KIND_TAIL, 0},
+                                  {40, 40, MFSDP_KIND_MATRIX, 0}, {96, 64, MFSDP_KIND_MATRIX, 0}};
+    mfsdp_matrix_shard sm[3], back[3];
+    mfsdp_tail_shard st[1], tback[1];
+    int32_t nm = 0, nt = 0;
+    int64_t me[2], te[2];
+    CHECK(mfsdp_plan_owners(small, 4, 2, 5, 128, sm, &nm, st, &nt, me, te) == MFSDP_OK);
+    int f = 0, c = 0, ft = 0, ct = 0;
+    while (f < nm && sm[f].owner != 1) ++f;
+    while (f + c < nm && sm[f + c].owner == 1) ++c;
+    while (ft < nt && st[ft].owner != 1) ++ft;
+    while (ft + ct < nt && st[ft + ct].owner == 1) ++ct;
+    static float mom[8192], mom2[8192], tp[256], tm[256], tv[256], tp2[256], tm2[256], tv2[256];
+    CHECK(me[1] <= 8192 && te[1] <= 256 && c >= 1);
+    for (int i = 0; i < 8192; ++i) mom[i] = (float)i * 0.5f - 7.0f;
+    for (int i = 0; i < 256; ++i) { tp[i] = (float)i; tm[i] = -(float)i; tv[i] = 0.25f * (float)i; }
+    mfsdp_checkpoint_header h;
+    memset(&h, 0, sizeof h);
+    h.world = 2; h.rank = 1; h.ns_steps = 5; h.n_matrix = c; h.n_tail = ct;
+    h.align_elems = 128; h.matrix_elems = me[1]; h.tail_elems = te[1]; h.adam_step = 3;
+    CHECK(mfsdp_checkpoint_write(argv[1], &h, sm + f, st + ft, mom, tp, tm, tv) == MFSDP_OK);
+    mfsdp_checkpoint_header r;
+    CHECK(mfsdp_checkpoint_read_header(argv[1], &r) == MFSDP_OK);
+    CHECK(r.world == 2 && r.rank == 1 && r.n_matrix == c && r.matrix_elems == me[1] && r.adam_step == 3);
+    CHECK(mfsdp_checkpoint_bytes(&r) == 64 + 48 * (size_t)c + 24 * (size_t)ct + 4 * (size_t)(me[1] + 3 * te[1]) + 8);
+    CHECK(mfsdp_checkpoint_read(argv[1], &r, back, 3, tback, 1, mom2, 8192, tp2, tm2, tv2, 256) == MFSDP_OK);
+    CHECK(memcmp(back, sm + f, (size_t)c * sizeof(mfsdp_matrix_shard)) == 0);
+    CHECK(ct == 0 || memcmp(tback, st + ft, (size_t)ct * sizeof(mfsdp_tail_shard)) == 0);
+    CHECK(memcmp(mom, mom2, (size_t)me[1] * sizeof(float)) == 0);
+    CHECK(memcmp(tv, tv2, (size_t)te[1] * sizeof(float)) == 0);
+    CHECK(mfsdp_checkpoint_read(argv[1], &r, back, c - 1, tback, 1, mom2, 8192, tp2, tm2, tv2, 256) ==
+          MFSDP_ERR_WORKSPACE_TOO_SMALL);
+  }
 
   const char* s = mfsdp_status_string(MFSDP_ERR_WORKSPACE_TOO_SMALL);
   CHECK(s != NULL && strlen(s) > 0);

@@ -1,7 +1,7 @@
 """The C ABI from plain C: tests/c/abi_from_c.c compiled as C99 against
 include/mfsdp.h alone and linked to the shared library (no torch, no C++), run
 on the host.  It exercises the planner, the size queries, the group query, the
-host-side argument checks and the status strings."""
+host-side argument checks, an owner-shard checkpoint and the status strings."""
 import os
 import shutil
 import subprocess
@@ -21,9 +21,12 @@ def test_abi_from_plain_c(mfsdp, tmp_path):
                             os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-o", exe, "-L", lib_dir, "-lmfsdp",
                             "-Wl,-rpath," + lib_dir], capture_output=True, text=True)
     assert build.returncode == 0, build.stderr
-    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    run = subprocess.run([exe, str(tmp_path / "rank0.ck")], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, run.stdout + run.stderr
     assert run.stdout.startswith("ok " + mfsdp.version())
+    ck = mfsdp.checkpoint_load(str(tmp_path / "rank0.ck"))      # the C program's file, read back here
+    assert (ck.header.world, ck.header.rank, ck.header.adam_step) == (2, 1, 3)
+    assert ck.momentum[10] == 10 * 0.5 - 7.0
 
 
 @pytest.mark.gpu
