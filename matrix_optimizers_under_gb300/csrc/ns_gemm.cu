@@ -778,11 +778,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       if (!live) break;
       ++acc_it;
       if (tl.phase + 1 < p.phase_end) {
-        // Publish this warp's share of the tile: its stores are ordered
-        // before the counter (release), and before the tensor copies that
-        // later tiles issue after reading it (proxy fence).
+        // Publish this warp's share of the tile: every lane's stores are
+        // ordered before the tensor copies that later tiles issue after
+        // reading the counter (proxy fence), and before lane 0's release add
+        // (the warp barrier orders the lanes' stores before it; the release is
+        // cumulative over them).
         ptx::fence_proxy_async_global();
-        __threadfence();
         __syncwarp();
         if (lane == 0) ptx::red_release_gpu_add(p.done + tl.mi, 1);
       }
