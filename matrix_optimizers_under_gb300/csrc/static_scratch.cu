@@ -43,7 +43,7 @@ struct ScratchCache {
 std::mutex g_scratch_mutex;
 ScratchCache g_scratch[kMaxDevices];
 
-// The driver's context queries, looked up once through the runtime (the
+// The CUDA driver API's context queries, looked up once through the runtime (the
 // library links no driver library).  Null when the driver lacks them; the
 // address is then looked up on every call.
 struct CtxQueries {
