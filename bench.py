@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from an ncu capture of dram__bytes_read.sum + dram__bytes_write.sum, keyed
 # by a digest of the kernel's sources (ns_source_digest): a kernel changed
 # since its capture reports null traffic until it is captured again.
-NS_GEMM_TRAFFIC = {("9643d0d35937fed1", "llama3_8b_rank"): 50.02e9, ("9643d0d35937fed1", "llama_1p3b_rank"): 8.36e9}
+NS_GEMM_TRAFFIC = {("5b7461985d5237d0", "llama3_8b_rank"): 50.00e9, ("5b7461985d5237d0", "llama_1p3b_rank"): 8.24e9}
 
 # The sources that make up the Newton-Schulz kernel.
 NS_SOURCES = ("ns_gemm.cu", "ptx.cuh", "mfsdp_internal.h")
