@@ -337,8 +337,9 @@ int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, in
  * *detail (may be NULL) receives the raw word: bits 0-7 the waiting role
  * (1 producer: a free pipeline stage; 2 MMA issuer: a stage's operands;
  * 3 MMA issuer: a drained accumulator; 4 epilogue: a finished accumulator;
- * 5 scheduler: the earlier products of a tile's matrix; 7 scheduler: a free
- * slot of a tile ring; 8 any role: the next tile), bits 8-31 the
+ * 5 producer, or a role waiting behind it: the earlier products of a tile's
+ * matrix; 7 scheduler: a free slot of a tile ring; 8 any role: the next
+ * tile), bits 8-31 the
  * Newton-Schulz product index (3 * iteration + 0 Gram / 1 polynomial /
  * 2 update) where the role knows it, else 0.  The status word is cleared by
  * every call that runs the momentum phase. */
@@ -348,8 +349,8 @@ int mfsdp_muon_device_status(const void* workspace, void* stream, int32_t* detai
  * hook then clears itself) gives tile `tile` of its tile list a dependency
  * that is never satisfied, so the wait for it runs out after 2 s.  The kernel
  * then ends in bounded time, and mfsdp_muon_device_status reports
- * MFSDP_ERR_DEVICE_TIMEOUT with role 5 (the scheduler's dependency wait) or 8
- * (a role of the same CTA pair waiting to be handed that tile).
+ * MFSDP_ERR_DEVICE_TIMEOUT with role 5 (a producer's dependency wait, or a
+ * role waiting behind it) or 8 (a role waiting to be handed a tile).
  * The context stays usable.  This exercises the bounded-wait path without
  * faulting or hanging the GPU.  Returns INVALID_ARG for tile < 0. */
 int mfsdp_test_inject_stall(int32_t tile);
@@ -359,7 +360,9 @@ int mfsdp_test_inject_stall(int32_t tile);
  * s_pad x l_pad, A/B s_pad x s_pad, bf16, stored as 1024-byte atoms of
  * 8 rows x 64 columns; atom (row/8, col/64) sits at
  * ((col/64) * (rows_pad/8) + row/8) * 1024, and inside it element (r, c) at
- * (r%8)*128 + ((((c%64)/8) ^ (r%8)) * 16) + (c%8)*2.  Returns the status. */
+ * (r%8)*128 + ((((c%64)/8) ^ (r%8)) * 16) + (c%8)*2.  A and B (symmetric)
+ * hold only their 256 x 256 blocks on or above the diagonal (col/256 >=
+ * row/256); the others are never written.  Returns the status. */
 int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int64_t* out);
 
 /* AdamW over a packed fp32 tail buffer (Abstract: non-matrix tensors "stay on

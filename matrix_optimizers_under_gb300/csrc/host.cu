@@ -136,7 +136,8 @@ int clear_status(uint8_t* ws, cudaStream_t stream) { return cuda_status(cudaMems
 // pair computes together and `width` (256, or 128 for narrow tiles) columns.
 // The Gram and polynomial outputs are symmetric: only the tiles on or above
 // the diagonal of 256 x 256 blocks are computed (for narrow tiles: the two
-// 128-column halves of each), and mirrored by the epilogue.
+// 128-column halves of each) and stored; the products that read them read the
+// blocks below that diagonal from their stored transposes.
 struct GemmTiling {
   int tiles, tiles_m, tiles_n, n_last, symmetric;
 };
@@ -212,7 +213,9 @@ bool ns_counts_fit(const Layout& L, int32_t ns_steps) {
       if (per_iter * ns_steps * 2 * kEpilogueWarps > INT32_MAX) return false;
       batch += per_iter;
     }
-    if (batch * ns_steps > INT32_MAX - 65536) return false;   // headroom: pairs overshoot the tile counter
+    // headroom: pairs overshoot the tile counter; bit 30 of a handed-out
+    // tile index is a flag
+    if (batch * ns_steps > (int64_t(1) << 30) - 65536) return false;
   }
   return true;
 }
@@ -261,7 +264,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.9.4"; }
+extern "C" const char* mfsdp_version(void) { return "0.9.5"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;

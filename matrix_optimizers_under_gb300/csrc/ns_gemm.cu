@@ -11,9 +11,12 @@
 // with the Frobenius prescale 1/(||U||+eps) folded into the first iteration's
 // epilogues (A scaled by its square, the new X by it).  A and B are symmetric:
 // their products compute only the tiles on or above the diagonal of 256 x 256
-// blocks and the epilogue writes every off-diagonal 128 x 128 block twice,
-// directly and transposed, so the stored A and B are exactly symmetric and the
-// Gram and polynomial products execute ~53 % of the dense FLOPs.  A pair's
+// blocks (~53 % of the dense FLOPs), and the workspace keeps only those blocks.
+// An operand block below that diagonal is read from the stored block across
+// it, as the MN-major image of its transpose (the tensor copies and the MMA
+// read either form; a diagonal 256 x 256 block is computed and stored whole,
+// so it needs none): every product reads exactly the values it would read
+// from the full matrix, and no epilogue writes a transposed copy.  A pair's
 // tile is 256 x 256, or 256 x 128 ("narrow") in a launch with few tiles per
 // iteration, where the chain of dependent products sets the time; each output
 // element sums the same products in the same order at either width.
@@ -21,8 +24,8 @@
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
 // atoms of one 64-column block contiguous.  So a CTA's share of a pipeline
-// stage is one 16 KB run of rows per column block for each operand (for the
-// MN-major X of the update, one 16 KB run of 128 K rows per 64-column block),
+// stage is one 16 KB run of rows per column block for each operand (for an
+// MN-major operand, one 16 KB run of 128 K rows per 64-column block),
 // and a tensor copy through a map that views the whole
 // workspace as 128-byte rows lands it in shared memory byte for byte, ready
 // for tcgen05.mma.  Two maps of that one view (boxes of 128 and 64 rows: 16 KB
@@ -38,11 +41,18 @@
 // operands the pairs share in L2.  A tile may start only once the earlier
 // products of its own matrix are stored: each epilogue warp that stores its
 // share of a tile adds one to the matrix's completion counter (release).  In
-// each pair a scheduler warp of the even CTA takes the next index, waits
-// (acquire) until the counter of its matrix covers every tile of the earlier
-// products, and hands the tile to the odd CTA's scheduler (a remote store and
-// mbarrier arrive); each scheduler passes it to its own CTA's roles through a
-// small ring in shared memory.  It runs a few tiles ahead, so taking a tile
+// each pair a scheduler warp of the even CTA takes the next index and hands
+// the tile to its own CTA's roles and to the odd CTA's scheduler (a remote
+// store and mbarrier arrive), which passes it to the odd CTA's roles; each CTA
+// passes tiles through a small ring in shared memory.  The producer of each
+// CTA waits (acquire) until the counter of the tile's matrix covers every tile
+// of the earlier products before its tensor copies, and tells its CTA's other
+// roles through an mbarrier; the scheduler takes the next index only once
+// that wait is over, so a pair that cannot start a tile takes no more of the
+// list.  Both producers watch the counter themselves because a hand-over
+// across the pair costs a cluster-scope release (~850 cycles on GB300), which
+// would otherwise lie between a product's last store and the next product's
+// first copies.  The scheduler runs ahead of the roles, so taking a tile
 // costs the pipeline nothing while work is ready.  Small matrices run ahead
 // through their iterations while large ones fill the machine, with no launch
 // gap or tail between products.  Every dependency points to an earlier
@@ -103,6 +113,9 @@ constexpr int32_t kArrivalsPerTile = 2 * kEpilogueWarps;   // completion-counter
 constexpr int kTileRing = 4;           // ready tiles handed from a CTA's scheduler to its roles
 constexpr uint32_t kTileReaders = 2 + kEpilogueWarps;   // producer, MMA issuer, epilogue warps
 constexpr int kPairRing = 4;           // tiles handed from the even CTA's scheduler to the odd one's
+// Set in a handed-out tile index when the scheduler found the tile's earlier
+// products not yet stored: the producers then wait for them themselves.
+constexpr int32_t kPollBit = 1 << 30;
 
 __device__ __forceinline__ int find_mat(const int32_t* start, int n, int t) {
   int lo = 0, hi = n - 1;
@@ -239,6 +252,8 @@ struct Tile {
   int mode;      // kGram, kPoly, kUpdate or kUpdateFinal
   bool first;    // first iteration: fold the Frobenius prescale into the epilogue
   bool symmetric;
+  bool a_sym;    // A operand is a symmetric product stored as its upper 256 x 256 blocks (polynomial, update)
+  bool b_sym;    // the K-major B operand likewise (polynomial)
   bool b_mn;     // B operand is the MN-major X (update products)
   bool zero;     // the matrix's momentum is exactly zero: no products
   int m0, n0;    // origin of the pair's 256-row output tile
@@ -284,6 +299,8 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
     r.k_blocks = d.s_pad / kBlockK;
   }
   r.symmetric = prod != kUpdate;
+  r.a_sym = prod != kGram;
+  r.b_sym = prod == kPoly;
   r.b_mn = prod == kUpdate;
   const int width = p.narrow ? kBlockN / 2 : kBlockN;    // tile columns
   if (r.symmetric) {
@@ -326,6 +343,19 @@ __device__ __forceinline__ const uint8_t* b_half_kmajor(const Tile& tl, int kb, 
 // MN-major X: 64-column block n0/64 + j, K rows [64 kb, 64 kb + 64).
 __device__ __forceinline__ const uint8_t* b_block_mn(const Tile& tl, int kb, size_t kstride, int j) {
   return tl.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
+}
+// A and B are stored as their 128 x 128 blocks (r, c) with c/2 >= r/2 only
+// (on or above the diagonal of 256 x 256 blocks).  Stage kb (K columns
+// [128 kb, 128 kb + 128)) of an operand whose 256-row block lies below K's
+// 256-block is read from the stored block across the diagonal, as the
+// MN-major image of the transpose (the matrix is symmetric): both CTAs of the
+// pair decide alike, since their rows share one 256-row block.
+__device__ __forceinline__ bool a_trans(const Tile& tl, int kb) { return tl.a_sym && (kb >> 1) < (tl.m0 >> 8); }
+__device__ __forceinline__ bool b_trans(const Tile& tl, int kb) { return tl.b_sym && (kb >> 1) < (tl.n0 >> 8); }
+// Transposed A: 64-column block mc/64 + j of the stored matrix, rows
+// [128 kb, 128 kb + 128): one 16 KB run.
+__device__ __forceinline__ const uint8_t* a_block_t(const Tile& tl, int kb, size_t kstride, int j) {
+  return tl.a_op + (size_t)((tl.mc >> 6) + j) * kstride + (size_t)kb * 16384;
 }
 
 // Row of the workspace tensor map (128-byte rows) where a blocked run starts.
@@ -431,12 +461,26 @@ __device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32
   return true;
 }
 
-// A role takes the tile of sequence number seq from its CTA's ring.
-__device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab) {
+// A role reads the tile of sequence number seq from its CTA's ring (`poll`:
+// whether kPollBit was set) ...
+__device__ __forceinline__ bool local_peek(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab,
+                                           bool* poll = nullptr) {
   const uint32_t k = seq % kTileRing, use = seq / kTileRing;
   if (!wait_or_abort(r.full0 + 8u * k, use & 1, ab, wait_code(0, kRoleTileFull))) return false;
-  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
-  ptx::mbar_arrive(r.empty0 + 8u * k);
+  int32_t v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(r.slot0 + 4u * k) : "memory");
+  if (poll) *poll = (v & kPollBit) != 0;
+  t = v & ~kPollBit;
+  return true;
+}
+// ... and gives the slot back (every reader of the CTA does, once per tile).
+__device__ __forceinline__ void local_release(const Ring& r, uint32_t seq) {
+  ptx::mbar_arrive(r.empty0 + 8u * (seq % kTileRing));
+}
+__device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab,
+                                           bool* poll = nullptr) {
+  if (!local_peek(r, seq, t, ab, poll)) return false;
+  local_release(r, seq);
   return true;
 }
 
@@ -450,13 +494,17 @@ __device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_
   return true;
 }
 
-// Pair ring, odd CTA's scheduler side.
+// Pair ring, odd CTA's scheduler side: takes the tile of sequence number seq.
 __device__ __forceinline__ bool pair_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab) {
   const uint32_t k = seq % kPairRing, use = seq / kPairRing;
   if (!wait_cluster_or_abort(r.full0 + 8u * k, use & 1, ab, wait_code(0, kRoleTileFull))) return false;
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(t) : "r"(r.slot0 + 4u * k) : "memory");
-  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.empty0 + 8u * k, 0));
   return true;
+}
+// ... and frees its slot for the even CTA's scheduler (called after the tile
+// has been passed on: the cluster-scope release stalls this thread).
+__device__ __forceinline__ void pair_free(const Ring& r, uint32_t seq) {
+  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.empty0 + 8u * (seq % kPairRing), 0));
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_constant__ NsBatch p,
@@ -472,6 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   __shared__ __align__(8) uint64_t ring_full[kTileRing];
   __shared__ __align__(8) uint64_t ring_empty[kTileRing];
   __shared__ int32_t ring_slot[kTileRing];
+  __shared__ __align__(8) uint64_t dep_bar[kTileRing];     // tile seq's earlier products are stored (producer)
   __shared__ __align__(8) uint64_t pair_full[kPairRing];    // used in the odd CTA
   __shared__ __align__(8) uint64_t pair_empty[kPairRing];   // used in the even CTA
   __shared__ int32_t pair_slot[kPairRing];                  // used in the odd CTA
@@ -504,6 +553,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
     for (int k = 0; k < kTileRing; ++k) {
       ptx::mbar_init(ptx::smem_u32(&ring_full[k]), 1);
       ptx::mbar_init(ptx::smem_u32(&ring_empty[k]), kTileReaders);
+      ptx::mbar_init(ptx::smem_u32(&dep_bar[k]), 1);
     }
     for (int k = 0; k < kPairRing; ++k) {
       ptx::mbar_init(ptx::smem_u32(&pair_full[k]), 1);
@@ -533,13 +583,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       bool ok = true;
       while (ok) {
         int32_t t;
-        ok = local_take(ring, seq++, t, ab);
+        bool poll = false;
+        ok = local_take(ring, seq, t, ab, &poll);
         if (!ok || t >= p.tile_end) break;
         const Tile tl = decode_tile(p, t, rank);
+        // A tile whose earlier products were not all stored when the
+        // scheduler took it: both producers of the pair wait (acquire) until
+        // they are, so neither CTA's copies wait for a hand-over after the
+        // last of them lands.  (Otherwise the scheduler's acquire reaches this
+        // thread through the rings.)  dep_bar passes the wait on to this CTA's
+        // epilogue (which reads those products too), MMA issuer and scheduler.
+        const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
+        if (poll && !wait_done(p.done + tl.mi, need, ab, wait_code(tl.phase, kRoleDependency))) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive(ptx::smem_u32(&dep_bar[seq % kTileRing]));   // releases the acquire (CTA scope)
+        ++seq;
         if (tl.zero) continue;
-        // The operands were stored by other CTAs (generic proxy) before the
-        // scheduler handed the tile out; the tensor copies read them through
-        // the async proxy.
+        // The operands were stored by other CTAs (generic proxy); the tensor
+        // copies read them through the async proxy.
         if (tl.need > 0) ptx::fence_proxy_async_global();
         const size_t kstride = colblock_stride(p.mat[tl.mi].s_pad);   // every operand has s_pad rows per column block
         const int nh = tl.N >> 1;                                      // this CTA's columns of B
@@ -556,18 +619,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, pair_bytes);
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
           // two column blocks (K atoms) per stage
+          // A: two 16 KB runs, K-major (column blocks 2 kb, 2 kb + 1) or, across
+          // the diagonal, MN-major (this CTA's rows as two 64-column blocks).
+          const bool at = a_trans(tl, kb), bmn = tl.b_mn || b_trans(tl, kb);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            ptx::tma_load_2d_pair(sa + (uint32_t)h * 16384u, &tmap_16k, 0, ws_row(p, a_block(tl, 2 * kb + h, kstride)), fb, pol);
-            if (!tl.b_mn) {
+            const uint8_t* asrc = at ? a_block_t(tl, kb, kstride, h) : a_block(tl, 2 * kb + h, kstride);
+            ptx::tma_load_2d_pair(sa + (uint32_t)h * 16384u, &tmap_16k, 0, ws_row(p, asrc), fb, pol);
+            if (!bmn) {
               const int32_t yb = ws_row(p, b_half_kmajor(tl, 2 * kb + h, kstride, rank));
               if (nh == 128) ptx::tma_load_2d_pair(sb + (uint32_t)h * 16384u, &tmap_16k, 0, yb, fb, pol);
               else ptx::tma_load_2d_pair(sb + (uint32_t)h * 8192u, &tmap_8k, 0, yb, fb, pol);
             }
           }
-          if (tl.b_mn) {
-            // X as the MN-major operand: per 64-column block, the stage's 128 K
-            // rows are one contiguous 16 KB run.
+          if (bmn) {
+            // X, or a symmetric B across the diagonal, as the MN-major operand:
+            // per 64-column block, the stage's 128 K rows are one contiguous
+            // 16 KB run.
             const int per = nh / 64;
             for (int jj = 0; jj < per; ++jj)
               ptx::tma_load_2d_pair(sb + (uint32_t)jj * 16384u, &tmap_16k, 0,
@@ -592,10 +660,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       bool ok = true;
       while (ok) {
         int32_t t;
-        ok = local_take(ring, seq++, t, ab);
+        if (rank != 0) {
+          ok = local_take(ring, seq++, t, ab);
+          if (!ok || t >= p.tile_end) break;
+          continue;
+        }
+        ok = local_peek(ring, seq, t, ab);
         if (!ok || t >= p.tile_end) break;
-        if (rank != 0) continue;
         const Tile tl = decode_tile(p, t, rank);
+        // Its operands can only land after the producer's dependency wait;
+        // waiting for that first makes a dependency that is never met show up
+        // as one (the slot is given back after it, as in the epilogue).
+        ok = wait_or_abort(ptx::smem_u32(&dep_bar[seq % kTileRing]), (seq / kTileRing) & 1, ab,
+                           wait_code(tl.phase, kRoleDependency));
+        local_release(ring, seq);
+        ++seq;
+        if (!ok) break;
         if (tl.zero) continue;
         const uint32_t a = acc_it & 1, ause = acc_it >> 1;
         // both CTAs' epilogues have drained accumulator a
@@ -604,7 +684,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + a * kAccCols;
-        const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, (uint32_t)tl.N, tl.b_mn ? 1u : 0u);
         for (int kb = 0; kb < tl.k_blocks; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t use = it / kStages;
@@ -614,16 +693,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           ptx::tc_fence_after();
           const uint32_t sa = smem_base + (uint32_t)s * kStageBytes, sb = sa + kStageBytesA;
           const uint32_t bh = (uint32_t)(tl.N >> 1) * 128u;   // bytes of one K atom of this CTA's B half
+          const bool at = a_trans(tl, kb), bmn = tl.b_mn || b_trans(tl, kb);
+          const uint32_t idesc = ptx::idesc_bf16_f32(kPairM, (uint32_t)tl.N, bmn ? 1u : 0u, at ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
             const uint32_t h = (uint32_t)k >> 2, kk = (uint32_t)k & 3;
-            // K-major operand: atom h, then 16 elements (32 bytes) inside the swizzle row.
-            const uint64_t adesc = ptx::smem_desc_sw128(sa + h * 16384u + kk * 32u, 16u, 1024u);
-            // MN-major operand: 16 K rows = two 8-row atoms (2 KB); 64-column
-            // blocks 16 KB apart (leading byte offset), 8-row K groups 1 KB
-            // apart (stride byte offset).
-            const uint64_t bdesc = tl.b_mn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 16384u, 1024u)
-                                           : ptx::smem_desc_sw128(sb + h * bh + kk * 32u, 16u, 1024u);
+            // K-major operand: atom h, then 16 elements (32 bytes) inside the
+            // swizzle row.  MN-major operand: 16 K rows = two 8-row atoms
+            // (2 KB); 64-column blocks 16 KB apart (leading byte offset), 8-row
+            // K groups 1 KB apart (stride byte offset).
+            const uint64_t adesc = at ? ptx::smem_desc_sw128(sa + (uint32_t)k * 2048u, 16384u, 1024u)
+                                      : ptx::smem_desc_sw128(sa + h * 16384u + kk * 32u, 16u, 1024u);
+            const uint64_t bdesc = bmn ? ptx::smem_desc_sw128(sb + (uint32_t)k * 2048u, 16384u, 1024u)
+                                       : ptx::smem_desc_sw128(sb + h * bh + kk * 32u, 16u, 1024u);
             ptx::umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           // frees stage s in both CTAs once these MMAs have read it
@@ -658,11 +740,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
     while (live) {
       int32_t t = 0;
       int got_tile = 1;
-      if (lane == 0) got_tile = local_take(ring, seq, t, ab);
-      ++seq;
+      if (lane == 0) got_tile = local_peek(ring, seq, t, ab);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (!__shfl_sync(0xffffffffu, got_tile, 0) || t >= p.tile_end) break;
       const Tile tl = decode_tile(p, t, rank);
+      // The tile's earlier products are stored (this CTA's producer has seen
+      // them, dep_bar) before its epilogue input is read; the ring slot is
+      // given back only after this wait, so dep_bar's phases cannot run ahead
+      // of it.
+      if (lane == 0) {
+        got_tile = wait_or_abort(ptx::smem_u32(&dep_bar[seq % kTileRing]), (seq / kTileRing) & 1, ab,
+                                 wait_code(tl.phase, kRoleDependency));
+        local_release(ring, seq);
+      }
+      ++seq;
+      if (!__shfl_sync(0xffffffffu, got_tile, 0)) break;
       const NsMat& d = p.mat[tl.mi];
       const int rrow = quad * 32 + lane;                 // this thread's row of the CTA's 128
       const int m = tl.mc + rrow;                        // its output row
@@ -680,7 +772,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const size_t stride = colblock_stride(d.s_pad);
       const bool has_c = (tl.mode != kGram);
       const bool final_out = (tl.mode == kUpdateFinal);
-      const int rblk = tl.mc >> 7;                       // this CTA's 128-row block
       const int nblk = cw >> 6;                          // 64-column blocks of this half
       const size_t run_off = (size_t)(tl.mc >> 3) * 1024;   // the CTA's rows in a column block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
@@ -700,13 +791,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const int32_t code = wait_code(tl.phase, kRoleAccFull);
       for (int blk = 0; blk < nblk && live; ++blk) {
         const int nb = tl.n0 + c0 + 64 * blk;            // first column of this 64-column block
-        // Symmetric products: a block below the diagonal (only inside a
-        // diagonal pair tile) is written by its mirror image; a block above
-        // it is written directly and transposed.
-        const int cblk = nb >> 7;
-        const bool below = tl.symmetric && cblk < rblk;
-        const bool mirror = tl.symmetric && cblk > rblk;
-        const bool staged_out = !final_out && !below;
+        // Symmetric products write their tiles as they are: the blocks below
+        // the diagonal of 256 x 256 blocks are never stored (the products that
+        // read them read the stored blocks across it, transposed).
+        const bool staged_out = !final_out;
         if (has_c) {
           put_run(stage, k, pre);
           if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the input block is staged
@@ -719,10 +807,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
           ptx::tmem_ld_wait();
           if (blk == nblk - 1 && hc == 1) {
-            // last accumulator read: hand it back to the MMA warp
+            // last accumulator read: hand it back to the MMA warp (the even
+            // CTA's barrier; the signal carries no data, see mbar_arrive_signal)
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));   // the even CTA's
+            if (lane == 0) ptx::mbar_arrive_signal(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));
           }
           float v[32];
           if (tl.mode == kGram) {
@@ -744,33 +833,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           }
           const int n = nb + cb;
           if (final_out) store_final(d, p, m, n, v);
-          else if (!below) stage_chunk(stage, rrow, cb, v);
+          else stage_chunk(stage, rrow, cb, v);
         }
         if (staged_out) {
           if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
           store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
-          if (mirror) {
-            // Element (nb + j, m) of the transposed block, from this thread's
-            // own staged row (8 values per 16-byte chunk); for each j the warp
-            // writes 64 contiguous bytes of row nb + j.  Rows nb + j lie in
-            // column block m / 64 of the output, in atom row (nb + j) / 8,
-            // swizzled chunk ((m % 64) / 8) ^ (j % 8).
-            uint8_t* out = static_cast<uint8_t*>(tl.out) + (size_t)(m >> 6) * stride + (size_t)(nb >> 3) * 1024 +
-                           (size_t)(m & 7) * 2;
-            const int c8 = (m & 63) >> 3;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 w = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, 0, q));
-              const uint32_t h[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int j = 8 * q + e;               // column nb + j of the direct block
-                const uint16_t bits = (uint16_t)((e & 1) ? (h[e >> 1] >> 16) : (h[e >> 1] & 0xFFFFu));
-                *reinterpret_cast<uint16_t*>(out + (size_t)(j >> 3) * 1024 + (size_t)(j & 7) * 128 +
-                                             (size_t)((c8 ^ (j & 7)) << 4)) = bits;
-              }
-            }
-          }
         }
         // the stage is free again before anyone writes the next block (or tile) into it
         if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }
@@ -791,30 +858,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   } else {
     if (lane == 0) {
       // ----------------------------------------------------------- scheduler
-      // Even CTA: takes the pair's tiles in list order, waits until the
-      // earlier products of each tile's matrix are stored, and hands the tile
-      // to the odd CTA's scheduler and to this CTA's roles (the end marker
-      // last).  Odd CTA: forwards what it receives to its own roles.  The
-      // roles' reads of the stored products are ordered after this wait
-      // through the rings' release/acquire chain.
+      // Even CTA: takes the pair's tiles in list order and hands each to
+      // this CTA's roles and to the odd CTA's scheduler (the end marker last),
+      // then waits until this CTA's producer has seen the tile's earlier
+      // products stored before it takes the next: a pair that cannot start a
+      // tile takes no more of the list, which other pairs may be able to
+      // start.  Odd CTA: forwards what it receives to its own roles, then
+      // frees the pair slot.  Each hand-over across the pair costs a
+      // cluster-scope release (~850 cycles), which is why the producers wait
+      // for the dependencies themselves and the local hand-overs go first.
       uint32_t seq = 0;
       while (true) {
         int32_t t;
         if (rank == 0) {
           t = p.tile_begin + atomicAdd(p.next_tile, 1);
           if (t > p.tile_end) t = p.tile_end;           // the end marker
+          bool ready = true;
           if (t < p.tile_end) {
             const Tile tl = decode_tile(p, t, 0);
             const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
-            if (!tl.zero && need > 0 &&
-                !wait_done(p.done + tl.mi, need, ab, wait_code(tl.phase, kRoleDependency)))
-              break;
+            ready = tl.zero || need <= 0 || ptx::ld_acquire_gpu(p.done + tl.mi) >= need;
           }
-          if (!pair_publish(pair, seq, t, ab)) break;
+          const int32_t v = ready ? t : (t | kPollBit);
+          if (!local_publish(ring, seq, v, ab) || !pair_publish(pair, seq, v, ab)) break;
+          // A pair takes its next tile only once this one may start.  In a
+          // launch with many tiles the scheduler watches the counter itself
+          // and moves on as soon as the tile is ready, so the few tiles it has
+          // taken ahead keep the pair busy across a wait.  In a launch with
+          // few tiles per iteration (narrow tiles) a pair takes one tile at a
+          // time, waiting until its producer has passed the dependency: one
+          // holding several would run them one after another while other
+          // pairs sit idle at the end of the product.
+          if (t < p.tile_end) {
+            if (p.narrow) {
+              if (!wait_or_abort(ptx::smem_u32(&dep_bar[seq % kTileRing]), (seq / kTileRing) & 1, ab,
+                                 wait_code(0, kRoleDependency)))
+                break;
+            } else if (!ready) {
+              const Tile tl = decode_tile(p, t, 0);
+              const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;
+              if (!wait_done(p.done + tl.mi, need, ab, wait_code(tl.phase, kRoleDependency))) break;
+            }
+          }
         } else {
-          if (!pair_take(pair, seq, t, ab)) break;
+          if (!pair_take(pair, seq, t, ab) || !local_publish(ring, seq, t, ab)) break;
+          pair_free(pair, seq);
+          t &= ~kPollBit;
         }
-        if (!local_publish(ring, seq++, t, ab) || t >= p.tile_end) break;
+        ++seq;
+        if (t >= p.tile_end) break;
       }
     }
     __syncwarp();

@@ -133,3 +133,16 @@ def unblock(ws_bytes: np.ndarray, off: int, rows_pad: int, cols_pad: int) -> np.
         out[:, :, r, ch, :] = atoms[:, :, r, ch ^ r, :]
     dense = out.transpose(1, 2, 0, 3, 4).reshape(rows_pad, cols_pad)
     return bf16_bits_to_f32(dense)
+
+
+def symmetric_from_upper(m: np.ndarray, block: int = 256) -> np.ndarray:
+    """The full symmetric matrix from its blocks on or above the block diagonal
+    (block x block blocks), the form in which the workspace keeps A and B: each
+    block below the diagonal is the transpose of its mirror image."""
+    out = m.copy()
+    nb = m.shape[0] // block
+    for i in range(nb):
+        for j in range(i):
+            out[i * block:(i + 1) * block, j * block:(j + 1) * block] = \
+                m[j * block:(j + 1) * block, i * block:(i + 1) * block].T
+    return out

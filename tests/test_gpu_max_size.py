@@ -9,8 +9,9 @@ permutation's pattern is exactly zero (all products of zeros are exact zeros).
 phi(1/sqrt(s)) is taken from the oracle on the 2 x 2 matrix
 diag(1/sqrt(s), sqrt(1 - 1/s)), which has unit norm like the big input and the
 same first normalised singular value.  The big case still runs every tile of a
-32768-wide Gram, polynomial and update, the mirrored stores of the symmetric
-products and (for the tall case) the transposed paths.
+32768-wide Gram, polynomial and update, the transposed reads of the symmetric
+products' blocks below the diagonal and (for the tall case) the transposed
+final stores.
 """
 import math
 

@@ -167,8 +167,10 @@ def test_each_product_from_workspace(mfsdp, ns_steps):
         Yw = H.unblock(wsb, x0, sp, lp).astype(np.float64)
         assert np.array_equal(Yw[:sd, :ld], X), "X0 is not bf16(U) (G is bf16 and M = G)"
         assert np.all(Yw[sd:, :] == 0) and np.all(Yw[:, ld:] == 0), "X0 padding not zero"
-        Aw = H.unblock(wsb, a_off, sp, sp).astype(np.float64)[:sd, :sd]
-        Bw = H.unblock(wsb, b_off, sp, sp).astype(np.float64)[:sd, :sd]
+        # A and B are kept as their blocks on or above the diagonal of
+        # 256 x 256 blocks
+        Aw = H.symmetric_from_upper(H.unblock(wsb, a_off, sp, sp)).astype(np.float64)[:sd, :sd]
+        Bw = H.symmetric_from_upper(H.unblock(wsb, b_off, sp, sp)).astype(np.float64)[:sd, :sd]
         O = upd[s.offset:s.offset + s.rows * s.cols].reshape(s.rows, s.cols).astype(np.float64)
         O = O.T if s.rows > s.cols else O
         if ns_steps == 1:

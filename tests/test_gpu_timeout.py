@@ -2,8 +2,8 @@
 
 The test hook makes one tile of the next Newton-Schulz launch wait for a
 dependency that nothing satisfies.  The first wait on it to pass its 2 s limit
-(the scheduler's, or its pair's roles waiting to be handed that tile) records
-the status word.  Every other wait of every CTA sees
+(its pair's producers', the roles waiting behind them, or roles waiting to be
+handed a tile) records the status word.  Every other wait of every CTA sees
 the word and stops, so the kernel ends in bounded time.  The host reads
 MFSDP_ERR_DEVICE_TIMEOUT with the waiting role and product in the detail
 word.  The context stays usable: the next step succeeds and matches the
@@ -21,7 +21,7 @@ from tests.test_gpu_parity import check_matrix, run_step
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-ROLE_DEPENDENCY = 5   # the scheduler's wait for the stalled tile's dependency
+ROLE_DEPENDENCY = 5   # a wait for the stalled tile's dependency (producer, or a role behind it)
 ROLE_TILE_FULL = 8    # a role of the stalled pair waiting for that tile to be handed out
 
 

@@ -19,3 +19,16 @@ def test_unblock_matches_documented_formula():
             buf[off + atom + inner: off + atom + inner + 2] = np.frombuffer(bits[r, c].tobytes(), np.uint8)
     out = H.unblock(buf, off, rows_pad, cols_pad)
     assert np.array_equal(out, H.bf16_bits_to_f32(bits))
+
+
+def test_symmetric_from_upper_restores_lower_blocks():
+    rng = np.random.default_rng(5)
+    full = rng.standard_normal((768, 768)).astype(np.float32)
+    full = full + full.T
+    kept = full.copy()
+    for i in range(3):
+        for j in range(i):
+            kept[i * 256:(i + 1) * 256, j * 256:(j + 1) * 256] = np.nan   # never stored
+    assert np.array_equal(H.symmetric_from_upper(kept), full)
+    # the diagonal 256 x 256 blocks are kept whole, including their lower halves
+    assert np.array_equal(H.symmetric_from_upper(kept)[300:400, 260:290], full[300:400, 260:290])
