@@ -160,14 +160,19 @@ GemmTiling gemm_tiling(int mode, int s_pad, int l_pad, int width = kBlockN) {
   return t;
 }
 
-// Narrow tiles (256 x 128) for a launch whose tiles per Newton-Schulz
-// iteration at the full width are fewer than twice the SMs: such an owner set
-// is bound by its chain of dependent products, and halving a tile halves its
-// epilogue and main loop, which sit on that chain; larger sets keep the
-// full-width tiles, whose per-stage fixed costs are spread over twice the
-// MMAs.  Every output element sums its products in the same order either way,
-// so the update is bit for bit the same.
-bool use_narrow_tiles(const Layout& L, int base, int cnt) {
+// Tile widths of a launch.  A launch whose tiles per Newton-Schulz iteration
+// at the full width are fewer than twice the SMs is "narrow": such an owner
+// set is bound by its chain of dependent products.  In it, a product whose
+// full-width tiles are fewer than the CTA pairs (half the SMs) uses narrow
+// tiles (256 x 128): twice the tiles for the idle pairs, half the epilogue
+// each, on the chain; a product with more tiles keeps the full width, since a
+// narrow pair MMA runs at half the full-width rate and such a product is
+// bound by its pairs' throughput.  Larger sets keep the full width
+// throughout.  Every output element sums its products in the same order at
+// either width, so the update is bit for bit the same.  Returns the launch's
+// flag; *mask (bit k: product k narrow) receives the widths.
+bool use_narrow_tiles(const Layout& L, int base, int cnt, int32_t* mask) {
+  *mask = 0;
   static std::mutex mu;
   static int sms[kMaxPipeDevices] = {};
   int dev = 0;
@@ -180,12 +185,16 @@ bool use_narrow_tiles(const Layout& L, int base, int cnt) {
     n_sm = sms[dev];
   }
   if (n_sm <= 0) return false;
-  int64_t per_iter = 0;
+  int64_t sym = 0, upd = 0;
   for (int i = base; i < base + cnt; ++i) {
     const MatLayout& m = L.mats[i];
-    per_iter += 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad).tiles + gemm_tiling(kUpdate, m.s_pad, m.l_pad).tiles;
+    sym += gemm_tiling(kGram, m.s_pad, m.l_pad).tiles;
+    upd += gemm_tiling(kUpdate, m.s_pad, m.l_pad).tiles;
   }
-  return per_iter < 2 * (int64_t)n_sm;
+  if (2 * sym + upd >= 2 * (int64_t)n_sm) return false;
+  if (2 * sym < n_sm) *mask |= (1 << kGram) | (1 << kPoly);
+  if (2 * upd < n_sm) *mask |= 1 << kUpdate;
+  return true;
 }
 
 // Tensor-core FLOPs one product of one matrix executes (padded dimensions;
@@ -264,7 +273,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.9.5"; }
+extern "C" const char* mfsdp_version(void) { return "0.9.6"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -807,8 +816,9 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       nb.decay = (float)(1.0 - apply->lr * apply->wd);
       nb.w_bf16 = apply->w_dtype == MFSDP_DTYPE_BF16;
     }
-    nb.narrow = use_narrow_tiles(L, base, cnt) ? 1 : 0;
-    const int width = nb.narrow ? kBlockN / 2 : kBlockN;
+    nb.narrow = use_narrow_tiles(L, base, cnt, &nb.narrow_mask) ? 1 : 0;
+    const int width_sym = (nb.narrow_mask >> kGram) & 1 ? kBlockN / 2 : kBlockN;
+    const int width_upd = (nb.narrow_mask >> kUpdate) & 1 ? kBlockN / 2 : kBlockN;
     for (int k = 0; k < cnt; ++k) {
       const int i = base + k;
       const MatLayout& m = L.mats[i];
@@ -826,8 +836,8 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       d.l_pad = m.l_pad;
       d.s = m.s;
       d.l = m.l;
-      const GemmTiling ts = gemm_tiling(kGram, m.s_pad, m.l_pad, width);
-      const GemmTiling tu = gemm_tiling(kUpdate, m.s_pad, m.l_pad, width);
+      const GemmTiling ts = gemm_tiling(kGram, m.s_pad, m.l_pad, width_sym);
+      const GemmTiling tu = gemm_tiling(kUpdate, m.s_pad, m.l_pad, width_upd);
       d.tiles_sym = ts.tiles;
       d.tiles_m = tu.tiles_m;
       d.tiles_n = tu.tiles_n;

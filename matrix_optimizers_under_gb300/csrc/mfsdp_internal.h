@@ -124,7 +124,8 @@ struct NsBatch {
   int32_t stall_tile;    // test hook: this tile's dependency target is never reached (-1: none)
   int32_t iter_tiles;    // tiles of one iteration (three products, all matrices)
   int32_t mode_start[3];
-  int32_t narrow;        // tiles 256 x 128 instead of 256 x 256 (owner sets with few tiles: twice the tiles, half the epilogue each)
+  int32_t narrow;        // a launch with few tiles per iteration (its pairs take one tile at a time)
+  int32_t narrow_mask;   // bit k: product k (kGram, kPoly, kUpdate) uses tiles 256 x 128 instead of 256 x 256
   int32_t out_bf16;      // final update dtype
   int32_t w_bf16;        // apply: weight dtype
   float a, b, c;

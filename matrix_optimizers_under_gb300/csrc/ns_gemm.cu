@@ -17,9 +17,10 @@
 // read either form; a diagonal 256 x 256 block is computed and stored whole,
 // so it needs none): every product reads exactly the values it would read
 // from the full matrix, and no epilogue writes a transposed copy.  A pair's
-// tile is 256 x 256, or 256 x 128 ("narrow") in a launch with few tiles per
-// iteration, where the chain of dependent products sets the time; each output
-// element sums the same products in the same order at either width.
+// tile is 256 x 256, or 256 x 128 ("narrow") for a product with fewer
+// full-width tiles than CTA pairs in a launch with few tiles per iteration,
+// where the chain of dependent products sets the time; each output element
+// sums the same products in the same order at either width.
 //
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
@@ -302,7 +303,7 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
   r.a_sym = prod != kGram;
   r.b_sym = prod == kPoly;
   r.b_mn = prod == kUpdate;
-  const int width = p.narrow ? kBlockN / 2 : kBlockN;    // tile columns
+  const int width = (p.narrow_mask >> prod) & 1 ? kBlockN / 2 : kBlockN;    // tile columns
   if (r.symmetric) {
     // Row pair-block I holds the tiles of columns 256 I .. s_pad - 1: nb2 - I
     // of them, or twice that for narrow tiles.
@@ -995,7 +996,7 @@ uint64_t wait_limit_ns(const NsBatch& b, int pairs) {
   double prod[3] = {0.0, 0.0, 0.0};
   for (int i = 0; i < b.n; ++i) {
     const NsMat& d = b.mat[i];
-    const double tile = 2.0 * kPairM * (b.narrow ? kBlockN / 2 : kBlockN);   // FLOPs of one output tile per unit of K
+    const double tile = 2.0 * kPairM * ((b.narrow_mask >> kGram) & 1 ? kBlockN / 2 : kBlockN);   // FLOPs of one symmetric tile per unit of K
     prod[kGram] += d.tiles_sym * tile * d.l_pad;
     prod[kPoly] += d.tiles_sym * tile * d.s_pad;
     prod[kUpdate] += 2.0 * d.s_pad * (double)d.s_pad * d.l_pad;

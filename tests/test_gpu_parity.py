@@ -467,10 +467,13 @@ def test_empty_owner_set(mfsdp):
 
 def test_narrow_and_full_width_tiles_agree(mfsdp):
     """A launch with few tiles per iteration (fewer than twice the SMs) runs
-    256 x 128 tiles, a larger one 256 x 256 tiles; each output element sums the
-    same products in the same order either way.  The 768 x 2304 matrix run
-    alone (narrow tiles) and inside a launch with twenty 2048 x 2048 matrices
-    (full width) gives the same update and momentum, bit for bit."""
+    256 x 128 tiles for each product with fewer full-width tiles than CTA
+    pairs, a larger one 256 x 256 tiles throughout; each output element sums
+    the same products in the same order either way.  The 768 x 2304 matrix run
+    alone (narrow tiles), beside the GPT-2 block's other three matrices (narrow
+    Gram and polynomial tiles, full-width update tiles) and inside a launch
+    with twenty 2048 x 2048 matrices (full width) gives the same update and
+    momentum, bit for bit."""
     dev = _dev()
     rng = np.random.default_rng(31)
     shapes = [(768, 2304)] + [(2048, 2048)] * 20
@@ -487,4 +490,13 @@ def test_narrow_and_full_width_tiles_agree(mfsdp):
     u1, m1, _ = run_step(mfsdp, [s], grad[:n].copy(), np.zeros(n, np.float32), update_dtype=torch.bfloat16)
     assert np.array_equal(u1.view(np.uint32), upd[:n].view(np.uint32))
     assert np.array_equal(m1, mom[:n])
+    mixed = [(768, 2304), (768, 768), (768, 3072), (3072, 768)]
+    shards_m, off = [], 0
+    for i, (r, c) in enumerate(mixed):
+        shards_m.append(mfsdp.make_shard(off, r, c, param_id=i))
+        off += r * c
+    grad_m = np.concatenate([grad[:n], W.f32_to_bf16_bits((rng.standard_normal(off - n) * 1e-3).astype(np.float32))])
+    u2, m2, _ = run_step(mfsdp, shards_m, grad_m, np.zeros(off, np.float32), update_dtype=torch.bfloat16)
+    assert np.array_equal(u2[:n].view(np.uint32), upd[:n].view(np.uint32))
+    assert np.array_equal(m2[:n], mom[:n])
     check_matrix(s, upd, mom, grad, mom0, ns_steps=5)
