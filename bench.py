@@ -383,30 +383,32 @@ class OwnerStep:
         # per batch of 128 matrices: momentum, norm finalise, one Newton-Schulz launch
         self.launches = 3 * batches + (1 if tail_numel else 0)
 
-    def adamw(self):
+    def adamw(self, stream=None):
         w = self.w
         self.mfsdp.adamw_tail_step(self.tp, self.tg, self.tm, self.tv, lr=w.lr, beta1=w.betas[0], beta2=w.betas[1],
-                                   eps=w.adam_eps, wd=w.weight_decay, step=self.count)
+                                   eps=w.adam_eps, wd=w.weight_decay, step=self.count, stream=stream)
 
-    def step(self, ev=None):
+    def step(self, ev=None, stream=None):
+        """One owner step on self.stream, or on `stream` (a capture stream)."""
         m = self.mfsdp
+        s = stream or self.stream
         self.count += 1
         if ev:
-            ev[0].record(self.stream)
+            ev[0].record(s)
         if self.shards:
             m.muon_owner_step(self.shards, self.grad, self.mom, self.upd, self.ws, phases=m.PHASE_MOMENTUM,
-                              **self.kw)
+                              stream=s, **self.kw)
         if ev:
-            ev[1].record(self.stream)
+            ev[1].record(s)
         if self.shards:
             m.muon_owner_step(self.shards, self.grad, self.mom, self.upd, self.ws, phases=m.PHASE_NEWTON_SCHULZ,
-                              **self.kw)
+                              stream=s, **self.kw)
         if ev:
-            ev[2].record(self.stream)
+            ev[2].record(s)
         if self.tail_numel:
-            self.adamw()
+            self.adamw(stream=s)
         if ev:
-            ev[3].record(self.stream)
+            ev[3].record(s)
 
     def check_status(self, when):
         if not self.shards:
@@ -476,6 +478,32 @@ def time_resident(step, steps, warmup, sampler=None, barrier=None):
     return t0.elapsed_time(t1), ms, per_step, clocks
 
 
+def time_graph(step, steps):
+    """The same owner step captured once in a CUDA graph and replayed `steps`
+    times back to back (3 untimed replays first): the device time of the step
+    without the host's per-call work between its launches, which a small owner
+    set's step is short enough to expose.  Returns ms per step."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step.step(stream=torch.cuda.current_stream())
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step.check_status("after the graph replays")
+    ms = e0.elapsed_time(e1) / steps
+    del graph
+    return ms
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -522,6 +550,8 @@ def run_ours(args):
     phases = figures(mfsdp, step, phase_ms, peaks)
     phases.update({"step_ms_median": round(statistics.median(steps_ms), 4), "step_ms_min": round(steps_ms[0], 4),
                    "step_ms_max": round(steps_ms[-1], 4)})
+    if rank == 0 and not args.no_supplementary:
+        phases["step_ms_graph"] = round(time_graph(step, min(args.steps, 10)), 4)
 
     # ---------------------------------------------------------- end to end
     # Through the host-buffer entry point: each step copies the gradient in from
@@ -663,10 +693,12 @@ def run_ours(args):
             st_ = OwnerStep(mfsdp, ws_, sh, nm, tn, g_np, dev)
             k = args.supp_steps
             tot, pms, sms, clk = time_resident(st_, k, max(args.warmup, 3), ClockSampler(local_rank))
+            graph_ms = time_graph(st_, max(k, 10))
             fig = figures(mfsdp, st_, pms, peaks)
             fig.pop("momentum_bytes")
             sup["workloads"][name] = {"owner_step_ms": round(tot / k, 4),
                                       "owner_step_ms_median": round(statistics.median(sms), 4),
+                                      "owner_step_ms_graph": round(graph_ms, 4),
                                       "steps": k, "matrices": len(sh), "elements": sum(s.rows * s.cols for s in sh),
                                       "tail_elems": tn, **fig,
                                       "sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons")}
