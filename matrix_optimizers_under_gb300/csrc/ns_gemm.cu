@@ -840,8 +840,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
           store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
         }
-        // the stage is free again before anyone writes the next block (or tile) into it
-        if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }
+        // the stage is free again before anyone writes the next block into it
+        // (after the last block: once this warp's share is published)
+        if (blk + 1 < nblk && !half_sync(hbar, hphase, ab, code)) { live = false; break; }
       }
       if (!live) break;
       ++acc_it;
@@ -855,6 +856,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         __syncwarp();
         if (lane == 0) ptx::red_release_gpu_add(p.done + tl.mi, 1);
       }
+      // ... and before anyone writes the next tile into it
+      if (!half_sync(hbar, hphase, ab, wait_code(tl.phase, kRoleAccFull))) break;
     }
   } else {
     if (lane == 0) {
