@@ -188,7 +188,7 @@ enum WaitRole : int32_t {
   kRoleStageFull = 2,   // MMA issuer: a stage's operands
   kRoleAccFree = 3,     // MMA issuer: an accumulator the epilogue has drained
   kRoleAccFull = 4,     // epilogue: a finished accumulator
-  kRoleDependency = 5,  // scheduler: earlier products of the tile's matrix
+  kRoleDependency = 5,  // producer or scheduler, or a role waiting behind the producer: earlier products of the tile's matrix
   kRoleTileFree = 7,    // scheduler: a ring slot every reader has taken
   kRoleTileFull = 8,    // producer, MMA issuer, epilogue: the next tile index
 };

@@ -45,16 +45,19 @@
 // each pair a scheduler warp of the even CTA takes the next index and hands
 // the tile to its own CTA's roles and to the odd CTA's scheduler (a remote
 // store and mbarrier arrive), which passes it to the odd CTA's roles; each CTA
-// passes tiles through a small ring in shared memory.  The producer of each
-// CTA waits (acquire) until the counter of the tile's matrix covers every tile
-// of the earlier products before its tensor copies, and tells its CTA's other
-// roles through an mbarrier; the scheduler takes the next index only once
-// that wait is over, so a pair that cannot start a tile takes no more of the
-// list.  Both producers watch the counter themselves because a hand-over
+// passes tiles through a small ring in shared memory.  The scheduler reads
+// the counter of the tile's matrix once (acquire): a tile whose earlier
+// products are all stored goes out "ready", any other marked "wait", and then
+// both producers of the pair poll the counter (acquire) until it covers every
+// tile of the earlier products before their tensor copies -- a hand-over
 // across the pair costs a cluster-scope release (~850 cycles on GB300), which
 // would otherwise lie between a product's last store and the next product's
-// first copies.  The scheduler runs ahead of the roles, so taking a tile
-// costs the pipeline nothing while work is ready.  Small matrices run ahead
+// first copies.  Each producer tells its CTA's other roles through an
+// mbarrier.  The scheduler takes the next index only once the tile may start
+// (it polls the counter too, or in a small launch waits for its producer), so
+// a pair that cannot start a tile takes no more of the list; otherwise it
+// runs ahead of the roles, so taking a tile costs the pipeline nothing while
+// work is ready.  Small matrices run ahead
 // through their iterations while large ones fill the machine, with no launch
 // gap or tail between products.  Every dependency points to an earlier
 // position of the list and tiles are taken in list order, so the lowest
@@ -862,14 +865,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   } else {
     if (lane == 0) {
       // ----------------------------------------------------------- scheduler
-      // Even CTA: takes the pair's tiles in list order and hands each to
-      // this CTA's roles and to the odd CTA's scheduler (the end marker last),
-      // then waits until this CTA's producer has seen the tile's earlier
-      // products stored before it takes the next: a pair that cannot start a
-      // tile takes no more of the list, which other pairs may be able to
-      // start.  Odd CTA: forwards what it receives to its own roles, then
-      // frees the pair slot.  Each hand-over across the pair costs a
-      // cluster-scope release (~850 cycles), which is why the producers wait
+      // Even CTA: takes the pair's tiles in list order, marks each "ready"
+      // or "wait" from one read of its matrix's counter, and hands it to this
+      // CTA's roles and to the odd CTA's scheduler (the end marker last); it
+      // takes the next tile only once this one may start (below), so a pair
+      // that cannot start a tile takes no more of the list, which other pairs
+      // may be able to start.  Odd CTA: forwards what it receives to its own
+      // roles, then frees the pair slot.  Each hand-over across the pair costs
+      // a cluster-scope release (~850 cycles), which is why the producers wait
       // for the dependencies themselves and the local hand-overs go first.
       uint32_t seq = 0;
       while (true) {
