@@ -120,9 +120,11 @@ int mfsdp_plan_owners(const mfsdp_param* params, int32_t n_params, int32_t world
 
 /* Bytes of device workspace mfsdp_muon_owner_step needs for these shards
  * (0 on invalid input).  Holds, per matrix, X (two bf16 ping-pong copies of
- * the s x l iterate) and the s x s bf16 matrices A = X X^T and B = bA + cA^2,
- * each padded to multiples of 128 (the short side to 256), plus norm
- * partials, the Newton-Schulz tile and completion counters and a status word. */
+ * the s x l iterate, the second at least three s x s matrices long when the
+ * shape may run the Gram-space form, whose C and Q it holds) and the s x s
+ * bf16 matrices A = X X^T and B = bA + cA^2 (Gram space: P), each padded to
+ * multiples of 128 (the short side to 256), plus norm partials, the
+ * Newton-Schulz tile and completion counters and a status word. */
 size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards);
 
 /* Owner-local Muon step over one rank's owned matrices (Abstract: the reduced
@@ -135,9 +137,19 @@ size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_sh
  *   X  = U / (||U||_F + eps), transposed to s x l when rows > cols
  *   ns_steps times:  A = X X^T,  B = b*A + c*A*A,  X <- a*X + B*X
  *   update[offset ..] = X, transposed back to rows x cols.
+ * A matrix with l >= 2 s, l >= s + 384 and s >= 128, for 1 <= ns_steps <= 5,
+ * evaluates the same iteration in Gram space: with P_k = a I + b A_k + c A_k A_k,
+ * X_{k+1} = P_k X_k, so A_{k+1} = P_k A_k P_k and the update is
+ * P_{T-1} ... P_0 X: it iterates the s x s matrices A (as C = P A, A <- C P)
+ * and Q = P_k Q_{k-1}, and multiplies X by Q once (about half the tensor
+ * FLOPs of the direct form for such shapes, and the long K = l only in the
+ * first Gram product; equal in exact arithmetic, and within the same error of
+ * the fp64 definition in bf16).  mfsdp_muon_gram_space_layout says which
+ * matrices do.
  * The Newton-Schulz products run on tensor cores with bf16 operands and fp32
- * accumulation; A, B and X are held in bf16 between products, and the
- * hyper-parameters are applied as fp32 values rounded from the doubles given.
+ * accumulation; A, B and X (Gram space: A, P, C, Q) are held in bf16 between
+ * products, and the hyper-parameters are applied as fp32 values rounded from
+ * the doubles given.
  * A matrix whose momentum is exactly zero gets an all-zero update.  The fp32
  * Gram product needs ||U||_F < 1e18 and the entries of U above ~1e-18 in
  * magnitude (outside that range the result may be Inf/NaN or lose the small
@@ -364,6 +376,18 @@ int mfsdp_test_inject_stall(int32_t tile);
  * hold only their 256 x 256 blocks on or above the diagonal (col/256 >=
  * row/256); the others are never written.  Returns the status. */
 int mfsdp_muon_workspace_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int64_t* out);
+
+/* Which form of the iteration each matrix runs for ns_steps, and where the
+ * Gram-space form keeps its matrices, for inspection: for shard i,
+ * out[4*i + 0..3] = { 1 if Gram space else 0, byte offset of C, of Q_even,
+ * of Q_odd } (s_pad x s_pad, the blocked layout above, inside X1's region;
+ * P_0 = Q_0 is written to Q_even, P_k (k >= 1) to B; after a step the
+ * workspace holds A_{T-1}, P_{T-1}, C_{T-2} and Q_{T-1} (in Q_even for odd T),
+ * the symmetric ones as their 256 x 256 blocks on or above the diagonal).
+ * Returns INVALID_ARG for ns_steps outside 0..64 or a NULL out, else as
+ * mfsdp_muon_workspace_layout. */
+int mfsdp_muon_gram_space_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t ns_steps,
+                                 int64_t* out);
 
 /* AdamW over a packed fp32 tail buffer (Abstract: non-matrix tensors "stay on
  * AdamW"), decoupled weight decay, step counted from 1:

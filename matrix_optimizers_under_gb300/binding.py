@@ -44,7 +44,8 @@ EXPORTED = ("mfsdp_plan_owners", "mfsdp_muon_workspace_bytes", "mfsdp_muon_owner
             "mfsdp_muon_step_flops", "mfsdp_muon_owner_step_host", "mfsdp_muon_owner_step_apply",
             "mfsdp_model_layout", "mfsdp_placement_segments", "mfsdp_segment_copy", "mfsdp_test_inject_stall",
             "mfsdp_host_step_groups", "mfsdp_muon_static_scratch_status", "mfsdp_checkpoint_bytes",
-            "mfsdp_checkpoint_write", "mfsdp_checkpoint_read_header", "mfsdp_checkpoint_read")
+            "mfsdp_checkpoint_write", "mfsdp_checkpoint_read_header", "mfsdp_checkpoint_read",
+            "mfsdp_muon_gram_space_layout")
 
 SEGMENT_REDUCE = 0
 SEGMENT_GATHER = 1
@@ -89,6 +90,8 @@ _lib.mfsdp_muon_workspace_bytes.argtypes = [ctypes.POINTER(MatrixShard), _i32]
 _lib.mfsdp_muon_workspace_bytes.restype = _sz
 _lib.mfsdp_muon_workspace_layout.argtypes = [ctypes.POINTER(MatrixShard), _i32, ctypes.POINTER(_i64)]
 _lib.mfsdp_muon_workspace_layout.restype = ctypes.c_int
+_lib.mfsdp_muon_gram_space_layout.argtypes = [ctypes.POINTER(MatrixShard), _i32, _i32, ctypes.POINTER(_i64)]
+_lib.mfsdp_muon_gram_space_layout.restype = ctypes.c_int
 _STEP_ARGS = [ctypes.POINTER(MatrixShard), _i32, _vp, _i32, _vp, _vp, _i32, _i64, _d, _i32, _i32, _d, _d, _d, _d,
               _vp, _sz, _vp]
 _lib.mfsdp_muon_owner_step.argtypes = _STEP_ARGS
@@ -267,6 +270,15 @@ def muon_workspace_layout(shards: Sequence[MatrixShard]) -> List[Tuple[int, ...]
     out = (_i64 * max(8 * len(shards), 1))()
     _check(_lib.mfsdp_muon_workspace_layout(_shard_array(shards), len(shards), out), "muon_workspace_layout")
     return [tuple(out[8 * i: 8 * i + 8]) for i in range(len(shards))]
+
+
+def muon_gram_space_layout(shards: Sequence[MatrixShard], ns_steps: int = 5) -> List[Tuple[int, ...]]:
+    """Per shard (1 if the Gram-space form runs else 0, offset of C, of Q_even,
+    of Q_odd) for ns_steps (see include/mfsdp.h)."""
+    out = (_i64 * max(4 * len(shards), 1))()
+    _check(_lib.mfsdp_muon_gram_space_layout(_shard_array(shards), len(shards), int(ns_steps), out),
+           "muon_gram_space_layout")
+    return [tuple(out[4 * i: 4 * i + 4]) for i in range(len(shards))]
 
 
 def muon_step_flops(shards: Sequence[MatrixShard], ns_steps: int = 5) -> Tuple[int, int]:

@@ -57,7 +57,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct MatLayout {
   int s, l, s_pad, l_pad;
   int transposed;
+  int gram_ok;           // the shape may run the Gram-space program (gram_space_shape)
   size_t x0, x1, a, b;   // byte offsets in the workspace
+  size_t c, q0, q1;      // Gram-space program: C and the Q ping-pong, inside X1's region
   int tiles_k1;          // momentum-kernel tiles (kTile x kTile over s_pad x l_pad)
   int partial0;
 };
@@ -78,6 +80,23 @@ int shape_ok(const mfsdp_matrix_shard& sh) {
   return MFSDP_OK;
 }
 
+// Shapes that run the Gram-space program (for 1 .. kGramSpaceMaxSteps steps):
+// a long side at least twice the short side, where it executes about half
+// the standard program's tensor FLOPs and keeps the long K = l out of every
+// iteration but the first, and a short side of at least 128.  A bf16
+// emulation of both programs against the fp64 definition gives the
+// Gram-space one the same or a smaller relative error on such shapes (0.7-1.1 %
+// at 5 steps), and a larger one on near-square shapes (5 % at l = s), which
+// keep the standard program.  Below a short side of 384 the long side must
+// also exceed it by 384: the Gram-space program runs one product more, which
+// on a small latency-bound matrix costs more than its shorter Gram products
+// save (256 x 512 alone: 1.03x the time).
+int gram_space_shape(int s, int l) { return s >= 128 && l >= 2 * s && l >= s + 384; }
+
+bool use_gram_space(const MatLayout& m, int32_t ns_steps) {
+  return m.gram_ok && ns_steps >= 1 && ns_steps <= kGramSpaceMaxSteps;
+}
+
 int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
   if (n < 0 || (n > 0 && !shards)) return MFSDP_ERR_INVALID_ARG;
   L->mats.resize(n);
@@ -91,6 +110,7 @@ int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
     m.s_pad = (int)round_up((size_t)m.s, kPadS);
     m.l_pad = (int)round_up((size_t)m.l, kPad);
     m.transposed = shards[i].rows > shards[i].cols ? 1 : 0;
+    m.gram_ok = gram_space_shape(m.s, m.l);
     m.tiles_k1 = (m.s_pad / kTile) * (m.l_pad / kTile);
     m.partial0 = partials;
     partials += m.tiles_k1;
@@ -107,7 +127,12 @@ int make_layout(const mfsdp_matrix_shard* shards, int n, Layout* L) {
     MatLayout& m = L->mats[i];
     const size_t xb = (size_t)m.s_pad * m.l_pad * 2, ab = (size_t)m.s_pad * m.s_pad * 2;
     m.x0 = off; off += xb;
-    m.x1 = off; off += xb;
+    // X1 (standard program) or C and the two Q (Gram-space program)
+    m.x1 = off;
+    m.c = off;
+    m.q0 = off + ab;
+    m.q1 = off + 2 * ab;
+    off += m.gram_ok ? std::max(xb, 3 * ab) : xb;
     m.a = off; off += ab;
     m.b = off; off += ab;
   }
@@ -213,18 +238,21 @@ uint64_t executed_flops(int mode, int s_pad, int l_pad) {
 bool ns_counts_fit(const Layout& L, int32_t ns_steps) {
   const int n = (int)L.mats.size();
   for (int base = 0; base < n; base += kMaxBatch) {
-    int64_t batch = 0;
+    int64_t batch = 0, fin = 0;
     for (int i = base; i < std::min(n, base + kMaxBatch); ++i) {
       const MatLayout& m = L.mats[i];
-      // narrow tiles, the larger count
-      const int64_t per_iter = 2 * (int64_t)gemm_tiling(kGram, m.s_pad, m.l_pad, kBlockN / 2).tiles +
-                               gemm_tiling(kUpdate, m.s_pad, m.l_pad, kBlockN / 2).tiles;
-      if (per_iter * ns_steps * 2 * kEpilogueWarps > INT32_MAX) return false;
+      // narrow tiles, the larger count; either program (the Gram-space one
+      // has four symmetric products per iteration and a final update-like one)
+      const int64_t sym = gemm_tiling(kGram, m.s_pad, m.l_pad, kBlockN / 2).tiles;
+      const int64_t upd = gemm_tiling(kUpdate, m.s_pad, m.l_pad, kBlockN / 2).tiles;
+      const int64_t per_iter = 4 * sym + upd;
+      if ((per_iter * ns_steps + upd) * 2 * kEpilogueWarps > INT32_MAX) return false;
       batch += per_iter;
+      fin += upd;
     }
     // headroom: pairs overshoot the tile counter; bit 30 of a handed-out
     // tile index is a flag
-    if (batch * ns_steps > (int64_t(1) << 30) - 65536) return false;
+    if (batch * ns_steps + fin > (int64_t(1) << 30) - 65536) return false;
   }
   return true;
 }
@@ -273,7 +301,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.9.6"; }
+extern "C" const char* mfsdp_version(void) { return "0.10.0"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -801,7 +829,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
     nb.n = cnt;
     nb.ns_steps = ns_steps;
     nb.phase_begin = 0;
-    nb.phase_end = 3 * ns_steps;
+    nb.phase_end = 3 * ns_steps;   // + 1 below when a Gram-space matrix has its final product
     nb.out_bf16 = update_dtype == MFSDP_DTYPE_BF16;
     nb.a = a;
     nb.b = b;
@@ -827,6 +855,11 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       d.x[1] = ws + m.x1;
       d.a = ws + m.a;
       d.b = ws + m.b;
+      d.gram_space = use_gram_space(m, ns_steps) ? 1 : 0;
+      d.c = ws + m.c;
+      d.q[0] = ws + m.q0;
+      d.q[1] = ws + m.q1;
+      if (d.gram_space) nb.phase_end = 3 * ns_steps + 1;
       d.out = update ? static_cast<void*>(static_cast<uint8_t*>(update) + (size_t)shards[i].offset * usz) : nullptr;
       if (apply) {
         d.w = static_cast<uint8_t*>(apply->w) + (size_t)shards[i].offset * dtype_size(apply->w_dtype);
@@ -847,27 +880,38 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
     }
     // Inside each product, longest K first: the persistent pairs take tiles
-    // round-robin, so the last rounds hold the cheapest tiles.
+    // round-robin, so the last rounds hold the cheapest tiles.  Products 0-2
+    // repeat every iteration; product 3, after the last iteration, holds the
+    // Gram-space matrices' final X = Q X0.
     int32_t off = 0;
-    for (int prod = kGram; prod <= kUpdate; ++prod) {
+    for (int prod = 0; prod <= 3; ++prod) {
       std::vector<int> order(cnt);
       for (int k = 0; k < cnt; ++k) order[k] = k;
-      auto kb_of = [&](int k) { return prod == kGram ? nb.mat[k].l_pad : nb.mat[k].s_pad; };
+      auto kb_of = [&](int k) {
+        const NsMat& d = nb.mat[k];
+        return prod == kGram && !d.gram_space ? d.l_pad : d.s_pad;
+      };
+      auto tiles_of = [&](const NsMat& d) {
+        if (prod == 3) return d.gram_space ? d.tiles_m * d.tiles_n : 0;
+        if (prod == 2) return d.gram_space ? 2 * d.tiles_sym : d.tiles_m * d.tiles_n;
+        return d.tiles_sym;
+      };
       std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return kb_of(x) > kb_of(y); });
-      nb.mode_start[prod] = off;
+      if (prod < 3) nb.mode_start[prod] = off;
       int32_t tiles = 0;
       for (int j = 0; j < cnt; ++j) {
         const NsMat& d = nb.mat[order[j]];
         nb.order[prod][j] = (uint8_t)order[j];
         nb.tile_start[prod][j] = tiles;
-        tiles += prod == kUpdate ? d.tiles_m * d.tiles_n : d.tiles_sym;
+        tiles += tiles_of(d);
       }
       nb.tile_start[prod][cnt] = tiles;
-      off += tiles;
+      if (prod < 3) off += tiles;
+      else nb.tile_end = off * ns_steps + tiles;
     }
     nb.iter_tiles = off;
+    nb.final_start = off * ns_steps;
     nb.tile_begin = 0;
-    nb.tile_end = off * ns_steps;
     nb.stall_tile = g_stall_tile.exchange(-1);
     st = cuda_status(cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(n_shards + 1), stream));
     if (st != MFSDP_OK) return st;
@@ -891,11 +935,31 @@ extern "C" int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n
     const MatLayout& m = L.mats[i];
     const uint64_t s = (uint64_t)m.s, l = (uint64_t)m.l;
     dn += (uint64_t)ns_steps * (4 * s * s * l + 2 * s * s * s);
-    ex += (uint64_t)ns_steps * (executed_flops(kGram, m.s_pad, m.l_pad) + executed_flops(kPoly, m.s_pad, m.l_pad) +
-                                executed_flops(kUpdate, m.s_pad, m.l_pad));
+    const uint64_t gram = executed_flops(kGram, m.s_pad, m.l_pad), sym = executed_flops(kPoly, m.s_pad, m.l_pad),
+                   upd = executed_flops(kUpdate, m.s_pad, m.l_pad);
+    if (use_gram_space(m, ns_steps))   // A_0, T P_k, T-1 each of C, A and Q, the final Q X0
+      ex += gram + (uint64_t)ns_steps * sym + 3ull * (uint64_t)(ns_steps - 1) * sym + upd;
+    else
+      ex += (uint64_t)ns_steps * (gram + sym + upd);
   }
   *dense = dn;
   *executed = ex;
+  return MFSDP_OK;
+}
+
+extern "C" int mfsdp_muon_gram_space_layout(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t ns_steps,
+                                            int64_t* out) {
+  if (ns_steps < 0 || ns_steps > 64) return MFSDP_ERR_INVALID_ARG;
+  Layout L;
+  const int st = make_layout(shards, n_shards, &L);
+  if (st != MFSDP_OK) return st;
+  if (n_shards > 0 && !out) return MFSDP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_shards; ++i) {
+    const MatLayout& m = L.mats[i];
+    int64_t* o = out + 4 * i;
+    o[0] = use_gram_space(m, ns_steps) ? 1 : 0;
+    o[1] = (int64_t)m.c; o[2] = (int64_t)m.q0; o[3] = (int64_t)m.q1;
+  }
   return MFSDP_OK;
 }
 

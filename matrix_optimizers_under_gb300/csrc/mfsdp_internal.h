@@ -82,11 +82,18 @@ struct NormBatch {
 
 // ------------------------------------------------- Newton-Schulz GEMMs (K3-K5)
 enum GemmMode : int32_t {
-  kGram = 0,         // A = scale * X X^T               (X: K-major operand twice)
+  kGram = 0,         // A = scale * X X^T               (X: K-major operand twice); also a plain
+                     // product of two symmetric matrices (Gram-space program)
   kPoly = 1,         // B = b*A + c * A A               (A symmetric: K-major twice)
   kUpdate = 2,       // X' = scale * (a*X + B X)        (B K-major, X MN-major)
   kUpdateFinal = 3,  // same, written to the caller's update buffer
+  kPolyI = 4,        // P = a*I + b*A + c * A A          (Gram-space program)
+  kFinalQ = 5,       // X = scale * Q X0, written to the caller's update buffer (Gram-space program)
 };
+
+// The largest step count the Gram-space program runs (more steps take the
+// standard program): its error stays at the standard program's for up to 5.
+constexpr int kGramSpaceMaxSteps = 5;
 
 // One matrix of a Newton-Schulz launch: its workspace buffers and the tiling
 // of its three products.
@@ -99,6 +106,9 @@ struct NsMat {
   int32_t s_pad, l_pad;
   int32_t s, l;          // true short / long side
   int32_t tiles_sym;     // Gram / polynomial: pair tiles on or above the diagonal (256 or 128 wide)
+  int32_t gram_space;    // 1: the Gram-space program (below), 0: the standard one
+  uint8_t* c;            // Gram-space: blocked bf16 C = P A (s_pad x s_pad)
+  uint8_t* q[2];         // Gram-space: blocked bf16 Q ping-pong (Q_0 = P_0 is written to q[0])
   int32_t tiles_m, tiles_n;   // update: 256-row pair tiles, 256 (or 128, narrow) columns wide
   int32_t n_last;        // update: width of the last column tile
   int32_t norm_idx;      // index into the norm table
@@ -108,14 +118,26 @@ struct NsMat {
 };
 
 // One launch runs the products [phase_begin, phase_end) of the sequence
-//   for it in 0 .. ns_steps-1: Gram (3 it), polynomial (3 it + 1), update (3 it + 2)
-// over up to kMaxBatch matrices.  Its tiles form one list, product-major
-// (tile_begin .. tile_end-1 of the whole sequence's list), handed out in list
-// order to whichever CTA pair asks next.  Inside product k of
-// an iteration, matrix order[k][j] holds tiles [tile_start[k][j],
-// tile_start[k][j+1]) after mode_start[k].  A tile may start once every tile
-// of the earlier products of its matrix in this launch has been stored:
-// done[matrix] counts the epilogue warps that finished one.
+//   for it in 0 .. ns_steps-1: products 3 it, 3 it + 1, 3 it + 2
+//   then product 3 ns_steps (Gram-space matrices only)
+// over up to kMaxBatch matrices.  A matrix runs one of two programs that give
+// the same update in exact arithmetic:
+//   standard:     A = X X^T;  B = b A + c A A;  X <- a X + B X           (per iteration)
+//   Gram-space:   iteration 0: A_0 = X0 X0^T, P_0 = a I + b A_0 + c A_0 A_0, C_0 = P_0 A_0;
+//                 iteration k: A_k = C_{k-1} P_{k-1}, P_k = a I + b A_k + c A_k A_k,
+//                              C_k = P_k A_k (not in the last), Q_k = P_k Q_{k-1} (Q_0 = P_0);
+//                 then X = Q_{T-1} X0
+// (X_{k+1} = P_k X_k, so A_{k+1} = P_k A_k P_k and X_T = P_{T-1} .. P_0 X0).
+// Its tiles form one list, product-major (tile_begin .. tile_end-1 of the
+// whole sequence's list), handed out in list order to whichever CTA pair asks
+// next: iteration blocks of iter_tiles tiles, then the final Gram-space
+// products from final_start.  Inside product k of an iteration (k = 3: the
+// final block), matrix order[k][j] holds tiles [tile_start[k][j],
+// tile_start[k][j+1]) after mode_start[k].  A Gram-space matrix's product 2
+// holds its C tiles then its Q tiles; those that do not exist (Q in
+// iteration 0, C in the last) are null tiles, taken and skipped.  A tile may
+// start once every tile of the earlier products of its matrix in this launch
+// has been stored: done[matrix] counts the epilogue warps that finished one.
 struct NsBatch {
   int32_t n;
   int32_t ns_steps;
@@ -123,6 +145,7 @@ struct NsBatch {
   int32_t tile_begin, tile_end;
   int32_t stall_tile;    // test hook: this tile's dependency target is never reached (-1: none)
   int32_t iter_tiles;    // tiles of one iteration (three products, all matrices)
+  int32_t final_start;   // first tile of the final Gram-space products (ns_steps * iter_tiles)
   int32_t mode_start[3];
   int32_t narrow;        // a launch with few tiles per iteration (its pairs take one tile at a time)
   int32_t narrow_mask;   // bit k: product k (kGram, kPoly, kUpdate) uses tiles 256 x 128 instead of 256 x 256
@@ -136,8 +159,8 @@ struct NsBatch {
   uint64_t wait_limit_ns;  // every wait of the launch gives up after this long (ns_wait_limit_ns)
   int32_t* next_tile;    // tiles handed out so far (dynamic schedule), zeroed before the launch
   int32_t* done;         // per matrix of the launch, zeroed before it
-  int32_t tile_start[3][kMaxBatch + 1];
-  uint8_t order[3][kMaxBatch];
+  int32_t tile_start[4][kMaxBatch + 1];
+  uint8_t order[4][kMaxBatch];
   NsMat mat[kMaxBatch];
 };
 static_assert(kMaxBatch <= 256, "matrix order is stored in bytes");

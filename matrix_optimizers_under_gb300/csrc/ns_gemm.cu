@@ -252,14 +252,16 @@ __device__ __forceinline__ void store_final(const NsMat& d, const NsBatch& p, in
 
 struct Tile {
   int mi;        // matrix index in the batch
-  int phase;     // product index in the sequence: 3 * iteration + product
-  int mode;      // kGram, kPoly, kUpdate or kUpdateFinal
+  int phase;     // product index in the sequence: 3 * iteration + product (3 * ns_steps: final Gram-space)
+  int mode;      // a GemmMode
   bool first;    // first iteration: fold the Frobenius prescale into the epilogue
   bool symmetric;
-  bool a_sym;    // A operand is a symmetric product stored as its upper 256 x 256 blocks (polynomial, update)
-  bool b_sym;    // the K-major B operand likewise (polynomial)
-  bool b_mn;     // B operand is the MN-major X (update products)
+  bool a_sym;    // A operand is a symmetric product stored as its upper 256 x 256 blocks
+  bool b_sym;    // the K-major B operand likewise
+  bool b_mn;     // B operand is the MN-major X (update-like products)
   bool zero;     // the matrix's momentum is exactly zero: no products
+  bool null;     // a Gram-space product that does not exist (Q in iteration 0, C in the last): skipped
+  bool last;     // the matrix's last product: nothing waits for it
   int m0, n0;    // origin of the pair's 256-row output tile
   int mc;        // this CTA's 128 rows: [mc, mc + 128)
   int N;         // tile width (256, or 128 for the last column tile)
@@ -267,46 +269,111 @@ struct Tile {
   int32_t need;  // completions of this matrix's earlier products (this launch) to wait for
   const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
   const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
-  const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly, X for the update)
+  const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly / kPolyI, X for the update)
   void* out;             // blocked bf16 output, or the caller's buffer (final update)
 };
 
+// Tiles of a matrix's products [0, ph) that publish a completion: whole
+// iterations, then the products of the current one before it, less (Gram-space)
+// the null tiles among them.
+__device__ __forceinline__ int tiles_before(const NsBatch& p, const NsMat& d, int ph) {
+  if (!d.gram_space) {
+    const int per_iter = 2 * d.tiles_sym + d.tiles_m * d.tiles_n;
+    return (ph / 3) * per_iter + (ph % 3) * d.tiles_sym;
+  }
+  const int sym = d.tiles_sym;
+  int n = (ph / 3) * 4 * sym + (ph % 3 >= 1 ? sym : 0) + (ph % 3 >= 2 ? sym : 0);
+  if (ph > 2) n -= sym;                        // Q of iteration 0
+  if (ph > 3 * p.ns_steps - 1) n -= sym;       // C of the last iteration
+  return n;
+}
+
 // Tile t of the sequence's list.  Symmetric products: 256 x 256 tiles on or
-// above the diagonal, row pair-block I holding tiles I .. nb2-1; update: 256-row
-// tiles, rows fastest (neighbours share B-operand columns).
+// above the diagonal, row pair-block I holding tiles I .. nb2-1; update-like
+// products: 256-row tiles, rows fastest (neighbours share B-operand columns).
 __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t rank) {
   Tile r;
-  const int it = t / p.iter_tiles;
-  int rem = t - it * p.iter_tiles;
-  const int prod = rem >= p.mode_start[2] ? 2 : (rem >= p.mode_start[1] ? 1 : 0);
-  rem -= p.mode_start[prod];
+  int it, prod, rem;
+  if (t < p.final_start) {
+    it = t / p.iter_tiles;
+    rem = t - it * p.iter_tiles;
+    prod = rem >= p.mode_start[2] ? 2 : (rem >= p.mode_start[1] ? 1 : 0);
+    rem -= p.mode_start[prod];
+  } else {
+    it = p.ns_steps;
+    prod = 3;
+    rem = t - p.final_start;
+  }
   const int k = find_mat(p.tile_start[prod], p.n, rem);
   r.mi = p.order[prod][k];
-  const int local = rem - p.tile_start[prod][k];
+  int local = rem - p.tile_start[prod][k];
   const NsMat& d = p.mat[r.mi];
-  const bool last = it == p.ns_steps - 1;
-  r.phase = 3 * it + prod;
-  r.first = it == 0;
-  uint8_t* xc = d.x[it & 1];
-  if (prod == kGram) {
-    r.mode = kGram;
-    r.a_op = xc; r.b_op = xc; r.c_in = nullptr; r.out = d.a;
-    r.k_blocks = d.l_pad / kBlockK;
-  } else if (prod == kPoly) {
-    r.mode = kPoly;
-    r.a_op = d.a; r.b_op = d.a; r.c_in = d.a; r.out = d.b;
-    r.k_blocks = d.s_pad / kBlockK;
+  const bool last_it = it == p.ns_steps - 1;
+  r.phase = prod == 3 ? 3 * p.ns_steps : 3 * it + prod;
+  r.first = false;
+  r.null = false;
+  r.symmetric = true;
+  r.a_sym = r.b_sym = r.b_mn = false;
+  r.c_in = nullptr;
+  r.k_blocks = d.s_pad / kBlockK;
+  if (!d.gram_space) {
+    uint8_t* xc = d.x[it & 1];
+    r.first = it == 0;
+    r.last = prod == kUpdate && last_it;
+    if (prod == kGram) {
+      r.mode = kGram;
+      r.a_op = xc; r.b_op = xc; r.out = d.a;
+      r.k_blocks = d.l_pad / kBlockK;
+    } else if (prod == kPoly) {
+      r.mode = kPoly;
+      r.a_op = d.a; r.b_op = d.a; r.c_in = d.a; r.out = d.b;
+      r.a_sym = r.b_sym = true;
+    } else {
+      r.mode = last_it ? kUpdateFinal : kUpdate;
+      r.a_op = d.b; r.b_op = xc; r.c_in = xc;
+      r.out = last_it ? d.out : static_cast<void*>(d.x[(it + 1) & 1]);
+      r.symmetric = false;
+      r.a_sym = r.b_mn = true;
+    }
   } else {
-    r.mode = last ? kUpdateFinal : kUpdate;
-    r.a_op = d.b; r.b_op = xc; r.c_in = xc;
-    r.out = last ? d.out : static_cast<void*>(d.x[(it + 1) & 1]);
-    r.k_blocks = d.s_pad / kBlockK;
+    // Gram-space: P_0 is kept in q[0] (it is Q_0), P_k (k >= 1) in b.
+    uint8_t* const p_it = it == 0 ? d.q[0] : d.b;
+    r.last = prod == 3;
+    if (prod == 0) {
+      r.mode = kGram;
+      if (it == 0) {                                   // A_0 = X0 X0^T (prescaled)
+        r.first = true;
+        r.a_op = d.x[0]; r.b_op = d.x[0];
+        r.k_blocks = d.l_pad / kBlockK;
+      } else {                                         // A_it = C_{it-1} P_{it-1}
+        r.a_op = d.c; r.b_op = it == 1 ? d.q[0] : d.b;
+        r.a_sym = r.b_sym = true;
+      }
+      r.out = d.a;
+    } else if (prod == 1) {                            // P_it = a I + b A + c A A
+      r.mode = kPolyI;
+      r.a_op = d.a; r.b_op = d.a; r.c_in = d.a; r.out = p_it;
+      r.a_sym = r.b_sym = true;
+    } else if (prod == 2) {
+      r.mode = kGram;
+      r.a_sym = r.b_sym = true;
+      if (local < d.tiles_sym) {                       // C_it = P_it A_it
+        r.a_op = p_it; r.b_op = d.a; r.out = d.c;
+        r.null = last_it;
+      } else {                                         // Q_it = P_it Q_{it-1}
+        local -= d.tiles_sym;
+        r.a_op = p_it; r.b_op = d.q[(it - 1) & 1]; r.out = d.q[it & 1];
+        r.null = it == 0;
+      }
+    } else {                                           // X = Q_{T-1} X0, prescaled
+      r.mode = kFinalQ;
+      r.a_op = d.q[(p.ns_steps - 1) & 1]; r.b_op = d.x[0]; r.out = d.out;
+      r.symmetric = false;
+      r.a_sym = r.b_mn = true;
+    }
   }
-  r.symmetric = prod != kUpdate;
-  r.a_sym = prod != kGram;
-  r.b_sym = prod == kPoly;
-  r.b_mn = prod == kUpdate;
-  const int width = (p.narrow_mask >> prod) & 1 ? kBlockN / 2 : kBlockN;    // tile columns
+  // tile columns: 128 in a narrow launch for a product class with few tiles
+  const int width = (p.narrow_mask >> (r.symmetric ? kGram : kUpdate)) & 1 ? kBlockN / 2 : kBlockN;
   if (r.symmetric) {
     // Row pair-block I holds the tiles of columns 256 I .. s_pad - 1: nb2 - I
     // of them, or twice that for narrow tiles.
@@ -327,12 +394,7 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
   }
   r.mc = r.m0 + (int)rank * kBlockM;
   r.zero = p.norm[d.norm_idx].x == 0.0f;
-  // Tiles of this matrix in products [0, ph): whole iterations, then the Gram
-  // (and polynomial) products of the current one.
-  const int per_iter = 2 * d.tiles_sym + d.tiles_m * d.tiles_n;
-  const int done_here = (r.phase / 3) * per_iter + (r.phase % 3) * d.tiles_sym;
-  const int done_before = (p.phase_begin / 3) * per_iter + (p.phase_begin % 3) * d.tiles_sym;
-  r.need = kArrivalsPerTile * (done_here - done_before);
+  r.need = kArrivalsPerTile * (tiles_before(p, d, r.phase) - tiles_before(p, d, p.phase_begin));
   return r;
 }
 
@@ -348,14 +410,26 @@ __device__ __forceinline__ const uint8_t* b_half_kmajor(const Tile& tl, int kb, 
 __device__ __forceinline__ const uint8_t* b_block_mn(const Tile& tl, int kb, size_t kstride, int j) {
   return tl.b_op + (size_t)((tl.n0 >> 6) + j) * kstride + (size_t)kb * 8 * 1024;
 }
-// A and B are stored as their 128 x 128 blocks (r, c) with c/2 >= r/2 only
-// (on or above the diagonal of 256 x 256 blocks).  Stage kb (K columns
-// [128 kb, 128 kb + 128)) of an operand whose 256-row block lies below K's
-// 256-block is read from the stored block across the diagonal, as the
-// MN-major image of the transpose (the matrix is symmetric): both CTAs of the
-// pair decide alike, since their rows share one 256-row block.
+// The symmetric products are stored as their 128 x 128 blocks (r, c) with
+// c/2 >= r/2 only (on or above the diagonal of 256 x 256 blocks); a block
+// below it stands for the transpose of its mirror image, while a diagonal
+// 256 x 256 block is stored whole, as computed.  A product of two such
+// matrices Y Z takes row m of Y and column n of Z for each stage kb (K columns
+// [128 kb, 128 kb + 128)):
+//   A operand (rows of Y): the stored rows where K's 256-block is on or right
+//     of the rows' one, else the MN-major image of the stored block across
+//     the diagonal;
+//   B operand (columns of Z, as rows of its transpose): the MN-major image of
+//     the stored block where K's 256-block is on or above the columns' one,
+//     else the stored rows of the block across the diagonal.
+// (For an exactly symmetric Z -- the standard form's A -- both images of the
+// diagonal block hold the same values.  The Gram-space form's products P A,
+// C P and P Q are symmetric only up to rounding, and reading the diagonal
+// blocks as columns makes each one the true product of the stored matrices,
+// as its polynomial needs.)  Both CTAs of the pair decide alike, since their
+// rows, and their halves of the tile's columns, share one 256-block.
 __device__ __forceinline__ bool a_trans(const Tile& tl, int kb) { return tl.a_sym && (kb >> 1) < (tl.m0 >> 8); }
-__device__ __forceinline__ bool b_trans(const Tile& tl, int kb) { return tl.b_sym && (kb >> 1) < (tl.n0 >> 8); }
+__device__ __forceinline__ bool b_trans(const Tile& tl, int kb) { return tl.b_sym && (kb >> 1) <= (tl.n0 >> 8); }
 // Transposed A: 64-column block mc/64 + j of the stored matrix, rows
 // [128 kb, 128 kb + 128): one 16 KB run.
 __device__ __forceinline__ const uint8_t* a_block_t(const Tile& tl, int kb, size_t kstride, int j) {
@@ -604,7 +678,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         }
         ptx::mbar_arrive(ptx::smem_u32(&dep_bar[seq % kTileRing]));   // releases the acquire (CTA scope)
         ++seq;
-        if (tl.zero) continue;
+        if (tl.zero || tl.null) continue;
         // The operands were stored by other CTAs (generic proxy); the tensor
         // copies read them through the async proxy.
         if (tl.need > 0) ptx::fence_proxy_async_global();
@@ -680,7 +754,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         local_release(ring, seq);
         ++seq;
         if (!ok) break;
-        if (tl.zero) continue;
+        if (tl.zero || tl.null) continue;
         const uint32_t a = acc_it & 1, ause = acc_it >> 1;
         // both CTAs' epilogues have drained accumulator a
         ok = wait_cluster_or_abort(ptx::smem_u32(&tempty_bar[a]), (ause & 1) ^ 1, ab,
@@ -764,8 +838,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const int m = tl.mc + rrow;                        // its output row
       const int cw = tl.N >> 1;                          // columns of this half (128, or 64)
       const int c0 = half * cw;
-      if (tl.zero) {
-        if (tl.mode == kUpdateFinal) {
+      if (tl.zero || tl.null) {
+        if (tl.zero && (tl.mode == kUpdateFinal || tl.mode == kFinalQ)) {
           float z[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = 0.f;
@@ -774,8 +848,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         continue;
       }
       const size_t stride = colblock_stride(d.s_pad);
-      const bool has_c = (tl.mode != kGram);
-      const bool final_out = (tl.mode == kUpdateFinal);
+      const bool has_c = tl.c_in != nullptr;
+      const bool final_out = tl.mode == kUpdateFinal || tl.mode == kFinalQ;
       const int nblk = cw >> 6;                          // 64-column blocks of this half
       const size_t run_off = (size_t)(tl.mc >> 3) * 1024;   // the CTA's rows in a column block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
@@ -790,7 +864,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       ptx::tc_fence_after();
       const float2 nrm = p.norm[d.norm_idx];
       const float scale_gram = tl.first ? nrm.y * nrm.y : 1.0f;
-      const float scale_upd = tl.first ? nrm.y : 1.0f;
+      const float scale_upd = (tl.first || tl.mode == kFinalQ) ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
       const int32_t code = wait_code(tl.phase, kRoleAccFull);
       for (int blk = 0; blk < nblk && live; ++blk) {
@@ -821,15 +895,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (tl.mode == kGram) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
+          } else if (tl.mode == kFinalQ) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_upd;
           } else {
             uint4 xin[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
             float x[32];
             unpack_bf16x32(xin, x);
-            if (tl.mode == kPoly) {
+            if (tl.mode == kPoly || tl.mode == kPolyI) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
+              if (tl.mode == kPolyI) {
+                // a I: the diagonal element of this row, if among these columns
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (nb + cb + j == m) v[j] += p.a;
+              }
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
@@ -849,7 +932,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       }
       if (!live) break;
       ++acc_it;
-      if (tl.phase + 1 < p.phase_end) {
+      if (!tl.last) {
         // Publish this warp's share of the tile: every lane's stores are
         // ordered before the tensor copies that later tiles issue after
         // reading the counter (proxy fence), and before lane 0's release add
@@ -884,7 +967,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           if (t < p.tile_end) {
             const Tile tl = decode_tile(p, t, 0);
             const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
-            ready = tl.zero || need <= 0 || ptx::ld_acquire_gpu(p.done + tl.mi) >= need;
+            ready = tl.zero || tl.null || need <= 0 || ptx::ld_acquire_gpu(p.done + tl.mi) >= need;
           }
           const int32_t v = ready ? t : (t | kPollBit);
           if (!local_publish(ring, seq, v, ab) || !pair_publish(pair, seq, v, ab)) break;

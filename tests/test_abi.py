@@ -85,19 +85,44 @@ def test_planner_errors(mfsdp):
     assert plan.matrix_shards == [] and plan.rank_matrix_elems == [0, 0, 0]
 
 
+def gram_shape(s, l):
+    """Shapes that may run the Gram-space form (include/mfsdp.h)."""
+    return s >= 128 and l >= 2 * s and l >= s + 384
+
+
 def test_workspace_layout(mfsdp):
-    shards = [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131072, 300, 130), mfsdp.make_shard(200000, 1, 9)]
+    shards = [mfsdp.make_shard(0, 256, 512), mfsdp.make_shard(131072, 300, 130), mfsdp.make_shard(200000, 1, 9),
+              mfsdp.make_shard(200064, 200, 640)]
     lay = mfsdp.muon_workspace_layout(shards)
     total = mfsdp.muon_workspace_bytes(shards)
-    assert [l[4:] for l in lay] == [(256, 512, 256, 512), (256, 384, 130, 300), (256, 128, 1, 9)]
+    assert [l[4:] for l in lay] == [(256, 512, 256, 512), (256, 384, 130, 300), (256, 128, 1, 9),
+                                    (256, 640, 200, 640)]
     end = 0
-    for x0, x1, a, b, sp, lp, _, _ in lay:
+    for x0, x1, a, b, sp, lp, s_, l_ in lay:
         assert x0 % 1024 == 0 and x0 >= end
-        assert x1 == x0 + sp * lp * 2 and a == x1 + sp * lp * 2 and b == a + sp * sp * 2
+        # the second X region also holds C and both Q of the Gram-space form
+        # for shapes that may run it
+        x1_bytes = max(sp * lp, 3 * sp * sp) * 2 if gram_shape(s_, l_) else sp * lp * 2
+        assert x1 == x0 + sp * lp * 2 and a == x1 + x1_bytes and b == a + sp * sp * 2
         end = b + sp * sp * 2
     assert total == end
     assert mfsdp.muon_workspace_bytes([mfsdp.make_shard(0, 0, 5)]) == 0
     assert mfsdp.muon_workspace_bytes([mfsdp.make_shard(0, 40000, 40000)]) == 0
+    # the Gram-space form: 200 x 640 only (256 x 512 and 130 x 300: l < s +
+    # 384 with s < 384; 1 x 9: s < 128), for 1 .. 5 steps; C and the Q
+    # ping-pong follow each other in X1's region
+    for steps, want in [(0, [0, 0, 0, 0]), (1, [0, 0, 0, 1]), (5, [0, 0, 0, 1]), (6, [0, 0, 0, 0])]:
+        gl = mfsdp.muon_gram_space_layout(shards, steps)
+        assert [g[0] for g in gl] == want
+        for (flag, c, q0, q1), (x0, x1, a, b, sp, lp, _, _) in zip(gl, lay):
+            assert c == x1 and q0 == c + sp * sp * 2 and q1 == q0 + sp * sp * 2
+    dense, executed = mfsdp.muon_step_flops(shards[3:], 5)
+    # 200 x 640 in Gram space (padded to 256 x 640): A_0 (K = 640), 5 P, 4
+    # each of C, A, Q (K = 256) and the final Q X0, each a single 256 x 256
+    # tile but the last
+    tile = 2 * 256 * 256
+    assert executed == tile * 640 + (5 + 3 * 4) * tile * 256 + 2 * 256 * 256 * 640
+    assert dense == 5 * (4 * 200 * 200 * 640 + 2 * 200 ** 3)
 
 
 # ------------------------------------------------------------ error paths
@@ -214,14 +239,22 @@ def test_step_flops(mfsdp):
                      [(4096, 14336), (1024, 4096), (300, 130)])
     assert dense == want_dense
 
-    def ex(s, l):   # short side padded to 256, long to 128; upper-triangle 256x256 tiles when symmetric
+    def ex(s, l, steps=5):   # short side padded to 256, long to 128; upper-triangle 256x256 tiles when symmetric
         sp, lp = -(-s // 256) * 256, -(-l // 128) * 128
         nb2 = sp // 256
         tiles = nb2 * (nb2 + 1) // 2
-        return 5 * (tiles * 256 * 256 * 2 * lp + tiles * 256 * 256 * 2 * sp + 2 * sp * sp * lp)
+        gram, sym, upd = tiles * 256 * 256 * 2 * lp, tiles * 256 * 256 * 2 * sp, 2 * sp * sp * lp
+        if gram_shape(s, l) and 1 <= steps <= 5:
+            # Gram space: A_0, one P per step, C, A and Q for all but one, the final Q X0
+            return gram + steps * sym + 3 * (steps - 1) * sym + upd
+        return steps * (gram + sym + upd)
+    # the first two run the Gram-space form, 130 x 300 the direct one
     assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300)
     assert executed < dense     # the symmetric skipping outweighs the padding here
     assert mfsdp.muon_step_flops([], 5) == (0, 0)
+    # at 6 steps every shape takes the direct form
+    dense6, executed6 = mfsdp.muon_step_flops(shards, 6)
+    assert executed6 == sum(ex(s, l, 6) for s, l in [(4096, 14336), (1024, 4096), (130, 300)])
 
 
 def test_newton_schulz_index_limits(mfsdp):

@@ -151,37 +151,63 @@ def test_tiny_workload(mfsdp, ns_steps, upd_dtype):
 
 @pytest.mark.parametrize("ns_steps", [1, 2])
 def test_each_product_from_workspace(mfsdp, ns_steps):
-    """Isolates every kernel: the workspace keeps X0 = bf16(U), the last
-    iteration's A and B, and (for two steps) X1, so each product is checked
-    against fp64 arithmetic on the bf16 inputs it actually read.  ns_steps=1
-    covers the first-iteration prescale paths, ns_steps=2 the plain ones."""
+    """Isolates every kernel: the workspace keeps X0 = bf16(U) and the last
+    products, so each is checked against fp64 arithmetic on the bf16 inputs it
+    actually read.  ns_steps=1 covers the first-iteration prescale paths,
+    ns_steps=2 the plain ones.  The GPT-2 block has both forms of the
+    iteration: 768 x 768 runs the direct one (A, B and, for two steps, X1
+    kept), the three long matrices the Gram-space one (A, P, C and Q kept).
+    Symmetric products are read back as stored: their blocks on or above the
+    diagonal of 256 x 256 blocks, the others their mirror images' transposes,
+    and each product of two of them is the true product of those matrices."""
     w = W.get("gpt2_block")
     plan, r, shards, numel = owner_set(mfsdp, w)
     grad = H.build_grad_buffer(w, shards, numel)
     mom0 = np.zeros(numel, np.float32)
     upd, mom, ws = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32, ns_steps=ns_steps)
     wsb = ws.cpu().numpy()
-    for s, (x0, x1, a_off, b_off, sp, lp, sd, ld) in zip(shards, mfsdp.muon_workspace_layout(shards)):
+    programs = mfsdp.muon_gram_space_layout(shards, ns_steps)
+    assert sorted(g[0] for g in programs) == [0, 1, 1, 1]
+    for s, (x0, x1, a_off, b_off, sp, lp, sd, ld), (gram, c_off, q0_off, q1_off) in zip(
+            shards, mfsdp.muon_workspace_layout(shards), programs):
         G = grad_f64(grad, s)
         X = G.T if s.rows > s.cols else G
         Yw = H.unblock(wsb, x0, sp, lp).astype(np.float64)
         assert np.array_equal(Yw[:sd, :ld], X), "X0 is not bf16(U) (G is bf16 and M = G)"
         assert np.all(Yw[sd:, :] == 0) and np.all(Yw[:, ld:] == 0), "X0 padding not zero"
-        # A and B are kept as their blocks on or above the diagonal of
-        # 256 x 256 blocks
-        Aw = H.symmetric_from_upper(H.unblock(wsb, a_off, sp, sp)).astype(np.float64)[:sd, :sd]
-        Bw = H.symmetric_from_upper(H.unblock(wsb, b_off, sp, sp)).astype(np.float64)[:sd, :sd]
+
+        def sym(off):
+            return H.symmetric_from_upper(H.unblock(wsb, off, sp, sp)).astype(np.float64)[:sd, :sd]
         O = upd[s.offset:s.offset + s.rows * s.cols].reshape(s.rows, s.cols).astype(np.float64)
         O = O.T if s.rows > s.cols else O
+        inv = 1.0 / (np.sqrt(np.sum(X * X)) + W.NS_EPS)
+        I = np.eye(sd)
+        if not gram:
+            Aw, Bw = sym(a_off), sym(b_off)
+            if ns_steps == 1:
+                Xin, scale_a, scale_x = X, inv * inv, inv
+            else:
+                Xin = H.unblock(wsb, x1, sp, lp).astype(np.float64)[:sd, :ld]
+                scale_a = scale_x = 1.0
+            assert H.rel_fro(Aw, scale_a * (Xin @ Xin.T)) < 1e-2, "Gram product"
+            assert H.rel_fro(Bw, B * Aw + C * (Aw @ Aw)) < 1e-2, "polynomial product"
+            assert H.rel_fro(O, scale_x * (A * Xin + Bw @ Xin)) < 1e-2, "update product"
+            continue
+        # Gram space: P_0 = Q_0 in Q_even, P_k (k >= 1) in B; A holds A_{T-1}
+        A0 = inv * inv * (X @ X.T)
+        Aw = sym(a_off)
         if ns_steps == 1:
-            inv = 1.0 / (np.sqrt(np.sum(X * X)) + W.NS_EPS)
-            Xin, scale_a, scale_x = X, inv * inv, inv
+            assert H.rel_fro(Aw, A0) < 1e-2, "Gram product A_0"
+            P0 = sym(q0_off)
+            assert H.rel_fro(P0, A * I + B * Aw + C * (Aw @ Aw)) < 1e-2, "polynomial P_0"
+            assert H.rel_fro(O, inv * (P0 @ X)) < 1e-2, "final product Q_0 X0"
         else:
-            Xin = H.unblock(wsb, x1, sp, lp).astype(np.float64)[:sd, :ld]
-            scale_a = scale_x = 1.0
-        assert H.rel_fro(Aw, scale_a * (Xin @ Xin.T)) < 1e-2, "Gram product"
-        assert H.rel_fro(Bw, B * Aw + C * (Aw @ Aw)) < 1e-2, "polynomial product"
-        assert H.rel_fro(O, scale_x * (A * Xin + Bw @ Xin)) < 1e-2, "update product"
+            P0, C0, P1, Q1 = sym(q0_off), sym(c_off), sym(b_off), sym(q1_off)
+            assert H.rel_fro(C0, P0 @ A0) < 1e-2, "product C_0 = P_0 A_0"
+            assert H.rel_fro(Aw, C0 @ P0) < 1e-2, "product A_1 = C_0 P_0"
+            assert H.rel_fro(P1, A * I + B * Aw + C * (Aw @ Aw)) < 1e-2, "polynomial P_1"
+            assert H.rel_fro(Q1, P1 @ P0) < 1e-2, "product Q_1 = P_1 Q_0"
+            assert H.rel_fro(O, inv * (Q1 @ X)) < 1e-2, "final product Q_1 X0"
 
 
 @pytest.mark.parametrize("upd_dtype", ["f32", "bf16"])
