@@ -330,9 +330,12 @@ int mfsdp_muon_static_scratch_status(void* stream, int32_t* detail);
 /* FLOP counts of mfsdp_muon_owner_step for these shards, host only:
  * *dense = sum over matrices of ns_steps * (4 s^2 l + 2 s^3) (the algorithmic
  * count); *executed = the tensor-core FLOPs the kernels issue (dimensions
- * padded to multiples of 128; the symmetric Gram and polynomial products
- * computed on their upper-triangle 128 x 128 blocks only; matrices whose
- * momentum turns out to be zero, which skip all products, still counted).
+ * padded to multiples of 128, the short side to 256; the symmetric products
+ * computed on their 256 x 256 blocks on or above the diagonal only; a matrix
+ * that runs the Gram-space form counted with its own products: A_0, then per
+ * iteration P_k, C_k, A_{k+1} and Q_k where they exist, all symmetric, and
+ * the final Q X0; matrices whose momentum turns out to be zero, which skip
+ * all products, still counted).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
 int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, int32_t ns_steps,
                           uint64_t* dense, uint64_t* executed);
@@ -353,7 +356,8 @@ int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n_shards, in
  * matrix; 7 scheduler: a free slot of a tile ring; 8 any role: the next
  * tile), bits 8-31 the
  * Newton-Schulz product index (3 * iteration + 0 Gram / 1 polynomial /
- * 2 update) where the role knows it, else 0.  The status word is cleared by
+ * 2 update; in the Gram-space form 0 A_k, 1 P_k, 2 C_k and Q_k, and
+ * 3 * ns_steps the final Q X0) where the role knows it, else 0.  The status word is cleared by
  * every call that runs the momentum phase. */
 int mfsdp_muon_device_status(const void* workspace, void* stream, int32_t* detail);
 

@@ -20,8 +20,10 @@ NS_TOL_CLASS = ((1, 1, 0.024, 0.044), (2, 3, 0.226, 0.121), (4, 7, 0.226, 0.092)
                 (16, 31, 0.050, 0.038), (32, 63, 0.027, 0.039))
 # Full-size matrices, every 128 x 128 block of the stored update (ragged edge
 # blocks included): relative Frobenius error, and the largest elementwise
-# error over (block RMS + |reference element|); 1.5x the emulated maxima over
-# the workloads' shapes.
+# error over (block RMS + |reference element|); 1.5x the emulated maxima of
+# the standard program over the workloads' shapes (1.33 %, 0.060).  The
+# Gram-space program's maxima (1.11 %, 0.077 at 14336 x 4096 with Student-t
+# input) stay inside them.
 NS_BLOCK_REL = 2e-2
 NS_BLOCK_ELEM = 0.091
 ADAM_REL = 1e-5        # AdamW: fp32 arithmetic against fp64
