@@ -563,7 +563,7 @@ def run_ours(args):
     # overlapped with the compute of the neighbouring groups; the AdamW tail's
     # gradient comes in and its parameters go back out too.
     stream = step.stream
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, args.steps)           # the same K steps as the device-resident region
     e2e_groups = mfsdp.host_step_groups(shards, step.grad.dtype, step.upd.dtype, args.e2e_groups)[0]
     upd_host = torch.empty(numel, dtype=torch.bfloat16).pin_memory()
     tp_host = torch.empty_like(step.tg_host).pin_memory()
