@@ -10,8 +10,10 @@ phi(1/sqrt(s)) is taken from the oracle on the 2 x 2 matrix
 diag(1/sqrt(s), sqrt(1 - 1/s)), which has unit norm like the big input and the
 same first normalised singular value.  The big case still runs every tile of a
 32768-wide Gram, polynomial and update, the transposed reads of the symmetric
-products' blocks below the diagonal and (for the tall case) the transposed
-final stores.
+products' blocks below the diagonal and (for the tall cases) the transposed
+final stores.  65537 x 32768 (over 2^31 elements, long side at least twice the
+short one) runs the Gram-space form at the largest short side: every tile of
+its 32768-wide A, P, C and Q products and of the final Q X0.
 """
 import math
 
@@ -34,7 +36,7 @@ def phi_at(s: int) -> float:
     return float(newton_schulz_ref(D, 5, A, B, C, W.NS_EPS)[0, 0])
 
 
-@pytest.mark.parametrize("rows,cols", [(32768, 32768), (40001, 20483)])
+@pytest.mark.parametrize("rows,cols", [(32768, 32768), (40001, 20483), (65537, 32768)])
 def test_signed_permutation_at_max_short_side(mfsdp, rows, cols):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -57,6 +59,8 @@ def test_signed_permutation_at_max_short_side(mfsdp, rows, cols):
     mom = torch.zeros(numel, dtype=torch.float32, device=dev)
     upd = torch.full((numel,), float("nan"), dtype=torch.bfloat16, device=dev)
     shards = [mfsdp.make_shard(0, rows, cols)]
+    gram = mfsdp.muon_gram_space_layout(shards, 5)[0][0]
+    assert gram == (1 if max(rows, cols) >= 2 * s else 0), "program chosen for the shape"
     ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
     mfsdp.muon_owner_step(shards, grad, mom, upd, ws, beta=0.95, ns_steps=5, coeffs=W.NS_COEFFS, eps=W.NS_EPS)
     st, detail = mfsdp.muon_device_status(ws)
