@@ -53,6 +53,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # by a digest of the kernel's sources (ns_source_digest): a kernel changed
 # since its capture reports null traffic until it is captured again.
 NS_GEMM_TRAFFIC = {("0328eec573f11b13", "llama3_8b_rank"): 28.01e9, ("0328eec573f11b13", "llama_1p3b_rank"): 5.553e9}
+# Share of the same launch's elapsed cycles with the tensor pipe active
+# (sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed), keyed alike.
+NS_TENSOR_ACTIVE = {("0328eec573f11b13", "llama3_8b_rank"): 0.8724, ("0328eec573f11b13", "llama_1p3b_rank"): 0.7569}
 
 # The sources that make up the Newton-Schulz kernel.
 NS_SOURCES = ("ns_gemm.cu", "ptx.cuh", "mfsdp_internal.h")
@@ -723,6 +726,7 @@ def run_ours(args):
     peak_tf = peaks["bf16_tflops_sustained"]
     digest = ns_source_digest()
     traffic = NS_GEMM_TRAFFIC.get((digest, w.name))
+    tensor_active = NS_TENSOR_ACTIVE.get((digest, w.name))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -752,7 +756,7 @@ def run_ours(args):
         "phases": phases,
         "roofline": {"kernel": "ns_kernel", "bound": "tensor", "achieved": ns_tflops_exec,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ns_tflops_exec / peak_tf, 4),
-                     "traffic": traffic, "kernel_digest": digest,
+                     "traffic": traffic, "tensor_pipe_active_ncu": tensor_active, "kernel_digest": digest,
                      "peak_source": f"{peak_src} bf16_tflops_sustained",
                      "flops": ("executed tensor-core FLOPs (symmetric products: upper-triangle blocks only; "
                                "matrices with l >= 2s iterate on their s x s Gram matrix)"),
