@@ -422,9 +422,13 @@ class OwnerStep:
 
 
 def figures(mfsdp, step, ms, peaks):
-    """Algorithmic rates of one owner set's phases (ms: mean phase times)."""
+    """Algorithmic rates of one owner set's phases (ms: mean phase times).
+    Matrices whose gradient is all zero (the MoE set's unrouted experts) keep
+    a zero momentum and skip every Newton-Schulz product, so their FLOPs are
+    left out of both counts."""
     w, shards = step.w, step.shards
-    flops, flops_exec = mfsdp.muon_step_flops(shards, w.ns_steps) if shards else (0, 0)
+    active = [s for s in shards if s.param_id not in w.zero_params]
+    flops, flops_exec = mfsdp.muon_step_flops(active, w.ns_steps) if active else (0, 0)
     elems = sum(s.rows * s.cols for s in shards)
     gsz = 2 if w.grad_dtype == "bf16" else 4
     mom_bytes = elems * (gsz + 4 + 4 + 2)
