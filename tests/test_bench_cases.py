@@ -51,3 +51,20 @@ def test_kernel_digest_ignores_comments():
     changed = dict(srcs)
     changed["ptx.cuh"] = srcs["ptx.cuh"].replace("kSuspendHintNs = 32", "kSuspendHintNs = 64")
     assert changed["ptx.cuh"] != srcs["ptx.cuh"] and bench.ns_source_digest(changed) != base
+
+
+def test_figures_leave_zero_matrices_out(mfsdp):
+    """The MoE set's all-zero experts skip every Newton-Schulz product, so the
+    bench's FLOP counts are those of its nonzero matrices only: 29.22 TFLOP
+    dense over the 246 nonzero matrices of 272."""
+    import types
+    w = W.get("moe_skewed")
+    plan = mfsdp.plan_owners(w.param_table(), w.world, w.ns_steps, w.align_elems)
+    shards = plan.rank_matrices(bench.heaviest_rank(plan))
+    active = [s for s in shards if s.param_id not in w.zero_params]
+    assert (len(shards), len(active)) == (272, 246)
+    step = types.SimpleNamespace(w=w, shards=shards, tail_numel=0)
+    ms = {"ns": 1.0, "momentum": 1.0, "adamw": 0.0}
+    fig = bench.figures(mfsdp, step, ms, {"bf16_tflops_sustained": 1.0, "hbm_gbs": 1.0})
+    assert (fig["flops_dense"], fig["flops_executed"]) == mfsdp.muon_step_flops(active, w.ns_steps)
+    assert round(fig["flops_dense"] / 1e12, 2) == 29.22
