@@ -329,8 +329,9 @@ int mfsdp_muon_static_scratch_status(void* stream, int32_t* detail);
 
 /* FLOP counts of mfsdp_muon_owner_step for these shards, host only:
  * *dense = sum over matrices of ns_steps * (4 s^2 l + 2 s^3) (the algorithmic
- * count); *executed = the tensor-core FLOPs the kernels issue (dimensions
- * padded to multiples of 128, the short side to 256; the symmetric products
+ * count); *executed = the tensor-core FLOPs the kernels issue (outputs
+ * padded to multiples of 128, the short side to 256, and a contraction over
+ * the short side to s rounded up to 128; the symmetric products
  * computed on their 256 x 256 blocks on or above the diagonal only; a matrix
  * that runs the Gram-space form counted with its own products: A_0, then per
  * iteration P_k, C_k, A_{k+1} and Q_k where they exist, all symmetric, and

@@ -222,14 +222,17 @@ bool use_narrow_tiles(const Layout& L, int base, int cnt, int32_t* mask) {
   return true;
 }
 
-// Tensor-core FLOPs one product of one matrix executes (padded dimensions;
-// symmetric products: the 256 x 256 pair tiles on or above the diagonal).
-uint64_t executed_flops(int mode, int s_pad, int l_pad) {
+// Tensor-core FLOPs one product of one matrix executes: outputs padded to
+// 256 (short side) and 128 (long side), symmetric products on their 256 x 256
+// pair tiles on or above the diagonal; a contraction over the short side runs
+// to s rounded up to 128 (the K loop skips the all-zero padding beyond it).
+uint64_t executed_flops(int mode, int s, int s_pad, int l_pad) {
   const uint64_t nb2 = (uint64_t)s_pad / kPairM;
   const uint64_t tile = (uint64_t)kPairM * kPairM * 2;
+  const uint64_t k_s = (uint64_t)round_up((size_t)s, kBlockK);
   if (mode == kGram) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)l_pad;
-  if (mode == kPoly) return nb2 * (nb2 + 1) / 2 * tile * (uint64_t)s_pad;
-  return 2ull * s_pad * s_pad * (uint64_t)l_pad;
+  if (mode == kPoly) return nb2 * (nb2 + 1) / 2 * tile * k_s;
+  return 2ull * s_pad * (uint64_t)l_pad * k_s;
 }
 
 // The Newton-Schulz launch indexes its tiles and counts completions in int32:
@@ -301,7 +304,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.10.0"; }
+extern "C" const char* mfsdp_version(void) { return "0.10.1"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -935,8 +938,8 @@ extern "C" int mfsdp_muon_step_flops(const mfsdp_matrix_shard* shards, int32_t n
     const MatLayout& m = L.mats[i];
     const uint64_t s = (uint64_t)m.s, l = (uint64_t)m.l;
     dn += (uint64_t)ns_steps * (4 * s * s * l + 2 * s * s * s);
-    const uint64_t gram = executed_flops(kGram, m.s_pad, m.l_pad), sym = executed_flops(kPoly, m.s_pad, m.l_pad),
-                   upd = executed_flops(kUpdate, m.s_pad, m.l_pad);
+    const uint64_t gram = executed_flops(kGram, m.s, m.s_pad, m.l_pad), sym = executed_flops(kPoly, m.s, m.s_pad, m.l_pad),
+                   upd = executed_flops(kUpdate, m.s, m.s_pad, m.l_pad);
     if (use_gram_space(m, ns_steps))   // A_0, T P_k, T-1 each of C, A and Q, the final Q X0
       ex += gram + (uint64_t)ns_steps * sym + 3ull * (uint64_t)(ns_steps - 1) * sym + upd;
     else

@@ -315,7 +315,11 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
   r.symmetric = true;
   r.a_sym = r.b_sym = r.b_mn = false;
   r.c_in = nullptr;
-  r.k_blocks = d.s_pad / kBlockK;
+  // K = s: the operands' rows and columns past s hold zeros where they meet
+  // (the Gram-space P and Q carry a on their padded diagonal, which only ever
+  // multiplies zero rows into padded rows), so the K loop ends at the last
+  // 128-wide block that holds a real row.
+  r.k_blocks = (d.s + kBlockK - 1) / kBlockK;
   if (!d.gram_space) {
     uint8_t* xc = d.x[it & 1];
     r.first = it == 0;

@@ -233,28 +233,33 @@ def test_adamw_error_paths(mfsdp):
 
 
 def test_step_flops(mfsdp):
-    shards = [mfsdp.make_shard(0, 4096, 14336), mfsdp.make_shard(0, 1024, 4096), mfsdp.make_shard(0, 300, 130)]
+    shards = [mfsdp.make_shard(0, 4096, 14336), mfsdp.make_shard(0, 1024, 4096), mfsdp.make_shard(0, 300, 130),
+              mfsdp.make_shard(0, 1408, 2048)]
     dense, executed = mfsdp.muon_step_flops(shards, 5)
     want_dense = sum(5 * (4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3) for r, c in
-                     [(4096, 14336), (1024, 4096), (300, 130)])
+                     [(4096, 14336), (1024, 4096), (300, 130), (1408, 2048)])
     assert dense == want_dense
 
-    def ex(s, l, steps=5):   # short side padded to 256, long to 128; upper-triangle 256x256 tiles when symmetric
-        sp, lp = -(-s // 256) * 256, -(-l // 128) * 128
+    def ex(s, l, steps=5):   # outputs: short side padded to 256, long to 128; upper-triangle 256x256 tiles when
+        # symmetric; a contraction over the short side runs to s rounded up to 128
+        sp, lp, ks = -(-s // 256) * 256, -(-l // 128) * 128, -(-s // 128) * 128
         nb2 = sp // 256
         tiles = nb2 * (nb2 + 1) // 2
-        gram, sym, upd = tiles * 256 * 256 * 2 * lp, tiles * 256 * 256 * 2 * sp, 2 * sp * sp * lp
+        gram, sym, upd = tiles * 256 * 256 * 2 * lp, tiles * 256 * 256 * 2 * ks, 2 * sp * lp * ks
         if gram_shape(s, l) and 1 <= steps <= 5:
             # Gram space: A_0, one P per step, C, A and Q for all but one, the final Q X0
             return gram + steps * sym + 3 * (steps - 1) * sym + upd
         return steps * (gram + sym + upd)
-    # the first two run the Gram-space form, 130 x 300 the direct one
-    assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300)
+    # the first two run the Gram-space form, 130 x 300 and 1408 x 2048 the direct one
+    # (1408 x 2048: outputs 1536 rows, contractions over the short side K = 1408)
+    assert executed == ex(4096, 14336) + ex(1024, 4096) + ex(130, 300) + ex(1408, 2048)
+    sym_1408 = 21 * 256 * 256 * 2 * 1408
+    assert ex(1408, 2048) == 5 * (21 * 256 * 256 * 2 * 2048 + sym_1408 + 2 * 1536 * 2048 * 1408)
     assert executed < dense     # the symmetric skipping outweighs the padding here
     assert mfsdp.muon_step_flops([], 5) == (0, 0)
     # at 6 steps every shape takes the direct form
     dense6, executed6 = mfsdp.muon_step_flops(shards, 6)
-    assert executed6 == sum(ex(s, l, 6) for s, l in [(4096, 14336), (1024, 4096), (130, 300)])
+    assert executed6 == sum(ex(s, l, 6) for s, l in [(4096, 14336), (1024, 4096), (130, 300), (1408, 2048)])
 
 
 def test_newton_schulz_index_limits(mfsdp):
