@@ -22,6 +22,17 @@
 // where the chain of dependent products sets the time; each output element
 // sums the same products in the same order at either width.
 //
+// A matrix with l >= 2s runs the same iteration in Gram space instead: with
+// P_k = a I + b A_k + c A_k A_k, X_{k+1} = P_k X_k, so it iterates the s x s
+// matrices A_{k+1} = (P_k A_k) P_k and Q_k = P_k Q_{k-1} and multiplies X_0 by
+// Q_{T-1} once at the end.  All of them are polynomials in A_0, so every one
+// of these products is symmetric and stored like A; the long K = l appears
+// only in A_0 = X_0 X_0^T and the final Q X_0.  Products that read a diagonal
+// 256 x 256 block as their B operand read it as columns, so that a block that
+// is symmetric only up to rounding still gives the true product.  A
+// contraction over the short side stops at s rounded up to 128: beyond it the
+// operands' padding is zero where it meets.
+//
 // Operands live in the workspace in a blocked layout whose every 1 KB atom
 // (8 rows x 64 bf16 columns) is already in the UMMA 128-byte-swizzle order, with
 // atoms of one 64-column block contiguous.  So a CTA's share of a pipeline
@@ -88,8 +99,9 @@
 // frees TMEM and returns.
 //
 // Bounds of every tensor copy (the long side is padded to a multiple of 128
-// and the short side to a multiple of 256, so K is a multiple of 128 and a
-// stage covers column blocks 2kb and 2kb+1): a CTA's A rows in column block c
+// and the short side to a multiple of 256; K, l_pad or s rounded up to 128,
+// is a multiple of 128 and at most the operand's padded width, and a stage
+// covers column blocks 2kb and 2kb+1): a CTA's A rows in column block c
 // start at c*s_pad*128 + (mc/8)*1024 and span 16 KB, ending at most at
 // (K/64-1)*s_pad*128 + (s_pad-128)*128 + 16384 = K*s_pad*2, the end of the
 // operand; its K-major B half likewise ends at most at (K/64-1)*s_pad*128 +
