@@ -278,12 +278,14 @@ struct Tile {
   int mc;        // this CTA's 128 rows: [mc, mc + 128)
   int N;         // tile width (256, or 128 for the last column tile)
   int k_blocks;  // K / kBlockK
+  int s_pad;     // the matrix's padded short side: rows of every operand's column block
   int32_t need;  // completions of this matrix's earlier products (this launch) to wait for
   const uint8_t* a_op;   // blocked bf16 source of UMMA operand A (rows m)
   const uint8_t* b_op;   // blocked bf16 source of UMMA operand B
   const uint8_t* c_in;   // blocked bf16 epilogue input (A for kPoly / kPolyI, X for the update)
   void* out;             // blocked bf16 output, or the caller's buffer (final update)
 };
+static_assert(sizeof(Tile) % 8 == 0 && alignof(Tile) == 8, "tiles cross the pair as 8-byte words");
 
 // Tiles of a matrix's products [0, ph) that publish a completion: whole
 // iterations, then the products of the current one before it, less (Gram-space)
@@ -409,6 +411,7 @@ __device__ __forceinline__ Tile decode_tile(const NsBatch& p, int t, uint32_t ra
     r.N = (nt == d.tiles_n - 1) ? d.n_last : width;
   }
   r.mc = r.m0 + (int)rank * kBlockM;
+  r.s_pad = d.s_pad;
   r.zero = p.norm[d.norm_idx].x == 0.0f;
   r.need = kArrivalsPerTile * (tiles_before(p, d, r.phase) - tiles_before(p, d, p.phase_begin));
   return r;
@@ -546,12 +549,19 @@ struct Ring {
   uint32_t empty0;   // empty[0], in the writer's CTA
 };
 
-// CTA-local ring: the scheduler stores tile t into slot seq for this CTA's roles.
-__device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab) {
+// CTA-local ring: the scheduler stores tile t into slot seq for this CTA's
+// roles, with the tile decoded for this CTA (`tiles`, the ring's slots of
+// decoded tiles; unused for the end marker).  Decoding reads the launch's
+// tables from the kernel parameters at scattered offsets (~1800 cycles); the
+// scheduler, which runs ahead of the roles, does it once per CTA, and the
+// roles copy the result from shared memory.
+__device__ __forceinline__ bool local_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab,
+                                              Tile* tiles, const Tile* tl) {
   const uint32_t k = seq % kTileRing, use = seq / kTileRing;
   if (!wait_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, ab, wait_code(0, kRoleTileFree))) return false;
+  if (tl) tiles[k] = *tl;
   asm volatile("st.shared.s32 [%0], %1;" ::"r"(r.slot0 + 4u * k), "r"(t) : "memory");
-  ptx::mbar_arrive(r.full0 + 8u * k);   // releases the store (CTA scope)
+  ptx::mbar_arrive(r.full0 + 8u * k);   // releases the stores (CTA scope)
   return true;
 }
 
@@ -577,18 +587,30 @@ __device__ __forceinline__ bool local_take(const Ring& r, uint32_t seq, int32_t&
   local_release(r, seq);
   return true;
 }
+// The decoded tile of sequence number seq (read between peek and release).
+__device__ __forceinline__ Tile ring_tile(const Tile* tiles, uint32_t seq) { return tiles[seq % kTileRing]; }
 
-// Pair ring, even CTA's scheduler side: stores tile t into the odd CTA's slot seq.
-__device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab) {
+// Pair ring, even CTA's scheduler side: stores tile t into the odd CTA's slot
+// seq, with the tile decoded for the odd CTA (tl; null for the end marker)
+// into the odd CTA's copy of `tiles` (shared address of slot 0 in this CTA).
+__device__ __forceinline__ bool pair_publish(const Ring& r, uint32_t seq, int32_t t, const Abort& ab,
+                                             uint32_t tiles, const Tile* tl) {
   const uint32_t k = seq % kPairRing, use = seq / kPairRing;
   if (!wait_cluster_or_abort(r.empty0 + 8u * k, (use & 1) ^ 1, ab, wait_code(0, kRoleTileFree)))
     return false;
+  if (tl) {
+    const uint32_t dst = ptx::mapa_shared(tiles + (uint32_t)sizeof(Tile) * k, 1);
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(tl);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(Tile) / 8); ++i) ptx::st_shared_cluster_u64(dst + 8u * i, w[i]);
+  }
   ptx::st_shared_cluster_s32(ptx::mapa_shared(r.slot0 + 4u * k, 1), t);
-  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.full0 + 8u * k, 1));   // releases the store (cluster scope)
+  ptx::mbar_arrive_cluster(ptx::mapa_shared(r.full0 + 8u * k, 1));   // releases the stores (cluster scope)
   return true;
 }
 
-// Pair ring, odd CTA's scheduler side: takes the tile of sequence number seq.
+// Pair ring, odd CTA's scheduler side: takes the tile of sequence number seq
+// (its decoded form is then in slot seq % kPairRing of the pair's tiles).
 __device__ __forceinline__ bool pair_take(const Ring& r, uint32_t seq, int32_t& t, const Abort& ab) {
   const uint32_t k = seq % kPairRing, use = seq / kPairRing;
   if (!wait_cluster_or_abort(r.full0 + 8u * k, use & 1, ab, wait_code(0, kRoleTileFull))) return false;
@@ -614,10 +636,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
   __shared__ __align__(8) uint64_t ring_full[kTileRing];
   __shared__ __align__(8) uint64_t ring_empty[kTileRing];
   __shared__ int32_t ring_slot[kTileRing];
+  __shared__ Tile ring_tiles[kTileRing];                    // the ring's tiles, decoded for this CTA
   __shared__ __align__(8) uint64_t dep_bar[kTileRing];     // tile seq's earlier products are stored (producer)
   __shared__ __align__(8) uint64_t pair_full[kPairRing];    // used in the odd CTA
   __shared__ __align__(8) uint64_t pair_empty[kPairRing];   // used in the even CTA
   __shared__ int32_t pair_slot[kPairRing];                  // used in the odd CTA
+  __shared__ Tile pair_tiles[kPairRing];                    // used in the odd CTA: its decoded tiles
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -678,9 +702,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       while (ok) {
         int32_t t;
         bool poll = false;
-        ok = local_take(ring, seq, t, ab, &poll);
+        ok = local_peek(ring, seq, t, ab, &poll);
         if (!ok || t >= p.tile_end) break;
-        const Tile tl = decode_tile(p, t, rank);
+        const Tile tl = ring_tile(ring_tiles, seq);
+        local_release(ring, seq);
         // A tile whose earlier products were not all stored when the
         // scheduler took it: both producers of the pair wait (acquire) until
         // they are, so neither CTA's copies wait for a hand-over after the
@@ -698,7 +723,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         // The operands were stored by other CTAs (generic proxy); the tensor
         // copies read them through the async proxy.
         if (tl.need > 0) ptx::fence_proxy_async_global();
-        const size_t kstride = colblock_stride(p.mat[tl.mi].s_pad);   // every operand has s_pad rows per column block
+        const size_t kstride = colblock_stride(tl.s_pad);   // every operand has s_pad rows per column block
         const int nh = tl.N >> 1;                                      // this CTA's columns of B
         const uint32_t pair_bytes = 2u * (uint32_t)(kStageBytesA + nh * kBlockK * 2);
         for (int kb = 0; kb < tl.k_blocks; ++kb, ++it) {
@@ -761,7 +786,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
         }
         ok = local_peek(ring, seq, t, ab);
         if (!ok || t >= p.tile_end) break;
-        const Tile tl = decode_tile(p, t, rank);
+        const Tile tl = ring_tile(ring_tiles, seq);
         // Its operands can only land after the producer's dependency wait;
         // waiting for that first makes a dependency that is never met show up
         // as one (the slot is given back after it, as in the epilogue).
@@ -837,7 +862,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       if (lane == 0) got_tile = local_peek(ring, seq, t, ab);
       t = __shfl_sync(0xffffffffu, t, 0);
       if (!__shfl_sync(0xffffffffu, got_tile, 0) || t >= p.tile_end) break;
-      const Tile tl = decode_tile(p, t, rank);
+      const Tile tl = ring_tile(ring_tiles, seq);
+      __syncwarp();   // every lane has its copy before lane 0 gives the slot back
       // The tile's earlier products are stored (this CTA's producer has seen
       // them, dep_bar) before its epilogue input is read; the ring slot is
       // given back only after this wait, so dep_bar's phases cannot run ahead
@@ -980,13 +1006,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
           t = p.tile_begin + atomicAdd(p.next_tile, 1);
           if (t > p.tile_end) t = p.tile_end;           // the end marker
           bool ready = true;
+          Tile tl{}, tl_odd{};
           if (t < p.tile_end) {
-            const Tile tl = decode_tile(p, t, 0);
+            tl = decode_tile(p, t, 0);
+            tl_odd = tl;
+            tl_odd.mc += kBlockM;                          // the odd CTA's rows (all that differs)
             const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;   // the test hook: a count never reached
             ready = tl.zero || tl.null || need <= 0 || ptx::ld_acquire_gpu(p.done + tl.mi) >= need;
           }
           const int32_t v = ready ? t : (t | kPollBit);
-          if (!local_publish(ring, seq, v, ab) || !pair_publish(pair, seq, v, ab)) break;
+          const bool last = t >= p.tile_end;
+          if (!local_publish(ring, seq, v, ab, ring_tiles, last ? nullptr : &tl) ||
+              !pair_publish(pair, seq, v, ab, ptx::smem_u32(&pair_tiles[0]), last ? nullptr : &tl_odd))
+            break;
           // A pair takes its next tile only once this one may start.  In a
           // launch with many tiles the scheduler watches the counter itself
           // and moves on as soon as the tile is ready, so the few tiles it has
@@ -1001,13 +1033,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
                                  wait_code(0, kRoleDependency)))
                 break;
             } else if (!ready) {
-              const Tile tl = decode_tile(p, t, 0);
               const int32_t need = t == p.stall_tile ? INT32_MAX : tl.need;
               if (!wait_done(p.done + tl.mi, need, ab, wait_code(tl.phase, kRoleDependency))) break;
             }
           }
         } else {
-          if (!pair_take(pair, seq, t, ab) || !local_publish(ring, seq, t, ab)) break;
+          if (!pair_take(pair, seq, t, ab)) break;
+          const bool last = (t & ~kPollBit) >= p.tile_end;
+          if (!local_publish(ring, seq, t, ab, ring_tiles, last ? nullptr : &pair_tiles[seq % kPairRing])) break;
           pair_free(pair, seq);
           t &= ~kPollBit;
         }
