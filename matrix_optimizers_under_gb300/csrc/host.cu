@@ -304,7 +304,7 @@ extern "C" const char* mfsdp_status_string(int status) {
   }
 }
 
-extern "C" const char* mfsdp_version(void) { return "0.10.2"; }
+extern "C" const char* mfsdp_version(void) { return "0.10.3"; }
 
 extern "C" size_t mfsdp_muon_workspace_bytes(const mfsdp_matrix_shard* shards, int32_t n_shards) {
   Layout L;
@@ -880,7 +880,7 @@ int launch_ns_phase(const mfsdp_matrix_shard* shards, int n_shards, const Layout
       d.n_last = tu.n_last;
       d.norm_idx = i;
       d.transposed = m.transposed;
-      d.vec_ok = (shards[i].offset % 8 == 0) && (m.l % 8 == 0);
+      d.vec_ok = (shards[i].offset % 8 == 0) && ((m.transposed ? m.s : m.l) % 8 == 0);
     }
     // Inside each product, longest K first: the persistent pairs take tiles
     // round-robin, so the last rounds hold the cheapest tiles.  Products 0-2

@@ -113,7 +113,7 @@ struct NsMat {
   int32_t n_last;        // update: width of the last column tile
   int32_t norm_idx;      // index into the norm table
   int32_t transposed;    // final update: stored matrix is l x s
-  int32_t vec_ok;        // final update: row-major stores may use 16-byte vectors
+  int32_t vec_ok;        // final update: stored rows start 16-byte aligned (offset and row length multiples of 8)
   float lr_scale;        // apply: lr * shape scale of this matrix
 };
 

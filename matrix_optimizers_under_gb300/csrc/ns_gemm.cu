@@ -225,6 +225,43 @@ __device__ __forceinline__ void final_elem(const NsMat& d, const NsBatch& p, int
   }
 }
 
+// The Gram-space final product of a tall matrix (stored l x s, X = its
+// transpose) writes through the epilogue half's stage: each of the half's 128
+// threads holds X row m = mc + r for 32 consecutive X columns [n, n + 32),
+// i.e. one element of 32 consecutive stored rows, so the chunk is put into
+// the stage transposed (stored row j, then the 128 stored columns mc ..
+// mc + 127), and after the half's meeting copied out with 16-byte stores
+// along the stored rows -- instead of a 2-byte store per element, 64 bytes
+// per warp access.  Needs the stored rows to start 16-byte aligned
+// (vec_ok: offset and s multiples of 8); the stage's bytes per element are
+// those of the output (a 32 x 128 chunk: 8 KB bf16, 16 KB fp32).
+__device__ __forceinline__ void stage_final_t(uint8_t* stage, int r, const float (&v)[32], bool bf16) {
+  if (bf16) {
+    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) st[j * 128 + r] = __float2bfloat16_rn(v[j]);
+  } else {
+    float* st = reinterpret_cast<float*>(stage);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) st[j * 128 + r] = v[j];
+  }
+}
+// ... copied out by thread k of the half: stored rows n .. n + 31 (those below
+// l), columns mc .. mc + 127 (the 16-byte pieces below s).
+__device__ __forceinline__ void store_final_t(const NsMat& d, const NsBatch& p, const uint8_t* stage, int mc, int n,
+                                              int k) {
+  const int es = p.out_bf16 ? 2 : 4;
+  const int row_pieces = 128 * es / 16;                      // 16-byte pieces of one stored row's 128 columns
+  const int pieces = 32 * row_pieces;
+  for (int c = k; c < pieces; c += 128) {
+    const int j = c / row_pieces, col = (c - j * row_pieces) * (16 / es);
+    if (n + j >= d.l || mc + col >= d.s) continue;
+    const int64_t o = (int64_t)(n + j) * d.s + mc + col;
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(d.out) + o * es) =
+        *reinterpret_cast<const uint4*>(stage + (size_t)c * 16);
+  }
+}
+
 // Final update for 32 consecutive X columns [n, n+32) of X row m, in the
 // caller's layout: stored (m, n) when not transposed, (n, m) otherwise.
 __device__ __forceinline__ void store_final(const NsMat& d, const NsBatch& p, int m, int n, const float (&v)[32]) {
@@ -892,6 +929,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const size_t stride = colblock_stride(d.s_pad);
       const bool has_c = tl.c_in != nullptr;
       const bool final_out = tl.mode == kUpdateFinal || tl.mode == kFinalQ;
+      // a tall matrix's Gram-space final product (no epilogue input, so the
+      // stage is free) writes through the stage transposed
+      const bool final_t = tl.mode == kFinalQ && d.transposed && d.vec_ok && d.out != nullptr && d.w == nullptr;
       const int nblk = cw >> 6;                          // 64-column blocks of this half
       const size_t run_off = (size_t)(tl.mc >> 3) * 1024;   // the CTA's rows in a column block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
@@ -961,9 +1001,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
             }
           }
           const int n = nb + cb;
-          if (final_out) store_final(d, p, m, n, v);
-          else stage_chunk(stage, rrow, cb, v);
+          if (final_t) {
+            stage_final_t(stage, rrow, v, p.out_bf16 != 0);
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the chunk is staged
+            store_final_t(d, p, stage, tl.mc, n, k);
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // and copied out
+          } else if (final_out) {
+            store_final(d, p, m, n, v);
+          } else {
+            stage_chunk(stage, rrow, cb, v);
+          }
         }
+        if (!live) break;
         if (staged_out) {
           if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
           store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);

@@ -248,6 +248,40 @@ def test_ragged_shapes_odd_offsets(mfsdp, gdt):
         check_matrix(s, upd, mom, grad, mom0, ns_steps=5, zero=(s is zero))
 
 
+TALL_GRAM = [(1000, 200), (700, 136), (1544, 392), (1000, 130)]
+
+
+@pytest.mark.parametrize("udt", [torch.float32, torch.bfloat16])
+def test_tall_gram_space_final_store_paths(mfsdp, udt):
+    """Tall matrices in the Gram-space form (long side at least twice the short
+    one; ragged s and l) write their update through the epilogue's stage,
+    transposed, when the stored rows start 16-byte aligned, and element by
+    element otherwise (s = 130, or an offset that is not a multiple of 8).  Both
+    paths store the same values: the aligned set matches the oracle, and each
+    matrix run again at an odd offset gives the same bits."""
+    rng = np.random.default_rng(77)
+    shards, off = [], 0
+    for i, (r, c) in enumerate(TALL_GRAM):
+        shards.append(mfsdp.make_shard(off, r, c, param_id=i))
+        off += -(-(r * c) // 128) * 128
+    assert [g[0] for g in mfsdp.muon_gram_space_layout(shards, 5)] == [1, 1, 1, 1]
+    numel = off
+    vals = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
+    grad = W.f32_to_bf16_bits(vals)
+    mom0 = np.zeros(numel, np.float32)
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=udt)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=5)
+    for s in shards:
+        n = s.rows * s.cols
+        shifted = [mfsdp.make_shard(3, s.rows, s.cols, param_id=s.param_id)]
+        g1 = np.zeros(n + 3, grad.dtype)
+        g1[3:] = grad[s.offset:s.offset + n]
+        u1, _, _ = run_step(mfsdp, shifted, g1, np.zeros(n + 3, np.float32), update_dtype=udt)
+        a, b = upd[s.offset:s.offset + n], u1[3:]
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), f"{s.rows}x{s.cols}: store paths differ"
+
+
 def test_nesterov_and_second_step(mfsdp):
     w = W.get("gpt2_block")
     plan, r, shards, numel = owner_set(mfsdp, w)
