@@ -225,8 +225,8 @@ __device__ __forceinline__ void final_elem(const NsMat& d, const NsBatch& p, int
   }
 }
 
-// The Gram-space final product of a tall matrix (stored l x s, X = its
-// transpose) writes through the epilogue half's stage: each of the half's 128
+// The final update of a tall matrix (stored l x s, X = its transpose) writes
+// through the epilogue half's stage: each of the half's 128
 // threads holds X row m = mc + r for 32 consecutive X columns [n, n + 32),
 // i.e. one element of 32 consecutive stored rows, so the chunk is put into
 // the stage transposed (stored row j, then the 128 stored columns mc ..
@@ -929,9 +929,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const size_t stride = colblock_stride(d.s_pad);
       const bool has_c = tl.c_in != nullptr;
       const bool final_out = tl.mode == kUpdateFinal || tl.mode == kFinalQ;
-      // a tall matrix's Gram-space final product (no epilogue input, so the
-      // stage is free) writes through the stage transposed
-      const bool final_t = tl.mode == kFinalQ && d.transposed && d.vec_ok && d.out != nullptr && d.w == nullptr;
+      // a tall matrix's final update writes through the stage transposed (the
+      // standard form's epilogue input, X, is first read out of the stage
+      // into registers, block by block)
+      const bool final_t = final_out && d.transposed && d.vec_ok && d.out != nullptr && d.w == nullptr;
       const int nblk = cw >> 6;                          // 64-column blocks of this half
       const size_t run_off = (size_t)(tl.mc >> 3) * 1024;   // the CTA's rows in a column block
       // The epilogue input (A or X) does not depend on the accumulator: fetch
@@ -949,77 +950,118 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       const float scale_upd = (tl.first || tl.mode == kFinalQ) ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
       const int32_t code = wait_code(tl.phase, kRoleAccFull);
-      for (int blk = 0; blk < nblk && live; ++blk) {
-        const int nb = tl.n0 + c0 + 64 * blk;            // first column of this 64-column block
-        // Symmetric products write their tiles as they are: the blocks below
-        // the diagonal of 256 x 256 blocks are never stored (the products that
-        // read them read the stored blocks across it, transposed).
-        const bool staged_out = !final_out;
-        if (has_c) {
-          put_run(stage, k, pre);
-          if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the input block is staged
-          if (blk + 1 < nblk) load_run(tl.c_in + (size_t)((nb + 64) >> 6) * stride + run_off, k, pre);
-        }
-#pragma unroll 1
-        for (int hc = 0; hc < 2; ++hc) {
-          const int cb = 32 * hc;                        // columns [cb, cb + 32) of the block
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
-          ptx::tmem_ld_wait();
-          if (blk == nblk - 1 && hc == 1) {
-            // last accumulator read: hand it back to the MMA warp (the even
-            // CTA's barrier; the signal carries no data, see mbar_arrive_signal)
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_signal(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));
+      if (final_t) {
+        // A tall matrix's final update, through the stage transposed: per
+        // 64-column block, the epilogue input (X, standard form) is staged and
+        // each row's 64 values read back into registers; then per 32-column
+        // chunk the outputs are staged transposed and copied out.
+        for (int blk = 0; blk < nblk && live; ++blk) {
+          const int nb = tl.n0 + c0 + 64 * blk;          // first column of this 64-column block
+          if (has_c) {
+            if (blk > 0) load_run(tl.c_in + (size_t)(nb >> 6) * stride + run_off, k, pre);
+            put_run(stage, k, pre);
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the input block is staged
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              pre[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, 0, q));
+              pre[4 + q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, 32, q));
+            }
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the stage takes the outputs
           }
-          float v[32];
-          if (tl.mode == kGram) {
+#pragma unroll 1
+          for (int hc = 0; hc < 2; ++hc) {
+            const int cb = 32 * hc;                      // columns [cb, cb + 32) of the block
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
+            ptx::tmem_ld_wait();
+            if (blk == nblk - 1 && hc == 1) {
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive_signal(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));
+            }
+            float v[32];
+            if (has_c) {
+              uint4 xin[4];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
-          } else if (tl.mode == kFinalQ) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_upd;
-          } else {
-            uint4 xin[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
-            float x[32];
-            unpack_bf16x32(xin, x);
-            if (tl.mode == kPoly || tl.mode == kPolyI) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
-              if (tl.mode == kPolyI) {
-                // a I: the diagonal element of this row, if among these columns
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (nb + cb + j == m) v[j] += p.a;
-              }
-            } else {
+              for (int q = 0; q < 4; ++q) xin[q] = hc == 0 ? pre[q] : pre[4 + q];
+              float x[32];
+              unpack_bf16x32(xin, x);
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_upd;
             }
-          }
-          const int n = nb + cb;
-          if (final_t) {
             stage_final_t(stage, rrow, v, p.out_bf16 != 0);
             if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the chunk is staged
-            store_final_t(d, p, stage, tl.mc, n, k);
+            store_final_t(d, p, stage, tl.mc, nb + cb, k);
             if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // and copied out
-          } else if (final_out) {
-            store_final(d, p, m, n, v);
-          } else {
-            stage_chunk(stage, rrow, cb, v);
           }
         }
-        if (!live) break;
-        if (staged_out) {
-          if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
-          store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
+      } else {
+        for (int blk = 0; blk < nblk && live; ++blk) {
+          const int nb = tl.n0 + c0 + 64 * blk;            // first column of this 64-column block
+          // Symmetric products write their tiles as they are: the blocks below
+          // the diagonal of 256 x 256 blocks are never stored (the products that
+          // read them read the stored blocks across it, transposed).
+          const bool staged_out = !final_out;
+          if (has_c) {
+            put_run(stage, k, pre);
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the input block is staged
+            if (blk + 1 < nblk) load_run(tl.c_in + (size_t)((nb + 64) >> 6) * stride + run_off, k, pre);
+          }
+#pragma unroll 1
+          for (int hc = 0; hc < 2; ++hc) {
+            const int cb = 32 * hc;                        // columns [cb, cb + 32) of the block
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
+            ptx::tmem_ld_wait();
+            if (blk == nblk - 1 && hc == 1) {
+              // last accumulator read: hand it back to the MMA warp (the even
+              // CTA's barrier; the signal carries no data, see mbar_arrive_signal)
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive_signal(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));
+            }
+            float v[32];
+            if (tl.mode == kGram) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_gram;
+            } else if (tl.mode == kFinalQ) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_upd;
+            } else {
+              uint4 xin[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
+              float x[32];
+              unpack_bf16x32(xin, x);
+              if (tl.mode == kPoly || tl.mode == kPolyI) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(p.c, __uint_as_float(r[j]), p.b * x[j]);
+                if (tl.mode == kPolyI) {
+                  // a I: the diagonal element of this row, if among these columns
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (nb + cb + j == m) v[j] += p.a;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(p.a, x[j], __uint_as_float(r[j])) * scale_upd;
+              }
+            }
+            const int n = nb + cb;
+            if (final_out) store_final(d, p, m, n, v);
+            else stage_chunk(stage, rrow, cb, v);
+          }
+          if (staged_out) {
+            if (!half_sync(hbar, hphase, ab, code)) { live = false; break; }   // the output block is staged
+            store_run(static_cast<uint8_t*>(tl.out) + (size_t)(nb >> 6) * stride + run_off, stage, k);
+          }
+          // the stage is free again before anyone writes the next block into it
+          // (after the last block: once this warp's share is published)
+          if (blk + 1 < nblk && !half_sync(hbar, hphase, ab, code)) { live = false; break; }
         }
-        // the stage is free again before anyone writes the next block into it
-        // (after the last block: once this warp's share is published)
-        if (blk + 1 < nblk && !half_sync(hbar, hphase, ab, code)) { live = false; break; }
       }
       if (!live) break;
       ++acc_it;

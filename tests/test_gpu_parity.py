@@ -248,23 +248,25 @@ def test_ragged_shapes_odd_offsets(mfsdp, gdt):
         check_matrix(s, upd, mom, grad, mom0, ns_steps=5, zero=(s is zero))
 
 
-TALL_GRAM = [(1000, 200), (700, 136), (1544, 392), (1000, 130)]
+# tall shapes with ragged sides: four in the Gram-space form (long side at
+# least twice the short one), two in the standard form
+TALL = [(1000, 200), (700, 136), (1544, 392), (1000, 130), (1500, 1000), (1000, 520)]
 
 
 @pytest.mark.parametrize("udt", [torch.float32, torch.bfloat16])
-def test_tall_gram_space_final_store_paths(mfsdp, udt):
-    """Tall matrices in the Gram-space form (long side at least twice the short
-    one; ragged s and l) write their update through the epilogue's stage,
-    transposed, when the stored rows start 16-byte aligned, and element by
-    element otherwise (s = 130, or an offset that is not a multiple of 8).  Both
-    paths store the same values: the aligned set matches the oracle, and each
-    matrix run again at an odd offset gives the same bits."""
+def test_tall_final_store_paths(mfsdp, udt):
+    """Tall matrices write their update through the epilogue's stage,
+    transposed, when the stored rows start 16-byte aligned (offset and s
+    multiples of 8), and element by element otherwise (s = 130, or an offset
+    that is not a multiple of 8), in both forms of the iteration.  Both paths
+    store the same values: the aligned set matches the oracle, and each matrix
+    run again at an odd offset gives the same bits."""
     rng = np.random.default_rng(77)
     shards, off = [], 0
-    for i, (r, c) in enumerate(TALL_GRAM):
+    for i, (r, c) in enumerate(TALL):
         shards.append(mfsdp.make_shard(off, r, c, param_id=i))
         off += -(-(r * c) // 128) * 128
-    assert [g[0] for g in mfsdp.muon_gram_space_layout(shards, 5)] == [1, 1, 1, 1]
+    assert [g[0] for g in mfsdp.muon_gram_space_layout(shards, 5)] == [1, 1, 1, 1, 0, 0]
     numel = off
     vals = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
     grad = W.f32_to_bf16_bits(vals)
