@@ -940,12 +940,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
       // current one is processed.
       uint4 pre[kRunChunks];
       if (has_c) load_run(tl.c_in + (size_t)((tl.n0 + c0) >> 6) * stride + run_off, k, pre);
+      const float2 nrm = p.norm[d.norm_idx];             // read before the wait too: its latency hides under it
       const uint32_t a = acc_it & 1, ause = acc_it >> 1;
       const bool got = wait_or_abort(ptx::smem_u32(&tfull_bar[a]), ause & 1, ab,
                                      wait_code(tl.phase, kRoleAccFull));
       if (!__all_sync(0xffffffffu, got)) break;
       ptx::tc_fence_after();
-      const float2 nrm = p.norm[d.norm_idx];
       const float scale_gram = tl.first ? nrm.y * nrm.y : 1.0f;
       const float scale_upd = (tl.first || tl.mode == kFinalQ) ? nrm.y : 1.0f;
       const uint32_t t_row = tmem_base + a * kAccCols + ((uint32_t)(quad * 32) << 16);
@@ -1013,6 +1013,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
 #pragma unroll 1
           for (int hc = 0; hc < 2; ++hc) {
             const int cb = 32 * hc;                        // columns [cb, cb + 32) of the block
+            // this row's input chunk, read from the stage before the TMEM read
+            // so that the two latencies overlap
+            uint4 xin[4];
+            if (has_c) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
+            }
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
             ptx::tmem_ld_wait();
@@ -1031,9 +1038,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale_upd;
             } else {
-              uint4 xin[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) xin[q] = *reinterpret_cast<const uint4*>(stage + stage_off(rrow, cb, q));
               float x[32];
               unpack_bf16x32(xin, x);
               if (tl.mode == kPoly || tl.mode == kPolyI) {
