@@ -975,6 +975,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_kernel(const __grid_consta
             ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(nb - tl.n0 + cb), r);
             ptx::tmem_ld_wait();
             if (blk == nblk - 1 && hc == 1) {
+              // last accumulator read: hand it back to the MMA warp
               ptx::tc_fence_before();
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive_signal(ptx::mapa_shared(ptx::smem_u32(&tempty_bar[a]), 0));
