@@ -52,10 +52,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from an ncu capture of dram__bytes_read.sum + dram__bytes_write.sum, keyed
 # by a digest of the kernel's sources (ns_source_digest): a kernel changed
 # since its capture reports null traffic until it is captured again.
-NS_GEMM_TRAFFIC = {("5c1510c2a825ff62", "llama3_8b_rank"): 27.99e9, ("5c1510c2a825ff62", "llama_1p3b_rank"): 5.61e9}
+NS_GEMM_TRAFFIC = {("26400a1bdf0b290e", "llama3_8b_rank"): 28.58e9, ("26400a1bdf0b290e", "llama_1p3b_rank"): 5.48e9}
 # Share of the same launch's elapsed cycles with the tensor pipe active
 # (sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed), keyed alike.
-NS_TENSOR_ACTIVE = {("5c1510c2a825ff62", "llama3_8b_rank"): 0.9132, ("5c1510c2a825ff62", "llama_1p3b_rank"): 0.8347}
+NS_TENSOR_ACTIVE = {("26400a1bdf0b290e", "llama3_8b_rank"): 0.9134, ("26400a1bdf0b290e", "llama_1p3b_rank"): 0.8354}
 
 # The sources that make up the Newton-Schulz kernel.
 NS_SOURCES = ("ns_gemm.cu", "ptx.cuh", "mfsdp_internal.h")
