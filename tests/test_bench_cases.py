@@ -68,3 +68,14 @@ def test_figures_leave_zero_matrices_out(mfsdp):
     fig = bench.figures(mfsdp, step, ms, {"bf16_tflops_sustained": 1.0, "hbm_gbs": 1.0})
     assert (fig["flops_dense"], fig["flops_executed"]) == mfsdp.muon_step_flops(active, w.ns_steps)
     assert round(fig["flops_dense"] / 1e12, 2) == 29.22
+
+
+def test_ncu_figures_keyed_to_the_current_kernel():
+    """The DRAM traffic and tensor-pipe share the bench reports for the headline
+    owner set come from ncu captures of the kernel as committed: their key is
+    the digest of the current Newton-Schulz sources."""
+    digest = bench.ns_source_digest()
+    for name in ("llama3_8b_rank", "llama_1p3b_rank"):
+        assert (digest, name) in bench.NS_GEMM_TRAFFIC, name
+        assert (digest, name) in bench.NS_TENSOR_ACTIVE, name
+    assert all(0.0 < v <= 1.0 for v in bench.NS_TENSOR_ACTIVE.values())
