@@ -534,14 +534,12 @@ def run_ours(args):
     plan, sim_rank, shards, numel, tail_numel = owner_set(w, rank)
     supp_names = [] if (rank != 0 or args.no_supplementary) else [n for n in W.ORDER if n != w.name]
 
-    # Every gradient buffer is generated before the first CUDA call (a spawn pool).
+    # The headline's gradient buffer is generated before the first CUDA call
+    # (a spawn pool); the other owner sets' only after the headline's timed
+    # regions, so that no host memory but the headline's own is held while
+    # they run.
     t_gen = time.time()
     grad_np = W.owner_grad_buffer(w, shards, numel)
-    supp_inputs = {}
-    for name in supp_names:
-        ws_ = W.get(name)
-        _, _, sh, nm, tn = owner_set(ws_, 0)
-        supp_inputs[name] = (ws_, sh, nm, tn, W.owner_grad_buffer(ws_, sh, nm))
     t_gen = time.time() - t_gen
 
     import torch
@@ -555,6 +553,8 @@ def run_ours(args):
 
     # ---------------------------------------------------------- timed region
     step = OwnerStep(mfsdp, w, shards, numel, tail_numel, grad_np, dev, pin=True)
+    grad_bytes = grad_np.nbytes
+    del grad_np                                  # the step holds a pinned copy
     total_ms, phase_ms, steps_ms, clocks = time_resident(step, args.steps, args.warmup, ClockSampler(local_rank),
                                                          barrier)
     step_ms = max_over_ranks(total_ms / args.steps, dev)
@@ -587,13 +587,9 @@ def run_ours(args):
     # As many untimed warm-up steps as the device-resident measurement: with a
     # single one, the first timed step sometimes took ~200 ms more (a one-off
     # on the host-memory side) and dominated the mean.
-    e2e_sampler = ClockSampler(local_rank)      # clocks and throttle reasons of the e2e region too
-    e2e_sampler.start()
-    # nvidia-smi's own start-up (NVML initialisation) stalls this process's CUDA
-    # calls for tens of ms; the host-buffer step, which enqueues copies group by
-    # group, then shows 50-100 ms steps.  Let it finish first, as the resident
-    # region does.
-    time.sleep(0.6)
+    # No clock sampler runs in this region (nvidia-smi's polling is kept away
+    # from the host-buffer copies); the clocks of the resident region, just
+    # before, stand for the box.
     for _ in range(max(args.warmup, 1)):
         one_step_host()
     torch.cuda.synchronize()
@@ -617,7 +613,6 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     gc.enable()
-    e2e_clocks = e2e_sampler.stop()
     step.check_status("after the end-to-end region")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     e2e_steps_ms = [round(step_ev[k].elapsed_time(step_ev[k + 1]), 3) for k in range(e2e_steps)]
@@ -710,8 +705,11 @@ def run_ours(args):
         torch.cuda.empty_cache()
         sup["workloads"] = {}
         for name in supp_names:
-            ws_, sh, nm, tn, g_np = supp_inputs.pop(name)
+            ws_ = W.get(name)
+            _, _, sh, nm, tn = owner_set(ws_, 0)
+            g_np = W.owner_grad_buffer(ws_, sh, nm)      # a spawn pool: safe after CUDA work
             st_ = OwnerStep(mfsdp, ws_, sh, nm, tn, g_np, dev)
+            del g_np
             k = args.supp_steps
             tot, pms, sms, clk = time_resident(st_, k, max(args.warmup, 3), ClockSampler(local_rank))
             graph_ms = time_graph(st_, max(k, 10))
@@ -723,7 +721,7 @@ def run_ours(args):
                                       "steps": k, "matrices": len(sh), "elements": sum(s.rows * s.cols for s in sh),
                                       "tail_elems": tn, **fig,
                                       "sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons")}
-            del st_, g_np
+            del st_
             torch.cuda.empty_cache()
 
     # ---------------------------------------------------------- figures
@@ -759,7 +757,7 @@ def run_ours(args):
                    "matrices": len(shards), "elements": elems, "ns_steps": w.ns_steps,
                    "grad_dtype": w.grad_dtype, "update_dtype": "bf16", "tail_elems": tail_numel,
                    "grad_dist": w.grad_dist,
-                   "l2": f"no flush: inputs {(grad_np.nbytes + 4 * numel) / 1e9:.1f} GB > 129 MB L2",
+                   "l2": f"no flush: inputs {(grad_bytes + 4 * numel) / 1e9:.1f} GB > 129 MB L2",
                    "parallelism": f"owner sets x{world}"},
         "phases": phases,
         "roofline": {"kernel": "ns_kernel", "bound": "tensor", "achieved": ns_tflops_exec,
@@ -774,7 +772,8 @@ def run_ours(args):
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "api": "mfsdp_muon_owner_step_host",
                 "pipeline_groups": e2e_groups, "steps_ms": e2e_steps_ms, "host_enqueue_ms": host_ms,
-                "median_ms": round(statistics.median(e2e_steps_ms), 3), "clocks": e2e_clocks},
+                "median_ms": round(statistics.median(e2e_steps_ms), 3),
+                "clocks": "not sampled in this region (see the top-level clocks)"},
         "gpu_launches": step_launches(shards, tail_numel) * args.steps,
         "cpu_baseline": cpu,
         "supplementary": sup,

@@ -258,7 +258,8 @@ def owner_grad_buffer(w: Workload, shards, numel: int, workers: Optional[int] = 
     """Flat gradient buffer of one rank as stored (bf16 bits or fp32), each shard
     (objects with param_id, offset, rows, cols) filled with its seeded gradient;
     padding is zero.  Large owner sets are generated per matrix in a
-    spawn-started process pool -- call this before any CUDA work in the process."""
+    spawn-started process pool (spawned workers inherit no CUDA state, so the
+    call is safe before or after CUDA work in this process)."""
     dtype = np.uint16 if w.grad_dtype == "bf16" else np.float32
     buf = np.zeros(numel, dtype)
     jobs = [(w.name, s.param_id) for s in shards]
