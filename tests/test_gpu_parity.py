@@ -284,6 +284,31 @@ def test_tall_final_store_paths(mfsdp, udt):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), f"{s.rows}x{s.cols}: store paths differ"
 
 
+@pytest.mark.parametrize("ns_steps", [3, 4, 6])
+def test_gram_space_step_counts(mfsdp, ns_steps):
+    """Wide and tall shapes of the Gram-space form (ragged sides, aligned and
+    odd offsets) at the step counts the other tests do not run: 3 and 4 (the
+    form's null tiles -- no Q in the first iteration, no C in the last -- and
+    the Q ping-pong's parity) and 6 (past its bound: every matrix takes the
+    standard form).  A second step from non-zero momentum, fp32 gradients,
+    Nesterov, fp32 update, against the oracle."""
+    shapes = [(200, 640), (640, 200), (384, 1032), (1032, 384), (256, 896)]
+    rng = np.random.default_rng(ns_steps)
+    shards, off = [], 0
+    for i, (r, c) in enumerate(shapes):
+        off += 128 if i % 2 == 0 else 131
+        shards.append(mfsdp.make_shard(off, r, c, param_id=i))
+        off += r * c
+    want = [1 if ns_steps <= 5 else 0] * len(shapes)
+    assert [g[0] for g in mfsdp.muon_gram_space_layout(shards, ns_steps)] == want
+    numel = off + 7
+    grad = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
+    mom0 = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
+    upd, mom, _ = run_step(mfsdp, shards, grad, mom0, update_dtype=torch.float32, ns_steps=ns_steps, nesterov=True)
+    for s in shards:
+        check_matrix(s, upd, mom, grad, mom0, ns_steps=ns_steps, nesterov=True)
+
+
 def test_nesterov_and_second_step(mfsdp):
     w = W.get("gpt2_block")
     plan, r, shards, numel = owner_set(mfsdp, w)
