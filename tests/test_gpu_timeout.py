@@ -61,6 +61,38 @@ def test_bounded_wait_gives_up_and_reports(mfsdp):
         check_matrix(s, upd_np, mom_np, grad_np, np.zeros(numel, np.float32), ns_steps=w.ns_steps)
 
 
+def test_bounded_wait_in_a_gram_space_final_product(mfsdp):
+    """The same for a tile of the Gram-space form's final product Q X0 (list
+    position 3T): one 200 x 640 matrix runs 8 narrow tiles per iteration (A,
+    P, and C with Q, two 128-wide tiles each) and then its 5 final tiles, so
+    tile 40 is the first of those.  The wait that gives up records role 5 with
+    product 3T, or role 8 (no product); the next step is correct."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    shards = [mfsdp.make_shard(0, 200, 640)]
+    assert mfsdp.muon_gram_space_layout(shards, 5)[0][0] == 1
+    numel = 200 * 640
+    rng = np.random.default_rng(8)
+    grad_np = (rng.standard_normal(numel) * 1e-3).astype(np.float32)
+    grad = torch.from_numpy(grad_np).to(dev)
+    mom = torch.zeros(numel, dtype=torch.float32, device=dev)
+    upd = torch.zeros(numel, dtype=torch.float32, device=dev)
+    ws = torch.empty(mfsdp.muon_workspace_bytes(shards), dtype=torch.uint8, device=dev)
+
+    mfsdp.test_inject_stall(40)
+    t0 = time.monotonic()
+    mfsdp.muon_owner_step(shards, grad, mom, upd, ws, ns_steps=5, coeffs=W.NS_COEFFS, eps=W.NS_EPS)
+    st, detail = mfsdp.muon_device_status(ws)
+    waited = time.monotonic() - t0
+    assert st == mfsdp.ERR_DEVICE_TIMEOUT, (st, detail)
+    assert (detail & 0xFF, detail >> 8) in ((ROLE_DEPENDENCY, 15), (ROLE_TILE_FULL, 0)), detail
+    assert 1.5 < waited < 30.0, waited
+
+    upd_np, mom_np, _ = run_step(mfsdp, shards, grad_np, np.zeros(numel, np.float32), update_dtype=torch.float32)
+    check_matrix(shards[0], upd_np, mom_np, grad_np, np.zeros(numel, np.float32), ns_steps=5)
+
+
 def test_static_scratch_timeout_is_reported(mfsdp):
     """The static-scratch entry point keeps its status word in the library's
     scratch array, out of the caller's reach: a bounded wait that gives up
